@@ -1,0 +1,225 @@
+/*
+ * q4gemm: block-scaled 4-bit quantization and the GEMMs that consume it, for
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * Formats (all codes are packed two per byte: element 2j of a row in the low
+ * nibble of byte j, element 2j+1 in the high nibble):
+ *
+ *  NVFP4   E2M1 codes, one E4M3 scale per 16 elements along K, one FP32 scale
+ *          per tensor.  "Quantization in deployment" (anrans.github.io AI-infra
+ *          handbook), section "Fake quantization" (nvfp4, fp4) and the format
+ *          cheat sheet; "Quantization chains" (inferenceinterviews.com),
+ *          section "Bits per weight, scales included".
+ *  MXFP4   E2M1 codes, one E8M0 (power-of-two) scale per 32.  Same page,
+ *          "Fake quantization" (mxfp4).
+ *  INT4    symmetric integers in [-8, 7] (two's complement nibbles), one FP16
+ *          scale per 128.  "Low-bit inference for very large MoE", section
+ *          "Why quantization-aware training" (fake_int4), with the group of
+ *          128 and FP16 scale of "Quantization chains", "Bits per weight".
+ *
+ * The E2M1 code of a value y = clamp(x / S, -6, 6) is the nearest of
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6 with ties going to the smaller magnitude; its
+ * sign bit (bit 3) is set when x < 0.  Bit-exact definitions of every step
+ * are in the documentation of each call below.
+ *
+ * Conventions for every call:
+ *  - All data pointers are DEVICE pointers to caller-owned memory unless a
+ *    parameter says otherwise.  The library never allocates device memory;
+ *    calls that need scratch take a caller-provided workspace whose size is
+ *    given by q4_workspace_size().  Workspaces must be 256-byte aligned.
+ *  - Every call is asynchronous on the given CUDA stream (0 = legacy default
+ *    stream).  Argument errors are detected on the host and returned before
+ *    anything is launched.  Errors found by a kernel (a non-finite input, a
+ *    pipeline wait that timed out) are latched in a device status word and
+ *    returned by q4_sync_status().
+ *  - Matrices are row-major.  GEMMs compute C = A . B^T with A [M, K] and B
+ *    [N, K] (B is in the weight layout).
+ *  - Block-scale tensors exist in two layouts:
+ *      Q4_SCALES_ROWMAJOR  [rows, K / block], one byte per block;
+ *      Q4_SCALES_MMA       the tensor-core layout: rows are grouped by 128
+ *                          and scale columns by 4; the 512-byte tile of
+ *                          row group R and column group J starts at
+ *                          (R * ceil(nsf / 4) + J) * 512 and holds the scale
+ *                          of row r, column s at
+ *                          (r % 32) * 16 + ((r % 128) / 32) * 4 + s % 4.
+ *                          Its size is ceil(rows / 128) * 128 * ceil(nsf / 4)
+ *                          * 4 bytes (nsf = K / block); padding is zero.
+ */
+#ifndef Q4GEMM_H_
+#define Q4GEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* q4_stream_t; /* the same type as cudaStream_t */
+
+typedef int q4_status;
+#define Q4_OK 0
+#define Q4_ERR_INVALID_ARG (-1)       /* null pointer, negative size, bad enum, misalignment */
+#define Q4_ERR_UNSUPPORTED_SHAPE (-2) /* K not a multiple of the required block, sizes too large */
+#define Q4_ERR_CUDA (-3)              /* a CUDA runtime or driver call failed */
+#define Q4_ERR_TIMEOUT (-4)           /* a kernel's bounded pipeline wait ran out */
+#define Q4_ERR_NONFINITE (-5)         /* a quantizer saw a NaN or infinite input */
+#define Q4_ERR_WORKSPACE (-6)         /* workspace missing, too small or misaligned */
+
+typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
+typedef enum { Q4_SCALES_ROWMAJOR = 0, Q4_SCALES_MMA = 1 } q4_scale_layout;
+
+/* Operation codes for q4_workspace_size(). */
+typedef enum {
+  Q4_OP_QUANTIZE_NVFP4 = 0,
+  Q4_OP_GEMM_W4A4_NVFP4 = 1, /* M, N, K; both operands given raw (the largest case) */
+  Q4_OP_GEMM_W4A4_MXFP4 = 2,
+  Q4_OP_GEMM_W4A16_INT4 = 3,
+  Q4_OP_GROUPED_GEMM_MOE = 4 /* M = number of tokens T, N, K; E and R via q4_workspace_size_moe */
+} q4_op;
+
+/*
+ * One FP4 GEMM operand [rows, K].
+ *  raw != NULL: the operand is given unquantized ([rows, K] in raw_dtype) and
+ *               the GEMM call quantizes it into the workspace first (NVFP4:
+ *               with its own per-tensor scale).  codes/scales/tensor_scale
+ *               are then ignored.
+ *  raw == NULL: codes [rows, K/2], scales in scale_layout and (NVFP4 only)
+ *               tensor_scale, a device pointer to one float, as written by
+ *               quantize_nvfp4 / quantize_mxfp4.
+ */
+typedef struct {
+  const void* raw;
+  int raw_dtype; /* q4_dtype */
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int scale_layout; /* q4_scale_layout */
+  const float* tensor_scale;
+} q4_operand;
+
+/* Bytes of workspace the operation needs for these sizes (0 if none). */
+size_t q4_workspace_size(int op, int64_t M, int64_t N, int64_t K);
+size_t q4_workspace_size_moe(int64_t T, int64_t N, int64_t K, int E, int64_t R);
+
+/* Size in bytes of a Q4_SCALES_MMA scale tensor for rows x nsf scales. */
+size_t q4_mma_scales_bytes(int64_t rows, int64_t nsf);
+
+/*
+ * NVFP4 quantization of x [rows, K] (K % 16 == 0), "Quantization in
+ * deployment", "Fake quantization" (nvfp4 then fp4).  In float32 with IEEE
+ * rounding:
+ *   g  = max(max|x|, 1e-12) / 2688                     (written to *tensor_scale)
+ *   per block of 16 along K:
+ *     t  = (amax_b / 6) / g;  bs = E4M3(t), round to nearest even
+ *     S  = max(e4m3(bs), 1e-12) * g
+ *     code = E2M1(clamp(x / S, -6, 6))   (ties to the smaller magnitude)
+ *   a block whose scale byte is 0 gets all-zero codes.
+ * codes: [rows, K/2]; scales: E4M3 bytes in scale_layout; tensor_scale: one
+ * device float.  ws: q4_workspace_size(Q4_OP_QUANTIZE_NVFP4, rows, 0, K)
+ * bytes (the amax accumulator).  Two kernels are launched (amax, quantize).
+ */
+q4_status quantize_nvfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                         uint8_t* scales, int scale_layout, float* tensor_scale, void* ws,
+                         size_t ws_bytes, q4_stream_t stream);
+
+/*
+ * MXFP4 quantization of x [rows, K] (K % 32 == 0), "Quantization in
+ * deployment", "Fake quantization" (mxfp4).  Per block of 32:
+ *   e = floor(log2(max(amax_b, 1e-12))) - 2  (exact, from the float bits)
+ *   scale byte = e + 127 (E8M0);  code = E2M1(clamp(x / 2^e, -6, 6)).
+ */
+q4_status quantize_mxfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                         uint8_t* scales, int scale_layout, q4_stream_t stream);
+
+/*
+ * Symmetric INT4 quantization with one FP16 scale per 128 (K % 128 == 0),
+ * "Low-bit inference for very large MoE", "Why quantization-aware training"
+ * (fake_int4) with groups of 128:
+ *   s16 = fp16_rne(amax_g / 7);  q = clamp(rint(x / float(s16)), -8, 7)
+ *   (q = 0 where s16 == 0).  codes [rows, K/2]; scales [rows, K/128] FP16 bits.
+ */
+q4_status quantize_int4_g128(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                             uint16_t* scales, q4_stream_t stream);
+
+/*
+ * Scale re-layout: src [rows, nsf] row-major bytes -> dst in Q4_SCALES_MMA
+ * layout (q4_mma_scales_bytes(rows, nsf) bytes, padding zeroed).  No page
+ * prints this layout; it is the order in which the GB300 tensor cores read
+ * block scales.
+ */
+q4_status q4_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, uint8_t* dst,
+                           q4_stream_t stream);
+
+/*
+ * W4A4 GEMMs on the FP4 tensor cores ("Low-bit inference for very large
+ * MoE", "Kernels on different hardware": activations quantized to FP4 too,
+ * both operands enter the FP4 tensor cores).  C [M, N] = A_hat . B_hat^T
+ * with FP32 accumulation, where
+ *   NVFP4: x_hat = e2m1(code) * e4m3(scale) * g   (the product of the two
+ *          tensor scales gA * gB is applied in the FP32 epilogue)
+ *   MXFP4: x_hat = e2m1(code) * 2^(scale - 127)
+ * c_dtype is Q4_F32 or Q4_BF16 (round to nearest even).  K % 256 == 0; M and
+ * N are arbitrary (M, N >= 0).  Raw operands are quantized on the fly (see
+ * q4_operand).  ws: q4_workspace_size(op, M, N, K) bytes.
+ */
+q4_status gemm_w4a4_nvfp4(const q4_operand* A, const q4_operand* B, int64_t M, int64_t N,
+                          int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,
+                          q4_stream_t stream);
+q4_status gemm_w4a4_mxfp4(const q4_operand* A, const q4_operand* B, int64_t M, int64_t N,
+                          int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,
+                          q4_stream_t stream);
+
+/*
+ * W4A16 decode GEMM ("Low-bit inference for very large MoE", "Kernels on
+ * different hardware", W4A16 row: weights stay 4-bit in memory, activations
+ * bf16; decode is bound by weight reads):
+ *   C[m, n] = sum_g s16[n, g] * sum_{k in g} a[m, k] * q[n, k]
+ * A_bf16 [M, K]; Wq [N, K/2] INT4 codes; Ws [N, K/128] FP16 bits (as written
+ * by quantize_int4_g128); C_bf16 [M, N].  FP32 accumulation, one FP32
+ * multiply by the scale per group of 128.  K % 128 == 0; any M >= 0 (tuned
+ * for M <= 16).  Needs no workspace (ws may be NULL).
+ */
+q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t* Ws, int64_t M,
+                          int64_t N, int64_t K, void* C_bf16, void* ws, size_t ws_bytes,
+                          q4_stream_t stream);
+
+/*
+ * Grouped routed-MoE NVFP4 GEMM ("Low-bit inference for very large MoE",
+ * "Kernels on different hardware": one low-bit weight matrix per expert,
+ * grouped by routing).  The T tokens [T, K] bf16 are NVFP4-quantized once as
+ * one tensor (one per-tensor scale), then for every expert e
+ *   C[r, :] = A_hat[row_token[r], :] . W_hat_e^T   for r in
+ *   [expert_offsets[e], expert_offsets[e+1])
+ * expert_offsets: device int32 [E+1], non-decreasing, expert_offsets[0] = 0,
+ * expert_offsets[E] = R.  row_token: device int32 [R], values in [0, T).
+ * W_codes: [E, N, K/2]; W_scales: E consecutive Q4_SCALES_MMA tensors of
+ * q4_mma_scales_bytes(N, K/16) bytes; W_tensor_scales: device float [E].
+ * C_bf16: [R, N].  K % 256 == 0.  An expert with no rows is legal.
+ * ws: q4_workspace_size_moe(T, N, K, E, R) bytes.
+ */
+q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
+                           const int32_t* expert_offsets, const int32_t* row_token, int64_t R,
+                           int E, const uint8_t* W_codes, const uint8_t* W_scales,
+                           const float* W_tensor_scales, int64_t N, void* C_bf16, void* ws,
+                           size_t ws_bytes, q4_stream_t stream);
+
+/*
+ * Synchronizes the stream, then returns (and clears) the first error a kernel
+ * latched since the last call: Q4_OK, Q4_ERR_TIMEOUT or Q4_ERR_NONFINITE; or
+ * Q4_ERR_CUDA if the synchronization itself failed.
+ */
+q4_status q4_sync_status(q4_stream_t stream);
+
+/* Static description of a status code. */
+const char* q4_status_string(q4_status s);
+
+/* Upper bound, in milliseconds, of every bounded wait inside the kernels
+ * (default 2000).  Returns the previous value.  Host-side setting, read at
+ * launch. */
+int q4_set_wait_timeout_ms(int ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4GEMM_H_ */

@@ -1,0 +1,259 @@
+"""Python binding of the q4gemm C ABI (``include/q4gemm.h``).
+
+Argument marshalling only: tensors are passed by ``data_ptr()`` together with
+torch's current CUDA stream, and every step runs in the library's kernels.
+PyTorch provides device memory (outputs and workspaces are torch tensors
+allocated here, on the caller's side of the ABI) and streams.  There is no
+fallback: if ``libq4gemm.so`` is missing or a call fails, an exception is
+raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Union
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libq4gemm.so")
+
+Q4_OK = 0
+F32, BF16, F16 = 0, 1, 2
+ROWMAJOR, MMA = 0, 1
+OP_QUANTIZE_NVFP4, OP_GEMM_W4A4_NVFP4, OP_GEMM_W4A4_MXFP4, OP_GEMM_W4A16_INT4 = 0, 1, 2, 3
+
+_DTYPE = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+_LAYOUT = {"rowmajor": ROWMAJOR, "mma": MMA}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _lib.q4_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+
+
+class _Operand(ctypes.Structure):
+    _fields_ = [("raw", ctypes.c_void_p), ("raw_dtype", ctypes.c_int),
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("scale_layout", ctypes.c_int), ("tensor_scale", ctypes.c_void_p)]
+
+
+def _sig(lib, name, restype, *argtypes):
+    f = getattr(lib, name)
+    f.restype = restype
+    f.argtypes = list(argtypes)
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (built by ``__graft_entry__.build()`` or
+    ``python -m int4_gemm_gb300.build``).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m int4_gemm_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    _sig(lib, "q4_workspace_size", SZ, I, I64, I64, I64)
+    _sig(lib, "q4_workspace_size_moe", SZ, I64, I64, I64, I, I64)
+    _sig(lib, "q4_mma_scales_bytes", SZ, I64, I64)
+    _sig(lib, "quantize_nvfp4", I, P, I, I64, I64, P, P, I, P, P, SZ, P)
+    _sig(lib, "quantize_mxfp4", I, P, I, I64, I64, P, P, I, P)
+    _sig(lib, "quantize_int4_g128", I, P, I, I64, I64, P, P, P)
+    _sig(lib, "q4_scales_to_mma", I, P, I64, I64, P, P)
+    op = ctypes.POINTER(_Operand)
+    _sig(lib, "gemm_w4a4_nvfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
+    _sig(lib, "gemm_w4a4_mxfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
+    _sig(lib, "gemm_w4a16_int4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
+    _sig(lib, "grouped_gemm_moe", I, P, I64, I64, P, P, I64, I, P, P, P, I64, P, P, SZ, P)
+    _sig(lib, "q4_sync_status", I, P)
+    _sig(lib, "q4_status_string", ctypes.c_char_p, I)
+    _sig(lib, "q4_set_wait_timeout_ms", I, I)
+    _lib = lib
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+def _check(fn: str, status: int):
+    if status != Q4_OK:
+        raise Q4Error(fn, status)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _cuda2d(x: torch.Tensor, name: str) -> torch.Tensor:
+    if not x.is_cuda or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D CUDA tensor")
+    return x
+
+
+def _empty(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 0), dtype=torch.uint8, device=device)
+
+
+def workspace(op: int, M: int, N: int, K: int, device) -> torch.Tensor:
+    n = lib().q4_workspace_size(op, M, N, K)
+    return _empty(max(n, 256), device)
+
+
+def mma_scales_bytes(rows: int, nsf: int) -> int:
+    return int(lib().q4_mma_scales_bytes(rows, nsf))
+
+
+# --------------------------------------------------------------------------- quantizers
+
+def quantize_nvfp4(x: torch.Tensor, scale_layout: str = "rowmajor", stream=None):
+    """-> (codes u8 [rows, K/2], scales u8, tensor_scale f32 [1])."""
+    _cuda2d(x, "x")
+    rows, K = x.shape
+    dev = x.device
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    lay = _LAYOUT[scale_layout]
+    if lay == ROWMAJOR:
+        scales = torch.empty((rows, K // 16), dtype=torch.uint8, device=dev)
+    else:
+        scales = _empty(mma_scales_bytes(rows, K // 16), dev)
+    ts = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = workspace(OP_QUANTIZE_NVFP4, rows, 0, K, dev)
+    _check("quantize_nvfp4", lib().quantize_nvfp4(
+        x.data_ptr(), _DTYPE[x.dtype], rows, K, codes.data_ptr(), scales.data_ptr(), lay,
+        ts.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return codes, scales, ts
+
+
+def quantize_mxfp4(x: torch.Tensor, scale_layout: str = "rowmajor", stream=None):
+    """-> (codes u8 [rows, K/2], scales u8)."""
+    _cuda2d(x, "x")
+    rows, K = x.shape
+    dev = x.device
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    lay = _LAYOUT[scale_layout]
+    if lay == ROWMAJOR:
+        scales = torch.empty((rows, K // 32), dtype=torch.uint8, device=dev)
+    else:
+        scales = _empty(mma_scales_bytes(rows, K // 32), dev)
+    _check("quantize_mxfp4", lib().quantize_mxfp4(
+        x.data_ptr(), _DTYPE[x.dtype], rows, K, codes.data_ptr(), scales.data_ptr(), lay,
+        _stream(stream)))
+    return codes, scales
+
+
+def quantize_int4_g128(x: torch.Tensor, stream=None):
+    """-> (codes u8 [rows, K/2], scales int16 [rows, K/128] holding FP16 bits)."""
+    _cuda2d(x, "x")
+    rows, K = x.shape
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((rows, K // 128), dtype=torch.int16, device=x.device)
+    _check("quantize_int4_g128", lib().quantize_int4_g128(
+        x.data_ptr(), _DTYPE[x.dtype], rows, K, codes.data_ptr(), scales.data_ptr(),
+        _stream(stream)))
+    return codes, scales
+
+
+def scales_to_mma(src: torch.Tensor, stream=None) -> torch.Tensor:
+    _cuda2d(src, "src")
+    rows, nsf = src.shape
+    dst = _empty(mma_scales_bytes(rows, nsf), src.device)
+    _check("q4_scales_to_mma", lib().q4_scales_to_mma(src.data_ptr(), rows, nsf, dst.data_ptr(),
+                                                      _stream(stream)))
+    return dst
+
+
+# --------------------------------------------------------------------------- GEMMs
+
+@dataclass
+class Fp4Operand:
+    """A quantized FP4 operand as returned by quantize_nvfp4 / quantize_mxfp4."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    scale_layout: str = "rowmajor"
+    tensor_scale: Optional[torch.Tensor] = None
+
+
+def _operand(x: Union[torch.Tensor, Fp4Operand]) -> tuple[_Operand, int]:
+    if isinstance(x, Fp4Operand):
+        return _Operand(None, 0, x.codes.data_ptr(), x.scales.data_ptr(), _LAYOUT[x.scale_layout],
+                        _ptr(x.tensor_scale)), x.codes.shape[0]
+    _cuda2d(x, "operand")
+    return _Operand(x.data_ptr(), _DTYPE[x.dtype], None, None, 0, None), x.shape[0]
+
+
+def _gemm_fp4(fn: str, op: int, A, B, K: int, out_dtype: torch.dtype, stream=None) -> torch.Tensor:
+    a, M = _operand(A)
+    b, N = _operand(B)
+    dev = (A.codes if isinstance(A, Fp4Operand) else A).device
+    C = torch.empty((M, N), dtype=out_dtype, device=dev)
+    ws = workspace(op, M, N, K, dev)
+    _check(fn, getattr(lib(), fn)(ctypes.byref(a), ctypes.byref(b), M, N, K, C.data_ptr(),
+                                  _DTYPE[out_dtype], ws.data_ptr(), ws.numel(), _stream(stream)))
+    return C
+
+
+def gemm_w4a4_nvfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """C = A_hat . B_hat^T; A and B are raw tensors (quantized on the fly) or
+    Fp4Operand."""
+    return _gemm_fp4("gemm_w4a4_nvfp4", OP_GEMM_W4A4_NVFP4, A, B, K, out_dtype, stream)
+
+
+def gemm_w4a4_mxfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    return _gemm_fp4("gemm_w4a4_mxfp4", OP_GEMM_W4A4_MXFP4, A, B, K, out_dtype, stream)
+
+
+def gemm_w4a16_int4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=None,
+                    stream=None) -> torch.Tensor:
+    """C [M, N] bf16 = A [M, K] bf16 . dequant(Wq, Ws)^T."""
+    _cuda2d(A, "A")
+    M, K = A.shape
+    N = Wq.shape[0]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    _check("gemm_w4a16_int4", lib().gemm_w4a16_int4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(), M,
+                                                     N, K, C.data_ptr(), None, 0, _stream(stream)))
+    return C
+
+
+def moe_workspace(T: int, N: int, K: int, E: int, R: int, device) -> torch.Tensor:
+    return _empty(max(int(lib().q4_workspace_size_moe(T, N, K, E, R)), 256), device)
+
+
+def grouped_gemm_moe(tokens: torch.Tensor, expert_offsets: torch.Tensor, row_token: torch.Tensor,
+                     w_codes: torch.Tensor, w_scales: torch.Tensor, w_tensor_scales: torch.Tensor,
+                     N: int, ws: Optional[torch.Tensor] = None, out=None, stream=None) -> torch.Tensor:
+    """C [R, N] bf16: routed rows times their expert's NVFP4 weights.
+    w_codes [E, N, K/2]; w_scales: E stacked MMA-layout scale tensors;
+    w_tensor_scales [E] float32; expert_offsets [E+1] / row_token [R] int32."""
+    _cuda2d(tokens, "tokens")
+    T, K = tokens.shape
+    E = expert_offsets.numel() - 1
+    R = row_token.numel()
+    C = torch.empty((R, N), dtype=torch.bfloat16, device=tokens.device) if out is None else out
+    if ws is None:
+        ws = moe_workspace(T, N, K, E, R, tokens.device)
+    _check("grouped_gemm_moe", lib().grouped_gemm_moe(
+        tokens.data_ptr(), T, K, expert_offsets.data_ptr(), row_token.data_ptr(), R, E,
+        w_codes.data_ptr(), w_scales.data_ptr(), w_tensor_scales.data_ptr(), N, C.data_ptr(),
+        ws.data_ptr(), ws.numel(), _stream(stream)))
+    return C
+
+
+def sync_status(stream=None) -> int:
+    """Synchronize and return (and clear) the first error latched by a kernel."""
+    return int(lib().q4_sync_status(_stream(stream)))
+
+
+def set_wait_timeout_ms(ms: int) -> int:
+    return int(lib().q4_set_wait_timeout_ms(ms))

@@ -1,0 +1,418 @@
+// The C ABI of q4gemm (declared in include/q4gemm.h): host-side argument
+// checks, workspace carving, dispatch to the kernels, the device status word
+// and TMA descriptor creation.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace q4 {
+
+// First error latched by any kernel on this device (0 = none).
+__device__ int g_q4_status = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_wait_ms{2000};
+int* g_status_ptr[kMaxDevices] = {nullptr};
+int g_sms[kMaxDevices] = {0};
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Sequential carving of a caller-provided workspace.
+struct Carver {
+  uint8_t* base;
+  size_t cap, used;
+  uint8_t* take(size_t bytes) {
+    uint8_t* p = base ? base + used : nullptr;
+    used += align256(bytes);
+    return p;
+  }
+  bool ok() const { return used <= cap; }
+};
+
+bool valid_dtype(int d) { return d == Q4_F32 || d == Q4_BF16 || d == Q4_F16; }
+size_t dtype_size(int d) { return d == Q4_F32 ? 4 : 2; }
+}  // namespace
+
+int* device_status_ptr() {
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  if (!g_status_ptr[d]) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_q4_status) != cudaSuccess) return nullptr;
+    g_status_ptr[d] = static_cast<int*>(p);
+  }
+  return g_status_ptr[d];
+}
+
+unsigned long long wait_budget_ns() { return (unsigned long long)g_wait_ms.load() * 1000000ull; }
+
+int num_sms() {
+  const int d = current_device();
+  if (d < 0) return 1;
+  if (!g_sms[d]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = n > 0 ? n : 1;
+  }
+  return g_sms[d];
+}
+
+q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                          bool swizzle128) {
+  if (!g_encode) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return Q4_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t dims[2] = {inner_bytes, rows};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? Q4_OK : Q4_ERR_CUDA;
+}
+
+namespace {
+
+// Workspace plan of one FP4 GEMM operand given raw or with row-major scales.
+struct OperandPlan {
+  uint8_t* codes;
+  uint8_t* sf;
+  unsigned* amax;
+  float* g;
+};
+
+OperandPlan plan_operand(Carver& c, int64_t rows, int64_t K, int block, bool nv) {
+  OperandPlan pl;
+  pl.codes = c.take((size_t)rows * (size_t)(K / 2));
+  pl.sf = c.take(mma_scales_bytes(rows, K / block));
+  uint8_t* small = c.take(256);
+  pl.amax = reinterpret_cast<unsigned*>(small);
+  pl.g = reinterpret_cast<float*>(small + 16);
+  (void)nv;
+  return pl;
+}
+
+q4_status check_operand(const q4_operand* op, int64_t rows, bool nv) {
+  if (!op) return Q4_ERR_INVALID_ARG;
+  if (rows == 0) return Q4_OK;
+  if (op->raw) {
+    if (!valid_dtype(op->raw_dtype) || !aligned(op->raw, 16)) return Q4_ERR_INVALID_ARG;
+    return Q4_OK;
+  }
+  if (!op->codes || !op->scales || !aligned(op->codes, 16) || !aligned(op->scales, 16))
+    return Q4_ERR_INVALID_ARG;
+  if (op->scale_layout != Q4_SCALES_ROWMAJOR && op->scale_layout != Q4_SCALES_MMA)
+    return Q4_ERR_INVALID_ARG;
+  if (nv && !op->tensor_scale) return Q4_ERR_INVALID_ARG;
+  return Q4_OK;
+}
+
+// Bring an operand into (codes, MMA-layout scales, tensor scale) form.
+q4_status resolve_operand(const q4_operand* op, int64_t rows, int64_t K, bool nv,
+                          const OperandPlan& pl, cudaStream_t s, const uint8_t** codes,
+                          const uint8_t** sf, const float** g) {
+  const int block = nv ? 16 : 32;
+  if (rows == 0) {
+    *codes = op->codes; *sf = op->scales; *g = op->tensor_scale;
+    return Q4_OK;
+  }
+  q4_status st;
+  if (op->raw) {
+    if (nv) {
+      Q4_CUDA_TRY(cudaMemsetAsync(pl.amax, 0, sizeof(unsigned), s));
+      if ((st = launch_amax(op->raw, op->raw_dtype, rows * K, pl.amax, s)) != Q4_OK) return st;
+      if ((st = launch_quant_nvfp4(op->raw, op->raw_dtype, rows, K, pl.codes, pl.sf, Q4_SCALES_MMA,
+                                   pl.amax, pl.g, s)) != Q4_OK)
+        return st;
+      *g = pl.g;
+    } else {
+      if ((st = launch_quant_mxfp4(op->raw, op->raw_dtype, rows, K, pl.codes, pl.sf, Q4_SCALES_MMA,
+                                   s)) != Q4_OK)
+        return st;
+      *g = nullptr;
+    }
+    *codes = pl.codes;
+    *sf = pl.sf;
+    return Q4_OK;
+  }
+  *codes = op->codes;
+  *g = nv ? op->tensor_scale : nullptr;
+  if (op->scale_layout == Q4_SCALES_MMA) {
+    *sf = op->scales;
+    return Q4_OK;
+  }
+  if ((st = launch_scales_to_mma(op->scales, rows, K / block, pl.sf, s)) != Q4_OK) return st;
+  *sf = pl.sf;
+  return Q4_OK;
+}
+
+size_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K, int block) {
+  Carver c{nullptr, 0, 0};
+  plan_operand(c, M, K, block, block == 16);
+  plan_operand(c, N, K, block, block == 16);
+  return c.used;
+}
+
+struct MoePlan {
+  uint8_t* tok_codes;
+  uint8_t* tok_sf;
+  unsigned* amax;
+  float* g;
+  int32_t* sched;
+  uint8_t* routed_sf;
+  int64_t cap_rows;
+};
+
+MoePlan plan_moe(Carver& c, int64_t T, int64_t K, int E, int64_t R) {
+  MoePlan pl;
+  pl.tok_codes = c.take((size_t)T * (size_t)(K / 2));
+  pl.tok_sf = c.take((size_t)T * (size_t)(K / 16));
+  uint8_t* small = c.take(256);
+  pl.amax = reinterpret_cast<unsigned*>(small);
+  pl.g = reinterpret_cast<float*>(small + 16);
+  pl.sched = reinterpret_cast<int32_t*>(c.take((size_t)(E + 1) * 4));
+  pl.cap_rows = (ceil_div(R, 128) + E) * 128;
+  pl.routed_sf = c.take(mma_scales_bytes(pl.cap_rows, K / 16));
+  return pl;
+}
+
+q4_status gemm_fp4_common(bool nv, const q4_operand* A, const q4_operand* B, int64_t M, int64_t N,
+                          int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,
+                          q4_stream_t stream) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M < 0 || N < 0 || K <= 0) return Q4_ERR_INVALID_ARG;
+  if (K % 256) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (c_dtype != Q4_F32 && c_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
+  q4_status st;
+  if ((st = check_operand(A, M, nv)) != Q4_OK) return st;
+  if ((st = check_operand(B, N, nv)) != Q4_OK) return st;
+  if (M == 0 || N == 0) return Q4_OK;
+  if (!C || !aligned(C, 16)) return Q4_ERR_INVALID_ARG;
+  const int block = nv ? 16 : 32;
+  const bool need_ws = A->raw || B->raw || A->scale_layout == Q4_SCALES_ROWMAJOR ||
+                       B->scale_layout == Q4_SCALES_ROWMAJOR;
+  Carver c{static_cast<uint8_t*>(ws), ws_bytes, 0};
+  const OperandPlan pa = plan_operand(c, M, K, block, nv);
+  const OperandPlan pb = plan_operand(c, N, K, block, nv);
+  if (need_ws && (!ws || !aligned(ws, 256) || !c.ok())) return Q4_ERR_WORKSPACE;
+  Fp4GemmArgs g = {};
+  if ((st = resolve_operand(A, M, K, nv, pa, s, &g.a_codes, &g.a_scales, &g.a_g)) != Q4_OK) return st;
+  if ((st = resolve_operand(B, N, K, nv, pb, s, &g.b_codes, &g.b_scales, &g.b_g)) != Q4_OK) return st;
+  g.M = M; g.N = N; g.K = K; g.C = C; g.c_dtype = c_dtype; g.nvfp4 = nv;
+  return launch_fp4_gemm(g, s);
+}
+
+}  // namespace
+}  // namespace q4
+
+using namespace q4;
+
+extern "C" {
+
+size_t q4_mma_scales_bytes(int64_t rows, int64_t nsf) {
+  if (rows < 0 || nsf < 0) return 0;
+  return mma_scales_bytes(rows, nsf);
+}
+
+size_t q4_workspace_size(int op, int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  switch (op) {
+    case Q4_OP_QUANTIZE_NVFP4: return 256;
+    case Q4_OP_GEMM_W4A4_NVFP4: return gemm_ws_bytes(M, N, K, 16);
+    case Q4_OP_GEMM_W4A4_MXFP4: return gemm_ws_bytes(M, N, K, 32);
+    case Q4_OP_GEMM_W4A16_INT4: return 0;
+    case Q4_OP_GROUPED_GEMM_MOE: return 0;  // needs E and R: q4_workspace_size_moe
+    default: return 0;
+  }
+}
+
+size_t q4_workspace_size_moe(int64_t T, int64_t N, int64_t K, int E, int64_t R) {
+  (void)N;
+  if (T < 0 || K < 0 || E < 0 || R < 0) return 0;
+  Carver c{nullptr, 0, 0};
+  plan_moe(c, T, K, E, R);
+  return c.used;
+}
+
+q4_status quantize_nvfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                         uint8_t* scales, int scale_layout, float* tensor_scale, void* ws,
+                         size_t ws_bytes, q4_stream_t stream) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rows < 0 || K <= 0 || !valid_dtype(x_dtype)) return Q4_ERR_INVALID_ARG;
+  if (K % 16) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (scale_layout != Q4_SCALES_ROWMAJOR && scale_layout != Q4_SCALES_MMA) return Q4_ERR_INVALID_ARG;
+  if (!tensor_scale) return Q4_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < 256 || !aligned(ws, 256)) return Q4_ERR_WORKSPACE;
+  if (rows > 0 && (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16)))
+    return Q4_ERR_INVALID_ARG;
+  unsigned* amax = static_cast<unsigned*>(ws);
+  Q4_CUDA_TRY(cudaMemsetAsync(amax, 0, sizeof(unsigned), s));
+  q4_status st;
+  if (rows == 0) {
+    // g of an empty tensor: max(0, 1e-12) / 2688
+    const float g = 1e-12f / 2688.0f;
+    Q4_CUDA_TRY(cudaMemcpyAsync(tensor_scale, &g, sizeof(float), cudaMemcpyHostToDevice, s));
+    Q4_CUDA_TRY(cudaStreamSynchronize(s));
+    return Q4_OK;
+  }
+  if ((st = launch_amax(x, x_dtype, rows * K, amax, s)) != Q4_OK) return st;
+  return launch_quant_nvfp4(x, x_dtype, rows, K, codes, scales, scale_layout, amax, tensor_scale, s);
+}
+
+q4_status quantize_mxfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                         uint8_t* scales, int scale_layout, q4_stream_t stream) {
+  if (rows < 0 || K <= 0 || !valid_dtype(x_dtype)) return Q4_ERR_INVALID_ARG;
+  if (K % 32) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (scale_layout != Q4_SCALES_ROWMAJOR && scale_layout != Q4_SCALES_MMA) return Q4_ERR_INVALID_ARG;
+  if (rows == 0) return Q4_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16)) return Q4_ERR_INVALID_ARG;
+  return launch_quant_mxfp4(x, x_dtype, rows, K, codes, scales, scale_layout,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status quantize_int4_g128(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                             uint16_t* scales, q4_stream_t stream) {
+  if (rows < 0 || K <= 0 || !valid_dtype(x_dtype)) return Q4_ERR_INVALID_ARG;
+  if (K % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return Q4_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 2))
+    return Q4_ERR_INVALID_ARG;
+  return launch_quant_int4(x, x_dtype, rows, K, codes, scales,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status q4_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, uint8_t* dst,
+                           q4_stream_t stream) {
+  if (rows < 0 || nsf < 0) return Q4_ERR_INVALID_ARG;
+  if (rows == 0 || nsf == 0) return Q4_OK;
+  if (!src || !dst) return Q4_ERR_INVALID_ARG;
+  return launch_scales_to_mma(src, rows, nsf, dst, reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status gemm_w4a4_nvfp4(const q4_operand* A, const q4_operand* B, int64_t M, int64_t N,
+                          int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,
+                          q4_stream_t stream) {
+  return gemm_fp4_common(true, A, B, M, N, K, C, c_dtype, ws, ws_bytes, stream);
+}
+
+q4_status gemm_w4a4_mxfp4(const q4_operand* A, const q4_operand* B, int64_t M, int64_t N,
+                          int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,
+                          q4_stream_t stream) {
+  return gemm_fp4_common(false, A, B, M, N, K, C, c_dtype, ws, ws_bytes, stream);
+}
+
+q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t* Ws, int64_t M,
+                          int64_t N, int64_t K, void* C_bf16, void* ws, size_t ws_bytes,
+                          q4_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (M < 0 || N < 0 || K <= 0) return Q4_ERR_INVALID_ARG;
+  if (K % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (ceil_div(N, 128) > 65535 || ceil_div(M, 16) > 65535) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return Q4_OK;
+  if (!A_bf16 || !Wq || !Ws || !C_bf16 || !aligned(A_bf16, 16) || !aligned(Wq, 16) ||
+      !aligned(Ws, 2) || !aligned(C_bf16, 2))
+    return Q4_ERR_INVALID_ARG;
+  return launch_w4a16(A_bf16, Wq, Ws, M, N, K, C_bf16, reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
+                           const int32_t* expert_offsets, const int32_t* row_token, int64_t R,
+                           int E, const uint8_t* W_codes, const uint8_t* W_scales,
+                           const float* W_tensor_scales, int64_t N, void* C_bf16, void* ws,
+                           size_t ws_bytes, q4_stream_t stream) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T < 0 || K <= 0 || R < 0 || E < 0 || N < 0) return Q4_ERR_INVALID_ARG;
+  if (K % 256) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (E > 1024 || T > INT32_MAX / 2 || R > INT32_MAX / 2 || (int64_t)E * N > INT32_MAX / 2)
+    return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (R == 0 || N == 0 || E == 0) return Q4_OK;
+  if (T == 0) return Q4_ERR_INVALID_ARG;  // routed rows need tokens
+  if (!tokens_bf16 || !expert_offsets || !row_token || !W_codes || !W_scales ||
+      !W_tensor_scales || !C_bf16)
+    return Q4_ERR_INVALID_ARG;
+  if (!aligned(tokens_bf16, 16) || !aligned(W_codes, 16) || !aligned(W_scales, 16) ||
+      !aligned(C_bf16, 16) || !aligned(expert_offsets, 4) || !aligned(row_token, 4))
+    return Q4_ERR_INVALID_ARG;
+  Carver c{static_cast<uint8_t*>(ws), ws_bytes, 0};
+  const MoePlan pl = plan_moe(c, T, K, E, R);
+  if (!ws || !aligned(ws, 256) || !c.ok()) return Q4_ERR_WORKSPACE;
+  q4_status st;
+  // the tokens are quantized once, as one tensor with one tensor scale
+  Q4_CUDA_TRY(cudaMemsetAsync(pl.amax, 0, sizeof(unsigned), s));
+  if ((st = launch_amax(tokens_bf16, Q4_BF16, T * K, pl.amax, s)) != Q4_OK) return st;
+  if ((st = launch_quant_nvfp4(tokens_bf16, Q4_BF16, T, K, pl.tok_codes, pl.tok_sf,
+                               Q4_SCALES_ROWMAJOR, pl.amax, pl.g, s)) != Q4_OK)
+    return st;
+  if ((st = launch_grouped_prep(expert_offsets, row_token, E, pl.tok_sf, K / 16, pl.sched,
+                                pl.routed_sf, pl.cap_rows, s)) != Q4_OK)
+    return st;
+  GroupedArgs g = {};
+  g.a_codes = pl.tok_codes; g.a_sf_rows = pl.routed_sf; g.a_g = pl.g;
+  g.offsets = expert_offsets; g.row_token = row_token; g.sched = pl.sched;
+  g.T = T; g.R = R; g.N = N; g.K = K; g.E = E;
+  g.w_codes = W_codes; g.w_scales = W_scales; g.w_g = W_tensor_scales; g.C = C_bf16;
+  return launch_grouped_gemm(g, s);
+}
+
+q4_status q4_sync_status(q4_stream_t stream) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return Q4_ERR_CUDA;
+  int* d = device_status_ptr();
+  if (!d) return Q4_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, d, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return Q4_ERR_CUDA;
+  if (cudaMemsetAsync(d, 0, sizeof(int), s) != cudaSuccess) return Q4_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return Q4_ERR_CUDA;
+  return h;
+}
+
+const char* q4_status_string(q4_status s) {
+  switch (s) {
+    case Q4_OK: return "ok";
+    case Q4_ERR_INVALID_ARG: return "invalid argument";
+    case Q4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case Q4_ERR_CUDA: return "CUDA error";
+    case Q4_ERR_TIMEOUT: return "kernel wait timed out";
+    case Q4_ERR_NONFINITE: return "non-finite input";
+    case Q4_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    default: return "unknown status";
+  }
+}
+
+int q4_set_wait_timeout_ms(int ms) {
+  if (ms <= 0) return g_wait_ms.load();
+  return g_wait_ms.exchange(ms);
+}
+
+}  // extern "C"

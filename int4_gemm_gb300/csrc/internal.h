@@ -1,0 +1,89 @@
+// Host-side declarations shared by the q4gemm translation units (not part of
+// the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/q4gemm.h"
+
+namespace q4 {
+
+struct KernelCtl;
+
+// Library-wide device state (status word) and settings.
+int* device_status_ptr();            // device address of this device's status word
+unsigned long long wait_budget_ns();  // bound on any kernel-side wait
+int num_sms();                        // SM count of the current device
+
+// Error helpers
+#define Q4_CUDA_TRY(expr)                         \
+  do {                                            \
+    cudaError_t e_ = (expr);                      \
+    if (e_ != cudaSuccess) return Q4_ERR_CUDA;    \
+  } while (0)
+
+// ---------------------------------------------------------------- quantizers
+q4_status launch_amax(const void* x, int dtype, int64_t n, unsigned* amax_bits,
+                      cudaStream_t stream);
+q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
+                             uint8_t* scales, int layout, const unsigned* amax_bits,
+                             float* tensor_scale, cudaStream_t stream);
+q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
+                             uint8_t* scales, int layout, cudaStream_t stream);
+q4_status launch_quant_int4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
+                            uint16_t* scales, cudaStream_t stream);
+q4_status launch_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, uint8_t* dst,
+                               cudaStream_t stream);
+
+// ---------------------------------------------------------------- GEMMs
+// FP4 GEMM on pre-quantized operands with tensor-core scale layouts.
+struct Fp4GemmArgs {
+  const uint8_t* a_codes;   // [M, K/2]
+  const uint8_t* a_scales;  // MMA layout
+  const float* a_g;         // NVFP4 tensor scale or nullptr
+  const uint8_t* b_codes;   // [N, K/2]
+  const uint8_t* b_scales;  // MMA layout
+  const float* b_g;
+  int64_t M, N, K;
+  void* C;
+  int c_dtype;
+  bool nvfp4;  // true: E4M3 scales per 16; false: E8M0 per 32
+};
+q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream);
+
+// Grouped (routed MoE) NVFP4 GEMM on a pre-quantized token tensor.
+struct GroupedArgs {
+  const uint8_t* a_codes;    // [T, K/2] quantized tokens
+  const uint8_t* a_sf_rows;  // routed scales, MMA layout, per-expert 128-row padded blocks
+  const float* a_g;
+  const int32_t* offsets;    // [E+1]
+  const int32_t* row_token;  // [R]
+  const int32_t* sched;      // [E+1] tile-row prefix (device, built by the prep kernel)
+  int64_t T, R, N, K;
+  int E;
+  const uint8_t* w_codes;    // [E, N, K/2]
+  const uint8_t* w_scales;   // E x mma_scales_bytes(N, K/16)
+  const float* w_g;          // [E]
+  void* C;                   // [R, N] bf16
+};
+q4_status launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int E,
+                              const uint8_t* tok_scales_rowmajor, int64_t nsf, int32_t* sched,
+                              uint8_t* a_sf_routed, int64_t sf_rows_cap, cudaStream_t stream);
+q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream);
+
+q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int64_t M, int64_t N,
+                       int64_t K, void* C, cudaStream_t stream);
+
+// TMA descriptor creation through the driver entry point.
+q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                          bool swizzle128);
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t mma_scales_bytes(int64_t rows, int64_t nsf) {
+  return (size_t)(ceil_div(rows, 128) * 128) * (size_t)(ceil_div(nsf, 4) * 4);
+}
+
+}  // namespace q4

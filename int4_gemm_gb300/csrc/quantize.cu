@@ -1,0 +1,308 @@
+// Block-scaled 4-bit quantizers: NVFP4 (tensor amax + per-16 E4M3 scales),
+// MXFP4 (per-32 E8M0 scales) and INT4 g128 (per-128 FP16 scales).
+//
+// Every element is loaded once with 128-bit loads; the threads that share a
+// scale block reduce its amax with warp shuffles; codes leave as packed 32-bit
+// words (8 codes per thread).  The arithmetic follows "Quantization in
+// deployment", section "Fake quantization" (fp4, mxfp4, nvfp4) and "Low-bit
+// inference for very large MoE", section "Why quantization-aware training"
+// (fake_int4): float32, IEEE-rounded divisions, E2M1 ties to the smaller
+// magnitude.
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+
+namespace q4 {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Eight consecutive elements starting at element index e (e % 8 == 0) as
+// floats, with 128-bit loads.
+template <typename T>
+__device__ __forceinline__ void load8(const T* __restrict__ x, int64_t e, float (&v)[8]);
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* __restrict__ x, int64_t e,
+                                             float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(x + e));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(x + e + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <typename H>
+__device__ __forceinline__ void load8_16bit(const H* __restrict__ x, int64_t e, float (&v)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + e));
+  const H* h = reinterpret_cast<const H*>(&u);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = Elem<H>::to_f(h[j]);
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* __restrict__ x, int64_t e,
+                                                     float (&v)[8]) {
+  load8_16bit(x, e, v);
+}
+template <>
+__device__ __forceinline__ void load8<__half>(const __half* __restrict__ x, int64_t e,
+                                              float (&v)[8]) {
+  load8_16bit(x, e, v);
+}
+
+// ------------------------------------------------------------------ amax
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t n8,
+                                                        unsigned* amax_bits, int* status) {
+  float m = 0.f;
+  bool bad = false;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n8; u += stride) {
+    float v[8];
+    load8<T>(x, u * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      bad |= nonfinite(v[j]);
+      m = fmaxf(m, fabsf(v[j]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float warp_max[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_max[warp] = m;
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    float b = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) b = fmaxf(b, warp_max[w]);
+    // |x| >= 0, so the float bit patterns order like the values
+    atomicMax(amax_bits, __float_as_uint(b));
+    if (bad) latch_status(status, Q4_ERR_NONFINITE);
+  }
+}
+
+// ------------------------------------------------------------------ NVFP4
+// One thread per 8 elements; a thread pair shares one 16-element block.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
+                 uint8_t* __restrict__ scales, int layout, int64_t nsf4,
+                 const unsigned* __restrict__ amax_bits, float* tensor_scale) {
+  const int64_t units = rows * (K / 8);
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = u < units;
+  float v[8];
+  float amax = 0.f;
+  if (live) {
+    load8<T>(x, u * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  if (!live) return;
+
+  // per-tensor scale g = max(amax_t, 1e-12) / (448 * 6)
+  const float g = __fdiv_rn(fmaxf(__uint_as_float(*amax_bits), 1e-12f), 2688.0f);
+  // block scale: E4M3 of (amax_b / 6) / g, round to nearest even
+  const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+  const __nv_fp8_storage_t bs = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+  const float bsf = __half2float(__half(__nv_cvt_fp8_to_halfraw(bs, __NV_E4M3)));
+  const float S = __fmul_rn(fmaxf(bsf, 1e-12f), g);
+
+  uint32_t packed = 0;
+  if (bs != 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float y = __fdiv_rn(v[j], S);
+      y = fminf(fmaxf(y, -6.0f), 6.0f);
+      const uint32_t c = e2m1_index(fabsf(y)) | (v[j] < 0.f ? 8u : 0u);
+      packed |= c << (4 * j);
+    }
+  }
+  reinterpret_cast<uint32_t*>(codes)[u] = packed;
+
+  if ((u & 1) == 0) {
+    const int64_t row = u / (K / 8);
+    const int64_t blk = (u % (K / 8)) >> 1;
+    const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
+                                                : row * (K / 16) + blk;
+    scales[off] = (uint8_t)bs;
+  }
+  if (u == 0 && tensor_scale) *tensor_scale = g;
+}
+
+// ------------------------------------------------------------------ MXFP4
+// One thread per 8 elements; four threads share one 32-element block.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
+                 uint8_t* __restrict__ scales, int layout, int64_t nsf4) {
+  const int64_t units = rows * (K / 8);
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = u < units;
+  float v[8];
+  float amax = 0.f;
+  if (live) {
+    load8<T>(x, u * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  if (!live) return;
+
+  amax = fmaxf(amax, 1e-12f);  // normal, so floor(log2) is its exponent field
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 2;
+  // x / 2^e and x * 2^-e round the same real number, so they are equal
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float y = __fmul_rn(v[j], inv);
+    y = fminf(fmaxf(y, -6.0f), 6.0f);
+    const uint32_t c = e2m1_index(fabsf(y)) | (v[j] < 0.f ? 8u : 0u);
+    packed |= c << (4 * j);
+  }
+  reinterpret_cast<uint32_t*>(codes)[u] = packed;
+
+  if ((u & 3) == 0) {
+    const int64_t row = u / (K / 8);
+    const int64_t blk = (u % (K / 8)) >> 2;
+    const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
+                                                : row * (K / 32) + blk;
+    scales[off] = (uint8_t)(e + 127);
+  }
+}
+
+// ------------------------------------------------------------------ INT4 g128
+// One thread per 8 elements; sixteen threads share one 128-element group.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    int4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
+                uint16_t* __restrict__ scales) {
+  const int64_t units = rows * (K / 8);
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = u < units;
+  float v[8];
+  float amax = 0.f;
+  if (live) {
+    load8<T>(x, u * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (!live) return;
+
+  const __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
+  const float sf = __half2float(s16);
+  uint32_t packed = 0;
+  if (sf != 0.f) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float q = rintf(__fdiv_rn(v[j], sf));
+      q = fminf(fmaxf(q, -8.0f), 7.0f);
+      packed |= ((uint32_t)(int)q & 0xFu) << (4 * j);
+    }
+  }
+  reinterpret_cast<uint32_t*>(codes)[u] = packed;
+  if ((u & 15) == 0) {
+    const int64_t row = u / (K / 8);
+    const int64_t grp = (u % (K / 8)) >> 4;
+    scales[row * (K / 128) + grp] = __half_as_ushort(s16);
+  }
+}
+
+// ------------------------------------------------------------------ scale re-layout
+__global__ void __launch_bounds__(kThreads)
+    scales_to_mma_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t nsf, int64_t nsf4,
+                         uint8_t* __restrict__ dst, int64_t total) {
+  const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (d >= total) return;
+  const int64_t tile = d >> 9, o = d & 511;
+  const int64_t r = (tile / nsf4) * 128 + ((o & 15) >> 2) * 32 + (o >> 4);
+  const int64_t s = (tile % nsf4) * 4 + (o & 3);
+  dst[d] = (r < rows && s < nsf) ? src[r * nsf + s] : (uint8_t)0;
+}
+
+inline unsigned blocks_for(int64_t units) { return (unsigned)ceil_div(units, kThreads); }
+
+}  // namespace
+
+q4_status launch_amax(const void* x, int dtype, int64_t n, unsigned* amax_bits,
+                      cudaStream_t stream) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return Q4_OK;
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n8, kThreads), (int64_t)num_sms() * 8);
+  int* st = device_status_ptr();
+  switch (dtype) {
+    case Q4_F32: amax_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, n8, amax_bits, st); break;
+    case Q4_BF16: amax_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, n8, amax_bits, st); break;
+    case Q4_F16: amax_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, n8, amax_bits, st); break;
+    default: return Q4_ERR_INVALID_ARG;
+  }
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
+                             uint8_t* scales, int layout, const unsigned* amax_bits,
+                             float* tensor_scale, cudaStream_t stream) {
+  const int64_t units = rows * (K / 8);
+  const int64_t nsf4 = ceil_div(K / 16, 4);
+  if (layout == Q4_SCALES_MMA)
+    Q4_CUDA_TRY(cudaMemsetAsync(scales, 0, mma_scales_bytes(rows, K / 16), stream));
+  if (units == 0) {
+    // an empty tensor still reports g = 1e-12 / 2688
+    return Q4_OK;
+  }
+  const unsigned grid = blocks_for(units);
+  switch (dtype) {
+    case Q4_F32: nvfp4_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, rows, K, codes, scales, layout, nsf4, amax_bits, tensor_scale); break;
+    case Q4_BF16: nvfp4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, rows, K, codes, scales, layout, nsf4, amax_bits, tensor_scale); break;
+    case Q4_F16: nvfp4_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, rows, K, codes, scales, layout, nsf4, amax_bits, tensor_scale); break;
+    default: return Q4_ERR_INVALID_ARG;
+  }
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
+                             uint8_t* scales, int layout, cudaStream_t stream) {
+  const int64_t units = rows * (K / 8);
+  const int64_t nsf4 = ceil_div(K / 32, 4);
+  if (layout == Q4_SCALES_MMA)
+    Q4_CUDA_TRY(cudaMemsetAsync(scales, 0, mma_scales_bytes(rows, K / 32), stream));
+  if (units == 0) return Q4_OK;
+  const unsigned grid = blocks_for(units);
+  switch (dtype) {
+    case Q4_F32: mxfp4_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, rows, K, codes, scales, layout, nsf4); break;
+    case Q4_BF16: mxfp4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, rows, K, codes, scales, layout, nsf4); break;
+    case Q4_F16: mxfp4_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, rows, K, codes, scales, layout, nsf4); break;
+    default: return Q4_ERR_INVALID_ARG;
+  }
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+q4_status launch_quant_int4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
+                            uint16_t* scales, cudaStream_t stream) {
+  const int64_t units = rows * (K / 8);
+  if (units == 0) return Q4_OK;
+  const unsigned grid = blocks_for(units);
+  switch (dtype) {
+    case Q4_F32: int4_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, rows, K, codes, scales); break;
+    case Q4_BF16: int4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, rows, K, codes, scales); break;
+    case Q4_F16: int4_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, rows, K, codes, scales); break;
+    default: return Q4_ERR_INVALID_ARG;
+  }
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+q4_status launch_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, uint8_t* dst,
+                               cudaStream_t stream) {
+  const int64_t total = (int64_t)mma_scales_bytes(rows, nsf);
+  if (total == 0) return Q4_OK;
+  scales_to_mma_kernel<<<blocks_for(total), kThreads, 0, stream>>>(src, rows, nsf, ceil_div(nsf, 4),
+                                                                   dst, total);
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+}  // namespace q4

@@ -1,0 +1,504 @@
+// W4A4 GEMM on the GB300 FP4 tensor cores: C = A_hat . B_hat^T with E2M1
+// operands and per-16 E4M3 (NVFP4) or per-32 E8M0 (MXFP4) block scales
+// ("Low-bit inference for very large MoE", section "Kernels on different
+// hardware": activations quantized to FP4 too, both operands enter the FP4
+// tensor cores; "Quantization in deployment", "Fake quantization" for the
+// formats).  Also the grouped routed-MoE variant (same section: one low-bit
+// weight matrix per expert, grouped by routing).
+//
+// Structure (one persistent CTA per SM, 6 warps):
+//   warp 0     producer: TMA tiles of packed codes (128-byte swizzle) and bulk
+//              copies of the scale tiles into a 4-stage shared-memory ring.
+//   warps 6-9  (grouped variant only) gather the routed A rows: plain loads,
+//              swizzled shared stores, proxy fence, mbarrier arrive.
+//   warp 1     allocates TMEM; one lane copies each stage's scales into TMEM
+//              (tcgen05.cp) and issues tcgen05.mma ... block_scale, 128x256x64
+//              per instruction, FP32 accumulation in TMEM.
+//   warps 2-5  epilogue: tcgen05.ld of the 128x256 FP32 accumulator, times
+//              gA * gB (NVFP4), rounded to bf16 (or kept FP32), stored.
+// Every wait is bounded: on timeout the CTA latches Q4_ERR_TIMEOUT, drains
+// its own copies and MMAs, frees TMEM and exits.
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+
+namespace q4 {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of codes)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
+constexpr int kGatherThreads = 128;    // grouped variant: 4 more warps gather A rows
+constexpr uint32_t kABytes = BM * BK / 2;     // 16 KiB
+constexpr uint32_t kBBytes = BN * BK / 2;     // 32 KiB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = BN;             // 256 FP32 columns
+constexpr uint32_t kSfColsPerStage = 48;      // 16 (A) + 32 (B)
+constexpr int kMaxExperts = 1024;
+
+template <bool NV>
+struct Cfg {
+  static constexpr uint32_t kSfaBytes = NV ? 2048u : 1024u;  // 128 rows x (16 | 8) scales
+  static constexpr uint32_t kSfbBytes = 2 * kSfaBytes;        // 256 rows
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr uint32_t kSfChunks = NV ? 4u : 2u;  // 512-byte chunks per 128 rows per stage
+};
+static_assert(Cfg<true>::kStageBytes % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0, "");
+static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory");
+
+struct Smem {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TileInfo {
+  int m_row0;    // first output row of the tile
+  int m_end;     // output rows < m_end are valid
+  int n0;        // first output column
+  int sf_block;  // A scale row-block (dense: m tile; grouped: tile-row)
+  int e;         // expert (grouped) or 0
+  bool ok;
+};
+
+struct Params {
+  int64_t M, N, K;
+  const uint8_t* a_sf;    // MMA layout
+  const uint8_t* b_sf;    // MMA layout (grouped: E consecutive tensors)
+  int64_t b_sf_expert_bytes;
+  const float* a_g;
+  const float* b_g;       // grouped: [E]
+  void* C;
+  int c_dtype;
+  int num_m, num_n;       // dense tile counts
+  // grouped
+  const int32_t* offsets;
+  const int32_t* row_token;
+  const int32_t* sched;
+  const uint8_t* a_codes;  // grouped: quantized tokens [T, K/2]
+  int E;
+  KernelCtl ctl;
+};
+
+__device__ __forceinline__ TileInfo dense_tile(const Params& p, int t) {
+  constexpr int GM = 16;  // m tiles per band: a band's A tiles stay in L2 while B streams
+  TileInfo ti;
+  const int band_tiles = GM * p.num_n;
+  const int band = t / band_tiles, r = t % band_tiles;
+  const int gm = min(GM, p.num_m - band * GM);
+  const int m = band * GM + r % gm, n = r / gm;
+  ti.m_row0 = m * BM;
+  ti.m_end = (int)p.M;
+  ti.n0 = n * BN;
+  ti.sf_block = m;
+  ti.e = 0;
+  ti.ok = true;
+  return ti;
+}
+
+// Grouped tiles: tile-row tr (expert-major, one per 128 routed rows of an
+// expert) x n tile; n varies fastest so an expert's weights are reused from
+// L2 by all of its tile-rows.
+__device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sched, int t) {
+  TileInfo ti;
+  const int tr = t / p.num_n, n = t % p.num_n;
+  int e = 0;
+  while (e + 1 < p.E && sched[e + 1] <= tr) ++e;
+  ti.e = e;
+  ti.m_row0 = __ldg(p.offsets + e) + (tr - sched[e]) * BM;
+  ti.m_end = __ldg(p.offsets + e + 1);
+  ti.n0 = n * BN;
+  ti.sf_block = tr;
+  ti.ok = ti.m_row0 < ti.m_end;
+  return ti;
+}
+
+
+template <bool NV, bool GROUPED>
+__global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
+    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+  using C_ = Cfg<NV>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Smem* sm = reinterpret_cast<Smem*>(smem + kStages * C_::kStageBytes);
+  __shared__ int s_sched[GROUPED ? kMaxExperts + 1 : 1];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = (int)(p.K / BK);
+
+  int total_tiles;
+  if constexpr (GROUPED) {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_sched[i] = __ldg(p.sched + i);
+    __syncthreads();
+    total_tiles = s_sched[p.E] * p.num_n;
+  } else {
+    total_tiles = p.num_m * p.num_n;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), GROUPED ? 1 + kGatherThreads : 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sm->acc_full), 1);
+    mbar_init(smem_u32(&sm->acc_empty), 4);
+    mbar_init(smem_u32(&sm->mma_done), 1);
+    sm->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort_flag = &sm->abort;
+
+  auto tile_at = [&](int t) -> TileInfo {
+    if constexpr (GROUPED) return grouped_tile(p, s_sched, t);
+    else return dense_tile(p, t);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    int issued[kStages];
+    uint32_t issued_phase[kStages];
+    for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
+    bool alive = true;
+    const int nsf4_a = (int)((p.K / (NV ? 16 : 32) + 3) / 4);
+    const int nblk_b = (int)((p.N + 127) / 128);
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      const TileInfo ti = tile_at(t);
+      if (!ti.ok) continue;
+      const uint8_t* sfa = p.a_sf + (int64_t)ti.sf_block * nsf4_a * 512;
+      const uint8_t* sfb = p.b_sf + (int64_t)ti.e * p.b_sf_expert_bytes;
+      const int nb0 = ti.n0 / 128;
+      const bool b_hi = nb0 + 1 < nblk_b;
+      const uint32_t bytes = (GROUPED ? 0u : kABytes) + kBBytes + C_::kSfaBytes +
+                             C_::kSfaBytes * (b_hi ? 2 : 1);
+      const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint8_t* st = smem + stage * C_::kStageBytes;
+        const uint32_t full = smem_u32(&sm->full[stage]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, bytes);
+          if constexpr (!GROUPED) tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
+          tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2), b_row, full);
+          const int64_t jsf = (int64_t)kb * C_::kSfChunks * 512;
+          bulk_load(smem_u32(st + kABytes + kBBytes), sfa + jsf, C_::kSfaBytes, full);
+          const uint8_t* sfb0 = sfb + (int64_t)nb0 * nsf4_a * 512 + jsf;
+          bulk_load(smem_u32(st + kABytes + kBBytes + C_::kSfaBytes), sfb0, C_::kSfaBytes, full);
+          if (b_hi)
+            bulk_load(smem_u32(st + kABytes + kBBytes + 2 * C_::kSfaBytes), sfb0 + nsf4_a * 512,
+                      C_::kSfaBytes, full);
+        }
+        issued[stage] = 1;
+        issued_phase[stage] = phase;
+        if (++stage == kStages) stage = 0, phase ^= 1;
+      }
+    }
+    // drain: every copy this warp issued has landed before the CTA exits
+    if (lane == 0) {
+      KernelCtl drain = p.ctl;
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t stage = 0, phase = 0, tcount = 0;
+    bool alive = true;
+    if (lane == 0) {
+      for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x, ++tcount) {
+        const TileInfo ti = tile_at(t);
+        if (!ti.ok) { --tcount; continue; }
+        if (!mbar_wait(smem_u32(&sm->acc_empty), (tcount & 1) ^ 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * C_::kStageBytes);
+          const uint32_t sfa_s = st + kABytes + kBBytes;
+          const uint32_t sfb_s = sfa_s + C_::kSfaBytes;
+          const uint32_t sf_t = tmem + kAccCols + stage * kSfColsPerStage;
+          // scales -> TMEM: chunk j of A at columns 4j, chunk (h, j) of B at 16 + 8j + 4h
+#pragma unroll
+          for (uint32_t j = 0; j < C_::kSfChunks; ++j) {
+            tc_cp_32x128b_x4(sf_t + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
+            tc_cp_32x128b_x4(sf_t + 16 + 8 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
+            tc_cp_32x128b_x4(sf_t + 16 + 8 * j + 4, smem_desc(sfb_s + C_::kSfaBytes + 512 * j, 0, 128, 0));
+          }
+#pragma unroll
+          for (uint32_t k = 0; k < BK / 64; ++k) {
+            const uint64_t ad = smem_desc(st + 32 * k, 16, 1024, 2);
+            const uint64_t bd = smem_desc(st + kABytes + 32 * k, 16, 1024, 2);
+            const uint32_t j = NV ? k : k >> 1;
+            const uint32_t sf_id = NV ? 0u : (k & 1) * 2;
+            const uint32_t idesc = fp4_idesc(BM, BN, !NV, sf_id, sf_id);
+            tc_mma_fp4<NV ? 4 : 2>(tmem, ad, bd, idesc, sf_t + 4 * j, sf_t + 16 + 8 * j,
+                                   (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&sm->empty[stage]));
+          if (++stage == kStages) stage = 0, phase ^= 1;
+        }
+        if (!alive) break;
+        tc_commit(smem_u32(&sm->acc_full));
+      }
+      // all MMAs this thread issued are complete before TMEM is released
+      tc_commit(smem_u32(&sm->mma_done));
+      KernelCtl drain = p.ctl;
+      mbar_wait(smem_u32(&sm->mma_done), 0, drain, nullptr);
+    }
+    __syncwarp();
+  } else if (GROUPED && warp >= kThreads / 32) {
+    // ------------------------------------------------------------ A-row gather (grouped)
+    // Thread i copies routed row i of the tile (its token's 128 code bytes of
+    // this K block) into the 128-byte-swizzled A tile, then makes the writes
+    // visible to the tensor core's async proxy before arriving.
+    const int i = threadIdx.x - kThreads;
+    uint32_t stage = 0, phase = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      const TileInfo ti = tile_at(t);
+      if (!ti.ok) continue;
+      const int r = ti.m_row0 + i;
+      const int tokr = __ldg(p.row_token + (r < ti.m_end ? r : ti.m_row0));
+      const uint8_t* src = p.a_codes + (int64_t)tokr * (p.K / 2);
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          v[c] = __ldg(reinterpret_cast<const uint4*>(src + kb * (BK / 2)) + c);
+        uint8_t* dst = smem + stage * C_::kStageBytes + i * (BK / 2);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(dst + ((c ^ (i & 7)) << 4)) = v[c];
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&sm->full[stage]));
+        if (++stage == kStages) stage = 0, phase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t tcount = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const TileInfo ti = tile_at(t);
+      if (!ti.ok) continue;
+      if (!mbar_wait(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
+      tc_fence_after();
+      float alpha = 1.f;
+      if constexpr (NV) alpha = __ldg(p.a_g) * __ldg(p.b_g + ti.e);
+      const int row = ti.m_row0 + q * 32 + lane;
+      const bool row_ok = row < ti.m_end;
+      const bool vec_ok = (p.N % 8) == 0;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
+        tmem_ld_wait();
+        const int col0 = ti.n0 + c * 32;
+        if (!row_ok || col0 >= p.N) continue;
+        const bool full_chunk = col0 + 32 <= p.N;
+        if (p.c_dtype == Q4_BF16) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.N + col0;
+          if (full_chunk && vec_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(
+                    __uint_as_float(r[v * 8 + 2 * i]) * alpha,
+                    __uint_as_float(r[v * 8 + 2 * i + 1]) * alpha);
+                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              reinterpret_cast<uint4*>(out)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < p.N) out[i] = __float2bfloat16_rn(__uint_as_float(r[i]) * alpha);
+          }
+        } else {
+          float* out = reinterpret_cast<float*>(p.C) + (int64_t)row * p.N + col0;
+          if (full_chunk && (p.N % 4) == 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<float4*>(out)[v] =
+                  make_float4(__uint_as_float(r[4 * v]) * alpha, __uint_as_float(r[4 * v + 1]) * alpha,
+                              __uint_as_float(r[4 * v + 2]) * alpha, __uint_as_float(r[4 * v + 3]) * alpha);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < p.N) out[i] = __uint_as_float(r[i]) * alpha;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm->acc_empty));
+      ++tcount;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ grouped prep
+// sched[e] = first tile-row of expert e (prefix of ceil(M_e / 128)).
+__global__ void grouped_sched_kernel(const int32_t* __restrict__ offsets, int E,
+                                     int32_t* __restrict__ sched) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    int acc = 0;
+    sched[0] = 0;
+    for (int e = 0; e < E; ++e) {
+      const int m = __ldg(offsets + e + 1) - __ldg(offsets + e);
+      acc += (max(m, 0) + BM - 1) / BM;
+      sched[e + 1] = acc;
+    }
+  }
+}
+
+// Routed A scales in the tensor-core layout: tile-row tr, local row i holds
+// the scales of token row_token[offsets[e] + (tr - sched[e]) * 128 + i]
+// (zero past the expert's last row).  One block of 128 threads per tile-row.
+__global__ void __launch_bounds__(128)
+    grouped_sf_kernel(const int32_t* __restrict__ offsets, const int32_t* __restrict__ row_token,
+                      const int32_t* __restrict__ sched, int E,
+                      const uint8_t* __restrict__ tok_sf, int64_t nsf,
+                      uint8_t* __restrict__ out) {
+  const int tr = blockIdx.x;
+  if (tr >= __ldg(sched + E)) return;
+  int e = 0;
+  while (e + 1 < E && __ldg(sched + e + 1) <= tr) ++e;
+  const int i = threadIdx.x;
+  const int r = __ldg(offsets + e) + (tr - __ldg(sched + e)) * BM + i;
+  const bool ok = r < __ldg(offsets + e + 1);
+  const uint32_t* src =
+      ok ? reinterpret_cast<const uint32_t*>(tok_sf + (int64_t)__ldg(row_token + r) * nsf) : nullptr;
+  const int64_t nsf4 = (nsf + 3) / 4;
+  for (int64_t J = 0; J < nsf4; ++J) {
+    const uint32_t w = ok ? __ldg(src + J) : 0u;
+    *reinterpret_cast<uint32_t*>(out + ((int64_t)tr * nsf4 + J) * 512 + (i & 31) * 16 + (i >> 5) * 4) = w;
+  }
+}
+
+}  // namespace
+
+namespace {
+
+template <bool NV, bool GROUPED>
+q4_status set_smem_attr() {
+  static int done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
+  if (!done[dev]) {
+    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)Cfg<NV>::kSmemBytes));
+    done[dev] = 1;
+  }
+  return Q4_OK;
+}
+
+}  // namespace
+
+q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
+  if (a.M == 0 || a.N == 0) return Q4_OK;
+  CUtensorMap ta, tb;
+  q4_status st;
+  if ((st = make_tmap_2d_u8(&ta, a.a_codes, a.K / 2, a.M, a.K / 2, BK / 2, BM, true)) != Q4_OK) return st;
+  if ((st = make_tmap_2d_u8(&tb, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN, true)) != Q4_OK) return st;
+  Params p = {};
+  p.M = a.M; p.N = a.N; p.K = a.K;
+  p.a_sf = a.a_scales; p.b_sf = a.b_scales; p.b_sf_expert_bytes = 0;
+  p.a_g = a.a_g; p.b_g = a.b_g;
+  p.C = a.C; p.c_dtype = a.c_dtype;
+  p.num_m = (int)ceil_div(a.M, BM); p.num_n = (int)ceil_div(a.N, BN);
+  p.ctl.status = device_status_ptr();
+  p.ctl.wait_ns = wait_budget_ns();
+  const int tiles = p.num_m * p.num_n;
+  const unsigned grid = (unsigned)std::min(tiles, num_sms());
+  if (a.nvfp4) {
+    if ((st = set_smem_attr<true, false>()) != Q4_OK) return st;
+    fp4_gemm_kernel<true, false><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(ta, tb, p);
+  } else {
+    if ((st = set_smem_attr<false, false>()) != Q4_OK) return st;
+    fp4_gemm_kernel<false, false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(ta, tb, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+q4_status launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int E,
+                              const uint8_t* tok_scales_rowmajor, int64_t nsf, int32_t* sched,
+                              uint8_t* a_sf_routed, int64_t sf_rows_cap, cudaStream_t stream) {
+  grouped_sched_kernel<<<1, 32, 0, stream>>>(offsets, E, sched);
+  if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+  const int64_t cap_blocks = sf_rows_cap / BM;
+  if (cap_blocks > 0) {
+    grouped_sf_kernel<<<(unsigned)cap_blocks, 128, 0, stream>>>(offsets, row_token, sched, E,
+                                                                 tok_scales_rowmajor, nsf, a_sf_routed);
+    if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+  }
+  return Q4_OK;
+}
+
+q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
+  if (a.R == 0 || a.N == 0 || a.E == 0) return Q4_OK;
+  if (a.E > kMaxExperts) return Q4_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap tb;
+  q4_status st;
+  // B: the E stacked expert weights as one tensor; A rows are gathered by threads
+  if ((st = make_tmap_2d_u8(&tb, a.w_codes, a.K / 2, (uint64_t)a.E * a.N, a.K / 2, BK / 2, BN, true)) != Q4_OK) return st;
+  Params p = {};
+  p.M = a.R; p.N = a.N; p.K = a.K;
+  p.a_sf = a.a_sf_rows; p.b_sf = a.w_scales;
+  p.b_sf_expert_bytes = (int64_t)mma_scales_bytes(a.N, a.K / 16);
+  p.a_g = a.a_g; p.b_g = a.w_g;
+  p.C = a.C; p.c_dtype = Q4_BF16;
+  p.num_m = 0; p.num_n = (int)ceil_div(a.N, BN);
+  p.offsets = a.offsets; p.row_token = a.row_token; p.sched = a.sched; p.E = a.E;
+  p.a_codes = a.a_codes;
+  p.ctl.status = device_status_ptr();
+  p.ctl.wait_ns = wait_budget_ns();
+  if ((st = set_smem_attr<true, true>()) != Q4_OK) return st;
+  fp4_gemm_kernel<true, true><<<(unsigned)num_sms(), kThreads + kGatherThreads, Cfg<true>::kSmemBytes,
+                                stream>>>(tb, tb, p);
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+}  // namespace q4

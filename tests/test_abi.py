@@ -1,0 +1,71 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function the
+public header declares, and rejects bad arguments on the host before any
+launch (these calls return before touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4gemm.h")
+
+
+@pytest.fixture(scope="module")
+def clib():
+    from int4_gemm_gb300 import build
+    import int4_gemm_gb300 as q4
+    build.build()
+    return q4.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ["quantize_nvfp4", "quantize_mxfp4", "quantize_int4_g128", "gemm_w4a4_nvfp4",
+                 "gemm_w4a4_mxfp4", "gemm_w4a16_int4", "grouped_gemm_moe", "q4_sync_status",
+                 "q4_workspace_size", "q4_scales_to_mma"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(clib):
+    for name in declared_functions():
+        assert hasattr(clib, name), name
+
+
+def test_host_argument_checks(clib):
+    P = ctypes.c_void_p
+    fake = 0x10000  # never dereferenced: every call below fails validation first
+    # K not a multiple of the block
+    assert clib.quantize_mxfp4(fake, 1, 4, 48, fake, fake, 0, None) == -2
+    assert clib.quantize_int4_g128(fake, 1, 4, 64, fake, fake, None) == -2
+    assert clib.gemm_w4a16_int4(fake, fake, fake, 4, 4, 100, fake, None, 0, None) == -2
+    # bad dtype, negative sizes, null pointers, misalignment
+    assert clib.quantize_mxfp4(fake, 7, 4, 64, fake, fake, 0, None) == -1
+    assert clib.quantize_int4_g128(fake, 1, -1, 128, fake, fake, None) == -1
+    assert clib.gemm_w4a16_int4(None, fake, fake, 4, 4, 128, fake, None, 0, None) == -1
+    assert clib.gemm_w4a16_int4(fake + 2, fake, fake, 4, 4, 128, fake, None, 0, None) == -1
+    # NVFP4 quantize needs its workspace
+    assert clib.quantize_nvfp4(fake, 1, 4, 64, fake, fake, 0, fake, None, 0, None) == -6
+    # empty problems are no-ops
+    assert clib.quantize_int4_g128(None, 1, 0, 128, None, None, None) == 0
+    assert clib.gemm_w4a16_int4(None, None, None, 0, 4, 128, None, None, 0, None) == 0
+
+
+def test_workspace_sizes(clib):
+    assert clib.q4_workspace_size(3, 16, 8192, 8192) == 0  # W4A16 needs none
+    n = clib.q4_workspace_size(1, 8192, 28672, 8192)
+    assert n >= 8192 * 4096 + 28672 * 4096  # room for both operands' codes
+    assert clib.q4_mma_scales_bytes(130, 5) == 256 * 8
+    assert clib.q4_workspace_size_moe(4096, 2048, 7168, 64, 32768) > 4096 * 3584
+
+
+def test_status_strings(clib):
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert clib.q4_status_string(s)

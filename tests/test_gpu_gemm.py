@@ -1,0 +1,143 @@
+"""GPU GEMMs against the FP64 oracle on shapes that span several tiles, ragged
+M / N tails, single and many K blocks, more tiles than SMs, both operand paths
+(raw operands quantized on the fly, pre-quantized operands in either scale
+layout) and both output types."""
+import numpy as np
+import pytest
+import torch
+
+import int4_gemm_gb300 as q4
+import oracle
+import workloads
+from tests._util import assert_gemm_close
+
+pytestmark = pytest.mark.gpu
+
+W4A4_SHAPES = [(16, 256, 512), (1, 256, 256), (130, 300, 768), (257, 520, 1024),
+               (128, 256, 4096), (2048, 4096, 256), (300, 1000, 512)]
+
+
+def _nv_pair(M, N, K, seed):
+    a, b = workloads.nvfp4_pair(M, N, K, seed, a_std=1.0, channel_outliers=True)
+    return a, b
+
+
+@pytest.mark.parametrize("shape", W4A4_SHAPES)
+def test_w4a4_nvfp4_raw_operands(lib, shape):
+    M, N, K = shape
+    a, b = _nv_pair(M, N, K, seed=sum(shape))
+    C = lib.gemm_w4a4_nvfp4(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), K,
+                            out_dtype=torch.float32)
+    R = oracle.gemm_w4a4_nvfp4(*oracle.quantize_nvfp4(a), *oracle.quantize_nvfp4(b))
+    assert_gemm_close(C.cpu().numpy(), R)
+    assert lib.sync_status() == 0
+
+
+@pytest.mark.parametrize("layout", ["rowmajor", "mma"])
+@pytest.mark.parametrize("shape", [(130, 300, 768), (512, 768, 1024)])
+def test_w4a4_nvfp4_prequantized_bf16(lib, layout, shape):
+    M, N, K = shape
+    a, b = _nv_pair(M, N, K, seed=3 + M)
+    ad = workloads.to_bf16(a).cuda()
+    qa = q4.Fp4Operand(*_q(lib.quantize_nvfp4(ad, scale_layout=layout), layout))
+    qb = q4.Fp4Operand(*_q(lib.quantize_nvfp4(torch.from_numpy(b).cuda(), scale_layout=layout), layout))
+    C = lib.gemm_w4a4_nvfp4(qa, qb, K, out_dtype=torch.bfloat16)
+    R = oracle.gemm_w4a4_nvfp4(*oracle.quantize_nvfp4(ad.float().cpu().numpy()), *oracle.quantize_nvfp4(b))
+    assert_gemm_close(C.float().cpu().numpy(), R)
+
+
+def _q(t, layout):
+    codes, scales, g = t
+    return codes, scales, layout, g
+
+
+@pytest.mark.parametrize("shape", W4A4_SHAPES)
+def test_w4a4_mxfp4_raw_operands(lib, shape):
+    M, N, K = shape
+    a, b = workloads.mxfp4_pair(M, N, K, seed=sum(shape) + 1)
+    ad = workloads.to_bf16(a).cuda()
+    C = lib.gemm_w4a4_mxfp4(ad, torch.from_numpy(b).cuda(), K, out_dtype=torch.bfloat16)
+    R = oracle.gemm_w4a4_mxfp4(*oracle.quantize_mxfp4(ad.float().cpu().numpy()), *oracle.quantize_mxfp4(b))
+    assert_gemm_close(C.float().cpu().numpy(), R)
+
+
+@pytest.mark.parametrize("layout", ["rowmajor", "mma"])
+def test_w4a4_mxfp4_prequantized(lib, layout):
+    M, N, K = 200, 600, 1280
+    a, b = workloads.mxfp4_pair(M, N, K, seed=11)
+    ca, sa = lib.quantize_mxfp4(torch.from_numpy(a).cuda(), scale_layout=layout)
+    cb, sb = lib.quantize_mxfp4(torch.from_numpy(b).cuda(), scale_layout=layout)
+    C = lib.gemm_w4a4_mxfp4(q4.Fp4Operand(ca, sa, layout), q4.Fp4Operand(cb, sb, layout), K,
+                            out_dtype=torch.float32)
+    R = oracle.gemm_w4a4_mxfp4(*oracle.quantize_mxfp4(a), *oracle.quantize_mxfp4(b))
+    assert_gemm_close(C.cpu().numpy(), R)
+
+
+def test_tiny_workload_fp32(lib):
+    """The tiny NVFP4 problem with the eight-weight worked row, fp32 output."""
+    a, b = workloads.tiny()
+    C = lib.gemm_w4a4_nvfp4(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), 512,
+                            out_dtype=torch.float32)
+    R = oracle.gemm_w4a4_nvfp4(*oracle.quantize_nvfp4(a), *oracle.quantize_nvfp4(b))
+    fro, _ = assert_gemm_close(C.cpu().numpy(), R)
+    assert fro < 1e-5  # fp32 output: only the accumulation order differs
+
+
+def test_identity_operand(lib):
+    """B = I (K = 256): C = c * A_hat with c = 6 * 448 * gB."""
+    M, K = 96, 256
+    a, _ = workloads.nvfp4_pair(M, 8, K, seed=5)
+    eye = np.zeros((K, K), np.float32)
+    np.fill_diagonal(eye, 1.0)
+    C = lib.gemm_w4a4_nvfp4(torch.from_numpy(a).cuda(), torch.from_numpy(eye).cuda(), K,
+                            out_dtype=torch.float32).cpu().numpy()
+    qa, qb = oracle.quantize_nvfp4(a), oracle.quantize_nvfp4(eye)
+    want = oracle.dequantize_nvfp4(*qa) * (6.0 * 448.0 * float(qb[2]))
+    assert np.allclose(C, want, rtol=1e-6, atol=0)
+
+
+W4A16_SHAPES = [(1, 256, 1024), (4, 520, 2048), (16, 1000, 1152), (5, 128, 128),
+                (17, 300, 8192), (33, 256, 512), (16, 2048, 8192)]
+
+
+@pytest.mark.parametrize("shape", W4A16_SHAPES)
+def test_w4a16_int4(lib, shape):
+    M, N, K = shape
+    A, W = workloads.decode(M, seed=sum(shape), N=N, K=K)
+    wq, ws = lib.quantize_int4_g128(torch.from_numpy(W).cuda())
+    owq, ows = oracle.quantize_int4_g128(W)
+    assert np.array_equal(wq.cpu().numpy(), owq) and np.array_equal(ws.cpu().numpy().view(np.uint16), ows)
+    C = lib.gemm_w4a16_int4(A.cuda(), wq, ws)
+    R = oracle.gemm_w4a16_int4(A.float().numpy(), owq, ows)
+    assert_gemm_close(C.float().cpu().numpy(), R)
+    assert lib.sync_status() == 0
+
+
+def test_w4a16_repeatable(lib):
+    A, W = workloads.decode(16, seed=9, N=1024, K=4096)
+    wq, ws = lib.quantize_int4_g128(torch.from_numpy(W).cuda())
+    c1 = lib.gemm_w4a16_int4(A.cuda(), wq, ws)
+    c2 = lib.gemm_w4a16_int4(A.cuda(), wq, ws)
+    assert torch.equal(c1, c2)  # deterministic split-K reduction
+
+
+def _grouped_case(T, E, N, K, top, seed):
+    tok = workloads.to_bf16(workloads.normal(workloads.rng_for(seed, 1), (T, K), 1.0))
+    offs, rt = workloads.route_top_k(T, E, top, seed)
+    ws = [workloads.expert_weight(seed, e, N, K) for e in range(E)]
+    return tok, offs, rt, ws
+
+
+@pytest.mark.parametrize("case", [(64, 5, 512, 512, 2), (300, 8, 320, 768, 4), (40, 3, 256, 256, 1)])
+def test_grouped_moe(lib, case):
+    T, E, N, K, top = case
+    tok, offs, rt, ws = _grouped_case(T, E, N, K, top, seed=T + E)
+    wc, wsf, wg = [], [], []
+    for w in ws:
+        c, s, g = lib.quantize_nvfp4(torch.from_numpy(w).cuda(), scale_layout="mma")
+        wc.append(c), wsf.append(s), wg.append(g)
+    C = lib.grouped_gemm_moe(tok.cuda(), torch.from_numpy(offs).cuda(), torch.from_numpy(rt).cuda(),
+                             torch.stack(wc), torch.cat(wsf), torch.cat(wg), N)
+    R = oracle.grouped_gemm_moe(tok.float().numpy(), offs, rt, [oracle.quantize_nvfp4(w) for w in ws])
+    assert_gemm_close(C.float().cpu().numpy(), R)
+    assert lib.sync_status() == 0

@@ -1,0 +1,150 @@
+"""GPU quantizers against the CPU oracle: codes, scales and tensor scales must
+match bit for bit, on ragged shapes, all input dtypes, both scale layouts and
+the edge cases of the method (ties, zero blocks, underflowing scales)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._util import spread, to_mma_layout
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [torch.float32, torch.bfloat16, torch.float16]
+
+
+def _dev(x, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dtype)
+    return t.cuda(), t.float().numpy()  # the oracle sees exactly the values the GPU sees
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 16), (7, 48), (130, 272), (257, 1024), (64, 7168)])
+def test_nvfp4_bit_exact(lib, dtype, shape):
+    x = spread(shape[0] * 31 + shape[1], *shape, lo=-6, hi=6)
+    xd, xh = _dev(x, dtype)
+    codes, scales, g = lib.quantize_nvfp4(xd)
+    oc, os_, og = oracle.quantize_nvfp4(xh)
+    assert g.item() == float(og)
+    assert np.array_equal(scales.cpu().numpy(), os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert lib.sync_status() == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 32), (5, 96), (130, 288), (257, 2048)])
+def test_mxfp4_bit_exact(lib, dtype, shape):
+    # fp16 holds +-65504 at most: keep its inputs finite
+    lo, hi = (-6, 6) if dtype == torch.float16 else (-20, 20)
+    x = spread(shape[0] * 17 + shape[1], *shape, lo=lo, hi=hi)
+    xd, xh = _dev(x, dtype)
+    codes, scales = lib.quantize_mxfp4(xd)
+    oc, os_ = oracle.quantize_mxfp4(xh)
+    assert np.array_equal(scales.cpu().numpy(), os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 128), (9, 384), (130, 1152), (300, 8192)])
+def test_int4_g128_bit_exact(lib, dtype, shape):
+    lo, hi = (-6, 6) if dtype == torch.float16 else (-10, 10)
+    x = spread(shape[0] * 13 + shape[1], *shape, lo=lo, hi=hi)
+    xd, xh = _dev(x, dtype)
+    codes, scales = lib.quantize_int4_g128(xd)
+    oc, os_ = oracle.quantize_int4_g128(xh)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), os_)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("shape", [(1, 256), (130, 512), (300, 768)])
+def test_mma_scale_layout(lib, fmt, shape):
+    x = spread(7, *shape)
+    xd, xh = _dev(x, torch.float32)
+    if fmt == "nvfp4":
+        c1, s_mma, _ = lib.quantize_nvfp4(xd, scale_layout="mma")
+        c2, s_row, _ = lib.quantize_nvfp4(xd)
+    else:
+        c1, s_mma = lib.quantize_mxfp4(xd, scale_layout="mma")
+        c2, s_row = lib.quantize_mxfp4(xd)
+    want = to_mma_layout(s_row.cpu().numpy())
+    assert np.array_equal(s_mma.cpu().numpy(), want)
+    assert torch.equal(c1, c2)
+    assert np.array_equal(lib.scales_to_mma(s_row).cpu().numpy(), want)
+
+
+def test_worked_row(lib):
+    x = np.zeros((1, 128), np.float32)
+    x[0, :8] = workloads.WORKED_ROW
+    xd, xh = _dev(x, torch.float32)
+    for got, want in ((lib.quantize_nvfp4(xd)[:2], oracle.quantize_nvfp4(xh)[:2]),
+                      (lib.quantize_mxfp4(xd), oracle.quantize_mxfp4(xh))):
+        assert all(np.array_equal(g.cpu().numpy(), w) for g, w in zip(got, want))
+    c, s = lib.quantize_int4_g128(xd)
+    oc, os_ = oracle.quantize_int4_g128(xh)
+    assert np.array_equal(c.cpu().numpy(), oc) and np.array_equal(s.cpu().numpy().view(np.uint16), os_)
+
+
+def test_exact_midpoints_tie_to_smaller(lib):
+    """Every E2M1 midpoint, positive and negative, at scale exactly 1."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    x = np.zeros((2, 32), np.float32)
+    x[0, :7], x[0, 8:15], x[0, 16] = mids, -mids, 6.0        # MXFP4: amax 6 -> scale 1
+    x[1, 0] = 2688.0                                          # NVFP4: g = 1
+    x[1, 16:23], x[1, 24:31] = mids, -mids
+    x[1, 31] = 6.0                                            # block amax 6 -> E4M3 1 -> S = 1
+    xd, xh = _dev(x, torch.float32)
+    c, s = lib.quantize_mxfp4(xd)
+    oc, os_ = oracle.quantize_mxfp4(xh)
+    assert np.array_equal(c.cpu().numpy(), oc) and np.array_equal(s.cpu().numpy(), os_)
+    c, s, g = lib.quantize_nvfp4(xd)
+    oc, os_, og = oracle.quantize_nvfp4(xh)
+    assert g.item() == 1.0 == float(og)
+    assert np.array_equal(c.cpu().numpy(), oc) and np.array_equal(s.cpu().numpy(), os_)
+
+
+def test_int4_half_integer_ties(lib):
+    x = np.zeros((1, 128), np.float32)
+    x[0, :6] = [3.5, 1.25, 0.75, 0.25, -0.25, -1.25]  # s = 0.5: x/s = 7, 2.5, 1.5, 0.5, ...
+    xd, xh = _dev(x, torch.float32)
+    c, s = lib.quantize_int4_g128(xd)
+    oc, os_ = oracle.quantize_int4_g128(xh)
+    assert np.array_equal(c.cpu().numpy(), oc) and np.array_equal(s.cpu().numpy().view(np.uint16), os_)
+
+
+def test_zero_and_underflowing_blocks(lib):
+    x = np.zeros((3, 256), np.float32)
+    x[1, 0] = 1000.0
+    x[1, 16:20] = [1e-6, -2e-6, 3e-7, -0.0]   # NVFP4 block scale rounds to 0
+    x[2, 128:130] = [1e-9, -1e-9]            # INT4 scale underflows FP16
+    x[2, 0] = -1e-30
+    xd, xh = _dev(x, torch.float32)
+    for got, want in ((lib.quantize_nvfp4(xd), oracle.quantize_nvfp4(xh)),
+                      (lib.quantize_mxfp4(xd), oracle.quantize_mxfp4(xh))):
+        assert np.array_equal(got[0].cpu().numpy(), want[0])
+        assert np.array_equal(got[1].cpu().numpy(), want[1])
+    c, s = lib.quantize_int4_g128(xd)
+    oc, os_ = oracle.quantize_int4_g128(xh)
+    assert np.array_equal(c.cpu().numpy(), oc) and np.array_equal(s.cpu().numpy().view(np.uint16), os_)
+    z = torch.zeros((4, 64), device="cuda")
+    c, s, g = lib.quantize_nvfp4(z)
+    assert g.item() == float(np.float32(np.float32(1e-12) / np.float32(2688)))
+    assert int(c.sum()) == 0 and int(s.sum()) == 0
+
+
+def test_nonfinite_input_is_reported(lib):
+    x = torch.ones((4, 64), device="cuda")
+    x[2, 5] = float("nan")
+    lib.quantize_nvfp4(x)
+    assert lib.sync_status() == -5
+    assert lib.sync_status() == 0  # cleared by the read
+
+
+def test_empty_rows(lib):
+    x = torch.empty((0, 64), device="cuda")
+    c, s, g = lib.quantize_nvfp4(x)
+    assert c.numel() == 0
+    c, s = lib.quantize_mxfp4(x)
+    c, s = lib.quantize_int4_g128(torch.empty((0, 128), device="cuda"))
+    assert lib.sync_status() == 0
