@@ -1,0 +1,694 @@
+"""Benchmark of the block-scaled 4-bit hot path on GB300.
+
+Default workload: the W4A16 decode GEMM, N = K = 8192 INT4 g128 weights, bf16
+activations at M = 1, 4 and 16.  One step runs the three decode GEMMs, each on
+its own copy of the weights (8 rotating copies, 277 MB > L2, so every launch
+streams its weights from HBM).  ``value`` is algorithmic HBM bytes per second
+over the timed steps, with all inputs resident in HBM; ``e2e`` is the same
+metric through the public Python API with the activations copied in from
+pinned host memory and the outputs copied back every step.
+
+Other workloads (``--workload``): ``prefill`` (NVFP4 W4A4, 8192 x 28672 x
+8192, A quantized on the fly), ``moe`` (MXFP4 W4A4, 256 x 2048 x 7168, A
+quantized on the fly), ``grouped`` (64-expert routed NVFP4 MoE), ``tiny``.
+
+``--impl reference`` times the CPU oracle (the reference arm: a plain, slow
+numpy/FP64 restatement of the method) on a bounded sample of the same
+workload.  Multi-GPU (torchrun): every rank runs an independent replica
+(weak scaling; the decode GEMM has no exchange step); ``value`` sums the
+ranks' work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense ratio FP4 : BF16 on GB300 (13.5 vs 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0
+
+# ncu-measured DRAM traffic per launch of the dominant kernel (bytes), keyed by
+# workload; None until a capture of the current kernel exists.
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, use_gpu: bool):
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if use_gpu else "gloo"
+            if use_gpu:
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+METRIC = "FP4/INT4 GEMM TFLOP/s & HBM GB/s at decode/prefill shapes, % of roofline"
+
+
+# --------------------------------------------------------------------------- workloads
+
+class Decode:
+    """W4A16 decode: INT4 g128 weights N = K = 8192, bf16 activations M = 1, 4, 16."""
+    name = "w4a16_decode"
+    unit = "GB/s"
+    bound = "hbm"
+    default_steps = 30000
+    N = K = 8192
+    Ms = (1, 4, 16)
+    copies = 8  # 8 x 34.6 MB of weights rotate, > 2 x L2
+    kernel = "w4a16_kernel"
+
+    def config(self):
+        return {"workload": "w4a16_decode N=K=8192 INT4-g128 weights, bf16 A, M=1,4,16 per step",
+                "M": list(self.Ms), "N": self.N, "K": self.K,
+                "l2": f"rotating {self.copies} weight copies ({self.copies * self.weight_bytes() / 1e6:.0f} MB > L2)"}
+
+    def weight_bytes(self):
+        return self.N * self.K // 2 + self.N * (self.K // 128) * 2
+
+    def bytes_per_gemm(self, M, N=None):
+        N = self.N if N is None else N
+        return N * self.K // 2 + N * (self.K // 128) * 2 + M * self.K * 2 + M * N * 2
+
+    def units_per_step(self):
+        return sum(self.bytes_per_gemm(M) for M in self.Ms)
+
+    def flops_per_step(self):
+        return sum(2 * M * self.N * self.K for M in self.Ms)
+
+    launches_per_step = 3
+
+    def setup(self, q4, dev, seed):
+        self.q4 = q4
+        w = workloads.int4_weights(self.N, self.K, seed)
+        wd = torch.from_numpy(w).to(dev)
+        wq, ws = q4.quantize_int4_g128(wd)
+        del wd
+        self.wq = [wq] + [wq.clone() for _ in range(self.copies - 1)]
+        self.ws = [ws] + [ws.clone() for _ in range(self.copies - 1)]
+        self.w_host = w
+        self.A = {M: workloads.to_bf16(workloads.normal(workloads.rng_for(seed, 1), (M, self.K), 1.0)).to(dev)
+                  for M in self.Ms}
+        self.C = {M: torch.empty((M, self.N), dtype=torch.bfloat16, device=dev) for M in self.Ms}
+        self.A_host = {M: self.A[M].cpu().pin_memory() for M in self.Ms}
+        self.C_host = {M: torch.empty((M, self.N), dtype=torch.bfloat16).pin_memory() for M in self.Ms}
+        self.h2d = sum(M * self.K * 2 for M in self.Ms)
+        self.d2h = sum(M * self.N * 2 for M in self.Ms)
+
+    def step(self, i):
+        for j, M in enumerate(self.Ms):
+            c = (3 * i + j) % self.copies
+            self.q4.gemm_w4a16_int4(self.A[M], self.wq[c], self.ws[c], out=self.C[M])
+
+    def kernel_only(self, i):
+        self.step(i)
+
+    kernel_units = units_per_step
+    kernel_launches = 3
+
+    def e2e_step(self, i):
+        for M in self.Ms:
+            self.A[M].copy_(self.A_host[M], non_blocking=True)
+        self.step(i)
+        for M in self.Ms:
+            self.C_host[M].copy_(self.C[M], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    # ---- oracle sample: the first `rows` weight rows, all three M
+    def oracle_prepare(self, rows):
+        import oracle
+        self.o_rows = rows
+        self.o_w = oracle.quantize_int4_g128(self.w_host[:rows])
+        self.o_a = {M: self.A_host[M].float().numpy() for M in self.Ms}
+
+    def oracle_step(self):
+        import oracle
+        for M in self.Ms:
+            oracle.gemm_w4a16_int4(self.o_a[M], *self.o_w)
+
+    def oracle_units(self):
+        return sum(self.bytes_per_gemm(M, self.o_rows) for M in self.Ms)
+
+    def oracle_sample_text(self):
+        return (f"first {self.o_rows} of {self.N} weight rows x M=1,4,16 "
+                f"(dequantize + FP64 GEMM; codes from the oracle's own quantizer)")
+
+    oracle_grain = 64
+
+
+class W4A4:
+    """W4A4 GEMM with A quantized on the fly; B pre-quantized (MMA scale layout)."""
+    nvfp4 = True
+
+    def setup_common(self, q4, dev, a_bf16, b_f32, a_copies=1, b_copies=1):
+        self.q4 = q4
+        self.M, self.K = a_bf16.shape
+        self.N = b_f32.shape[0]
+        bd = torch.from_numpy(b_f32).to(dev)
+        if self.nvfp4:
+            bc, bs, bg = q4.quantize_nvfp4(bd, scale_layout="mma")
+            bop = q4.Fp4Operand(bc, bs, "mma", bg)
+        else:
+            bc, bs = q4.quantize_mxfp4(bd, scale_layout="mma")
+            bop = q4.Fp4Operand(bc, bs, "mma", None)
+        del bd
+        self.B = [bop] + [q4.Fp4Operand(bop.codes.clone(), bop.scales.clone(), "mma",
+                                        None if bop.tensor_scale is None else bop.tensor_scale.clone())
+                          for _ in range(b_copies - 1)]
+        a = a_bf16.to(dev)
+        self.A = [a] + [a.clone() for _ in range(a_copies - 1)]
+        self.a_host = a_bf16
+        self.b_host = b_f32
+        op = q4.OP_GEMM_W4A4_NVFP4 if self.nvfp4 else q4.OP_GEMM_W4A4_MXFP4
+        self.ws = q4.workspace(op, self.M, self.N, self.K, dev)
+        self.C = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        self.fn = q4.gemm_w4a4_nvfp4 if self.nvfp4 else q4.gemm_w4a4_mxfp4
+        # pre-quantized copy of A for timing the GEMM kernel alone
+        if self.nvfp4:
+            ac, as_, ag = q4.quantize_nvfp4(self.A[0], scale_layout="mma")
+            self.Aq = q4.Fp4Operand(ac, as_, "mma", ag)
+        else:
+            ac, as_ = q4.quantize_mxfp4(self.A[0], scale_layout="mma")
+            self.Aq = q4.Fp4Operand(ac, as_, "mma", None)
+        self.A_pin = a_bf16.pin_memory()
+        self.C_host = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.M * self.K * 2
+        self.d2h = self.M * self.N * 2
+
+    launches_per_step = 3  # amax or memset-free quantize kernels + GEMM (see gpu_launches)
+
+    def step(self, i):
+        self.fn(self.A[i % len(self.A)], self.B[i % len(self.B)], self.K, out=self.C, ws=self.ws)
+
+    def kernel_only(self, i):
+        self.fn(self.Aq, self.B[i % len(self.B)], self.K, out=self.C, ws=self.ws)
+
+    kernel_launches = 1
+
+    def e2e_step(self, i):
+        self.A[0].copy_(self.A_pin, non_blocking=True)
+        self.fn(self.A[0], self.B[i % len(self.B)], self.K, out=self.C, ws=self.ws)
+        self.C_host.copy_(self.C, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def flops_per_step(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def bytes_per_step(self):
+        nsf = self.K // (16 if self.nvfp4 else 32)
+        return (self.M * self.K * 2 + self.N * self.K // 2 + self.N * nsf + self.M * self.N * 2)
+
+    def oracle_prepare(self, rows):
+        self.o_rows = rows
+        self.o_a = self.a_host.float().numpy()
+
+    def oracle_step(self):
+        import oracle
+        ra = np.arange(min(self.M, 64))
+        rb = np.arange(self.o_rows)
+        if self.nvfp4:
+            qa = oracle.quantize_nvfp4(self.o_a, rows=ra)
+            qb = oracle.quantize_nvfp4(self.b_host, rows=rb)
+            oracle.gemm_w4a4_nvfp4(*qa, *qb)
+        else:
+            qa = oracle.quantize_mxfp4(self.o_a, rows=ra)
+            qb = oracle.quantize_mxfp4(self.b_host, rows=rb)
+            oracle.gemm_w4a4_mxfp4(*qa, *qb)
+
+    def oracle_sample_text(self):
+        return (f"A rows 0..{min(self.M, 64) - 1} x B rows 0..{self.o_rows - 1}: quantize both "
+                f"(tensor scale over the whole operand) + FP64 GEMM")
+
+    oracle_grain = 128
+
+
+class Prefill(W4A4):
+    name = "nvfp4_prefill"
+    unit = "TFLOP/s"
+    bound = "tensor"
+    default_steps = 400
+    kernel = "fp4_gemm_kernel"
+    nvfp4 = True
+
+    def config(self):
+        return {"workload": "nvfp4_prefill A bf16 8192x8192 (quantized on the fly), B NVFP4 28672x8192",
+                "M": 8192, "N": 28672, "K": 8192, "l2": "inputs larger than L2 (A 134 MB bf16, B 132 MB)"}
+
+    def setup(self, q4, dev, seed):
+        a, b = workloads.prefill(seed)
+        self.setup_common(q4, dev, a, b)
+
+    def units_per_step(self):
+        return self.flops_per_step()
+
+    def kernel_units(self):
+        return self.flops_per_step()
+
+    def oracle_units(self):
+        return 2.0 * min(self.M, 64) * self.o_rows * self.K
+
+
+class Moe(W4A4):
+    name = "mxfp4_moe"
+    unit = "GB/s"
+    bound = "hbm"
+    default_steps = 5000
+    kernel = "fp4_gemm_kernel"
+    nvfp4 = False
+
+    def config(self):
+        return {"workload": "mxfp4_moe A bf16 256x7168 (0.5% channels x20, quantized on the fly), B MXFP4 2048x7168",
+                "M": 256, "N": 2048, "K": 7168, "l2": "rotating 8 A and 16 B copies (> L2)"}
+
+    def setup(self, q4, dev, seed):
+        a, b = workloads.moe(seed)
+        self.setup_common(q4, dev, a, b, a_copies=8, b_copies=16)
+
+    def units_per_step(self):
+        return self.bytes_per_step()
+
+    def kernel_units(self):
+        return self.N * self.K // 2 + self.N * self.K // 32 + self.M * self.K // 2 + self.M * self.K // 32 + self.M * self.N * 2
+
+    def oracle_units(self):
+        m = min(self.M, 64)
+        return m * self.K * 2 + self.o_rows * self.K // 2 + self.o_rows * self.K // 32 + m * self.o_rows * 2
+
+
+class Grouped:
+    """64-expert routed NVFP4 MoE: tokens quantized once, grouped tcgen05 GEMM."""
+    name = "grouped_moe"
+    unit = "GB/s"
+    bound = "hbm"
+    default_steps = 200
+    kernel = "grouped step (quantize tokens + routed scales + grouped GEMM)"
+    T, E, N, K, top = 4096, 64, 2048, 7168, 8
+    launches_per_step = 5  # amax, quantize, schedule, routed scales, grouped GEMM
+    kernel_launches = 5
+
+    def config(self):
+        return {"workload": "grouped_moe 64 experts NVFP4 2048x7168, 4096 bf16 tokens, top-8 routing",
+                "T": self.T, "E": self.E, "N": self.N, "K": self.K, "top_k": self.top,
+                "l2": "inputs larger than L2 (528 MB of expert weights)"}
+
+    def setup(self, q4, dev, seed):
+        self.q4 = q4
+        tok, _, offs, rt = workloads.grouped(seed, T=self.T, E=self.E, N=self.N, K=self.K,
+                                             top_k=self.top, experts=False)
+        self.R = int(offs[-1])
+        self.wc = torch.empty((self.E, self.N, self.K // 2), dtype=torch.uint8, device=dev)
+        sfb = q4.mma_scales_bytes(self.N, self.K // 16)
+        self.wsf = torch.empty(self.E * sfb, dtype=torch.uint8, device=dev)
+        self.wg = torch.empty(self.E, dtype=torch.float32, device=dev)
+        self.seed = seed
+        for e in range(self.E):
+            w = torch.from_numpy(workloads.expert_weight(seed, e, self.N, self.K)).to(dev)
+            c, s, g = q4.quantize_nvfp4(w, scale_layout="mma")
+            self.wc[e].copy_(c)
+            self.wsf[e * sfb:(e + 1) * sfb].copy_(s)
+            self.wg[e:e + 1].copy_(g)
+            del w
+        self.tok_host = tok
+        self.tok = tok.to(dev)
+        self.offs_h, self.rt_h = offs, rt
+        self.offs = torch.from_numpy(offs).to(dev)
+        self.rt = torch.from_numpy(rt).to(dev)
+        self.ws = q4.moe_workspace(self.T, self.N, self.K, self.E, self.R, dev)
+        self.C = torch.empty((self.R, self.N), dtype=torch.bfloat16, device=dev)
+        self.tok_pin = tok.pin_memory()
+        self.C_host = torch.empty((self.R, self.N), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.T * self.K * 2
+        self.d2h = self.R * self.N * 2
+
+    def step(self, i):
+        self.q4.grouped_gemm_moe(self.tok, self.offs, self.rt, self.wc, self.wsf, self.wg, self.N,
+                                 ws=self.ws, out=self.C)
+
+    kernel_only = step
+
+    def units_per_step(self):
+        return (self.E * self.N * self.K // 2 + self.E * self.N * self.K // 16 + self.T * self.K * 2
+                + self.R * self.N * 2)
+
+    kernel_units = units_per_step
+
+    def flops_per_step(self):
+        return 2.0 * self.R * self.N * self.K
+
+    def e2e_step(self, i):
+        self.tok.copy_(self.tok_pin, non_blocking=True)
+        self.step(i)
+        self.C_host.copy_(self.C, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def oracle_prepare(self, rows):
+        self.o_rows = rows
+        self.o_tok = self.tok_host.float().numpy()
+        self.o_w = workloads.expert_weight(self.seed, 0, self.N, self.K)
+
+    def oracle_step(self):
+        import oracle
+        r = self.rt_h[self.offs_h[0]:self.offs_h[0] + 64]
+        qa = oracle.quantize_nvfp4(self.o_tok, rows=r)
+        qb = oracle.quantize_nvfp4(self.o_w, rows=np.arange(self.o_rows))
+        oracle.gemm_w4a4_nvfp4(*qa, *qb)
+
+    def oracle_units(self):
+        return 64 * self.K * 2 + self.o_rows * self.K // 2 + self.o_rows * self.K // 16 + 64 * self.o_rows * 2
+
+    def oracle_sample_text(self):
+        return (f"64 routed rows of expert 0 x its first {self.o_rows} weight rows: quantize both + FP64 GEMM")
+
+    oracle_grain = 128
+
+
+WORKLOADS = {"decode": Decode, "prefill": Prefill, "moe": Moe, "grouped": Grouped}
+DTYPES = {"decode": "bf16 (exact int4 values) x bf16 -> fp32", "prefill": "e2m1 x e2m1 -> fp32",
+          "moe": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32"}
+
+
+def scale_units(x, unit):
+    return x / 1e9 if unit == "GB/s" else x / 1e12
+
+
+def time_oracle(wl, seconds: float):
+    """Time the oracle as it stands on a sample sized to about ``seconds``."""
+    rows = wl.oracle_grain
+    wl.oracle_prepare(rows)
+    t0 = time.perf_counter()
+    wl.oracle_step()
+    t1 = time.perf_counter() - t0
+    reps = max(1, int(seconds / max(t1, 1e-6)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        wl.oracle_step()
+    el = time.perf_counter() - t0
+    val = scale_units(wl.oracle_units() * reps / el, wl.unit)
+    return {"value": val, "unit": wl.unit, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{wl.oracle_sample_text()}; {reps} repetitions in {el:.1f} s; numpy "
+                      f"elementwise on 1 thread, FP64 matmul on the BLAS threads"}
+
+
+def chunk_for(K: int) -> int:
+    for g in range(min(K, 100), 0, -1):
+        if K % g == 0:
+            return g
+    return 1
+
+
+def run_reference(args, dist):
+    if dist.world > 1 and dist.rank != 0:
+        return
+    wl = WORKLOADS[args.workload]()
+    wl_setup_host(wl, args.seed)
+    K = args.steps or wl.default_steps
+    W = max(3, args.warmup)
+    # size the per-step sample so that the whole run takes about two minutes
+    wl.oracle_prepare(wl.oracle_grain)
+    t0 = time.perf_counter()
+    wl.oracle_step()
+    t1 = time.perf_counter() - t0
+    grains = max(1, int(120.0 / max((K + W) * t1, 1e-9)))
+    wl.oracle_prepare(wl.oracle_grain * min(grains, 64))
+    for _ in range(W):
+        wl.oracle_step()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        wl.oracle_step()
+    el = time.perf_counter() - t0
+    val = scale_units(wl.oracle_units() * K / el, wl.unit)
+    cfg = wl.config()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": wl.unit, "n_gpus": args.gpus,
+            "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": val, "unit": wl.unit,
+                             "sample": wl.oracle_sample_text() + " per step"},
+            "e2e": {"value": val, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def wl_setup_host(wl, seed):
+    """Host-only inputs for the oracle arm (no GPU needed)."""
+    if isinstance(wl, Decode):
+        wl.w_host = workloads.int4_weights(wl.N, wl.K, seed)
+        wl.A_host = {M: workloads.to_bf16(workloads.normal(workloads.rng_for(seed, 1), (M, wl.K), 1.0))
+                     for M in wl.Ms}
+    elif isinstance(wl, Grouped):
+        tok, _, offs, rt = workloads.grouped(seed, T=wl.T, E=wl.E, N=wl.N, K=wl.K, top_k=wl.top,
+                                             experts=False)
+        wl.tok_host, wl.offs_h, wl.rt_h, wl.seed = tok, offs, rt, seed
+    else:
+        a, b = workloads.prefill(seed) if isinstance(wl, Prefill) else workloads.moe(seed)
+        wl.a_host, wl.b_host = a, b
+        wl.M, wl.K = a.shape
+        wl.N = b.shape[0]
+
+
+SEEDS = {"decode": workloads.SEED_BASE + 2, "moe": workloads.SEED_BASE + 3,
+         "prefill": workloads.SEED_BASE + 4, "grouped": workloads.SEED_BASE + 5}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: per workload)")
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--oracle-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.seed is None:
+        args.seed = SEEDS[args.workload]
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+        return
+
+    dist.init(use_gpu=True)
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    import int4_gemm_gb300 as q4
+    q4.load()
+    wl = WORKLOADS[args.workload]()
+    wl.setup(q4, dev, args.seed)
+    K = args.steps or wl.default_steps
+    W = max(3, args.warmup)
+    for i in range(W):
+        wl.step(i)
+    torch.cuda.synchronize()
+    if q4.sync_status() != 0:
+        raise RuntimeError("a kernel reported an error during warm-up")
+
+    # the timed steps run as CUDA-graph replays of G steps each (K / G replays)
+    G = chunk_for(K)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(G):
+            wl.step(i)
+    graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else dist.local)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K // G):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    t = dist.max(e0.elapsed_time(e1) / 1e3)
+    total_units = dist.sum(wl.units_per_step() * K)
+    value = scale_units(total_units / t, wl.unit)
+    status = q4.sync_status()
+    if status != 0:
+        raise RuntimeError(f"a kernel reported status {status} during the timed steps")
+
+    # the dominant kernel alone, in the same graph form
+    pk, src = peaks()
+    if wl.bound == "hbm":
+        peak, punit = pk["hbm_gbs"], "GB/s"
+    else:
+        peak, punit = pk["bf16_tflops"] * FP4_OVER_BF16, "TFLOP/s"
+    kg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(kg):
+        for i in range(G):
+            wl.kernel_only(i)
+    kg.replay()
+    torch.cuda.synchronize()
+    reps = max(1, K // G // 2)
+    e0.record()
+    for _ in range(reps):
+        kg.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    launches = reps * G * wl.kernel_launches
+    avg_s = e0.elapsed_time(e1) / 1e3 / launches
+    per_launch = wl.kernel_units() / wl.kernel_launches
+    achieved = scale_units(per_launch / avg_s, punit)
+    roofline = {"bound": wl.bound, "achieved": achieved, "peak": peak, "unit": punit,
+                "frac": achieved / peak, "traffic": NCU_TRAFFIC.get(args.workload),
+                "kernel": wl.kernel, "avg_launch_us": avg_s * 1e6,
+                "peak_source": f"{src} ({'hbm_gbs' if punit == 'GB/s' else 'bf16_tflops x 6 (nominal FP4:BF16)'})"}
+
+    # end to end through the public API: host buffers, copies inside the timed region
+    n_e2e = min(K, 2000 if wl.unit == "GB/s" else 50)
+    for i in range(3):
+        wl.e2e_step(i)
+    dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        wl.e2e_step(i)
+    t_e2e = dist.max(time.perf_counter() - t0)
+    e2e_val = scale_units(dist.sum(wl.units_per_step() * n_e2e) / t_e2e, wl.unit)
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        cpu = time_oracle(wl, args.oracle_seconds)
+
+    if dist.rank == 0:
+        cfg = wl.config()
+        cfg["parallelism"] = f"replicas x{dist.world}" if dist.world > 1 else "single GPU"
+        line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": dist.world, "steps": K,
+                "warmup": W, "ms_per_step": t / K * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": DTYPES[args.workload], "data": "synthetic", "config": cfg,
+                "tflops": scale_units(dist.sum(wl.flops_per_step() * K) / t, "TFLOP/s"),
+                "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_val, "unit": wl.unit, "h2d_bytes_per_step": wl.h2d,
+                        "d2h_bytes_per_step": wl.d2h, "steps": n_e2e},
+                "gpu_launches": K * wl.launches_per_step, "clocks": clk,
+                "timing": f"CUDA events on the launching stream around {K // G} replays of a "
+                          f"{G}-step CUDA graph"}
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

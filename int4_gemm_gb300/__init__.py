@@ -193,25 +193,30 @@ def _operand(x: Union[torch.Tensor, Fp4Operand]) -> tuple[_Operand, int]:
     return _Operand(x.data_ptr(), _DTYPE[x.dtype], None, None, 0, None), x.shape[0]
 
 
-def _gemm_fp4(fn: str, op: int, A, B, K: int, out_dtype: torch.dtype, stream=None) -> torch.Tensor:
+def _gemm_fp4(fn: str, op: int, A, B, K: int, out_dtype: torch.dtype, stream=None, ws=None,
+              out=None) -> torch.Tensor:
     a, M = _operand(A)
     b, N = _operand(B)
     dev = (A.codes if isinstance(A, Fp4Operand) else A).device
-    C = torch.empty((M, N), dtype=out_dtype, device=dev)
-    ws = workspace(op, M, N, K, dev)
+    C = torch.empty((M, N), dtype=out_dtype, device=dev) if out is None else out
+    if ws is None:
+        ws = workspace(op, M, N, K, dev)
     _check(fn, getattr(lib(), fn)(ctypes.byref(a), ctypes.byref(b), M, N, K, C.data_ptr(),
                                   _DTYPE[out_dtype], ws.data_ptr(), ws.numel(), _stream(stream)))
     return C
 
 
-def gemm_w4a4_nvfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+def gemm_w4a4_nvfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None, ws=None,
+                    out=None) -> torch.Tensor:
     """C = A_hat . B_hat^T; A and B are raw tensors (quantized on the fly) or
-    Fp4Operand."""
-    return _gemm_fp4("gemm_w4a4_nvfp4", OP_GEMM_W4A4_NVFP4, A, B, K, out_dtype, stream)
+    Fp4Operand.  ``ws`` (from :func:`workspace`) and ``out`` may be given to
+    keep allocations out of a CUDA-graph capture."""
+    return _gemm_fp4("gemm_w4a4_nvfp4", OP_GEMM_W4A4_NVFP4, A, B, K, out_dtype, stream, ws, out)
 
 
-def gemm_w4a4_mxfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
-    return _gemm_fp4("gemm_w4a4_mxfp4", OP_GEMM_W4A4_MXFP4, A, B, K, out_dtype, stream)
+def gemm_w4a4_mxfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None, ws=None,
+                    out=None) -> torch.Tensor:
+    return _gemm_fp4("gemm_w4a4_mxfp4", OP_GEMM_W4A4_MXFP4, A, B, K, out_dtype, stream, ws, out)
 
 
 def gemm_w4a16_int4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=None,
