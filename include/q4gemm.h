@@ -65,6 +65,7 @@ typedef int q4_status;
 #define Q4_ERR_TIMEOUT (-4)           /* a kernel's bounded pipeline wait ran out */
 #define Q4_ERR_NONFINITE (-5)         /* a quantizer saw a NaN or infinite input */
 #define Q4_ERR_WORKSPACE (-6)         /* workspace missing, too small or misaligned */
+#define Q4_ERR_SCRATCH_TOO_SMALL (-7) /* problem exceeds the fixed scratch of a no-allocation call */
 
 typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
 typedef enum { Q4_SCALES_ROWMAJOR = 0, Q4_SCALES_MMA = 1 } q4_scale_layout;
@@ -202,6 +203,35 @@ q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            int E, const uint8_t* W_codes, const uint8_t* W_scales,
                            const float* W_tensor_scales, int64_t N, void* C_bf16, void* ws,
                            size_t ws_bytes, q4_stream_t stream);
+
+/*
+ * gemm_w4a4_nvfp4 without a workspace, for callers that cannot give the
+ * library any device memory beyond inputs and outputs: a plugin or custom-op
+ * interface that passes only input and output buffers, an engine whose memory
+ * pool is fully reserved at start-up, or code running while a stream is being
+ * captured (where cudaMalloc is not allowed).  The pages have no counterpart:
+ * this is a deployment convenience, not a step of the method.
+ *
+ * Computes exactly what gemm_w4a4_nvfp4 computes with A given raw (A [M, K]
+ * in a_dtype, NVFP4-quantized on the fly with its own tensor scale) and B
+ * pre-quantized with Q4_SCALES_MMA scales and a tensor scale.  The quantized
+ * activations live in one file-scope device array of
+ * q4_noalloc_scratch_bytes() (16 MiB) per GPU that loads the library, held
+ * until the process exits; a problem needing more (q4_noalloc_required_bytes(M,
+ * K): M * K / 2 code bytes plus its scales) returns Q4_ERR_SCRATCH_TOO_SMALL
+ * before anything is launched.  Nothing is allocated: no cudaMalloc, no
+ * cudaFree, no allocating library call.
+ *
+ * All calls share that array and it keeps the last call's contents, so calls
+ * that overlap on the GPU (several streams or host threads) race: serialize
+ * them.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make that
+ * first call before any stream capture.
+ */
+q4_status gemm_w4a4_nvfp4_noalloc(const void* A, int a_dtype, const q4_operand* B, int64_t M,
+                                  int64_t N, int64_t K, void* C, int c_dtype, q4_stream_t stream);
+size_t q4_noalloc_scratch_bytes(void);
+size_t q4_noalloc_required_bytes(int64_t M, int64_t K);
 
 /*
  * Synchronizes the stream, then returns (and clears) the first error a kernel

@@ -74,6 +74,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "q4_sync_status", I, P)
     _sig(lib, "q4_status_string", ctypes.c_char_p, I)
     _sig(lib, "q4_set_wait_timeout_ms", I, I)
+    _sig(lib, "gemm_w4a4_nvfp4_noalloc", I, P, I, op, I64, I64, I64, P, I, P)
+    _sig(lib, "q4_noalloc_scratch_bytes", SZ)
+    _sig(lib, "q4_noalloc_required_bytes", SZ, I64, I64)
     _lib = lib
     return lib
 
@@ -217,6 +220,22 @@ def gemm_w4a4_nvfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None, ws=None
 def gemm_w4a4_mxfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None, ws=None,
                     out=None) -> torch.Tensor:
     return _gemm_fp4("gemm_w4a4_mxfp4", OP_GEMM_W4A4_MXFP4, A, B, K, out_dtype, stream, ws, out)
+
+
+def gemm_w4a4_nvfp4_noalloc(A: torch.Tensor, B: Fp4Operand, K: int, out_dtype=torch.bfloat16,
+                            out=None, stream=None) -> torch.Tensor:
+    """gemm_w4a4_nvfp4 with raw activations for callers that cannot provide a
+    workspace: the quantized activations go to the library's fixed 16 MiB
+    per-GPU scratch array (see include/q4gemm.h).  B must carry MMA-layout
+    scales.  Calls that overlap on the GPU share that scratch and race."""
+    _cuda2d(A, "A")
+    M = A.shape[0]
+    b, N = _operand(B)
+    C = torch.empty((M, N), dtype=out_dtype, device=A.device) if out is None else out
+    _check("gemm_w4a4_nvfp4_noalloc", lib().gemm_w4a4_nvfp4_noalloc(
+        A.data_ptr(), _DTYPE[A.dtype], ctypes.byref(b), M, N, K, C.data_ptr(), _DTYPE[out_dtype],
+        _stream(stream)))
+    return C
 
 
 def gemm_w4a16_int4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=None,

@@ -406,6 +406,8 @@ const char* q4_status_string(q4_status s) {
     case Q4_ERR_TIMEOUT: return "kernel wait timed out";
     case Q4_ERR_NONFINITE: return "non-finite input";
     case Q4_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case Q4_ERR_SCRATCH_TOO_SMALL:
+      return "problem larger than the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }
