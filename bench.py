@@ -198,8 +198,10 @@ class Decode:
 
     launches_per_step = 3
 
-    def setup(self, q4, dev, seed):
+    def setup(self, q4, dev, seed, shape=None):
         self.q4 = q4
+        if shape:
+            self.N, self.K = shape[1], shape[2]
         w = workloads.int4_weights(self.N, self.K, seed)
         wd = torch.from_numpy(w).to(dev)
         wq, ws = q4.quantize_int4_g128(wd)
@@ -351,11 +353,11 @@ class Prefill(W4A4):
     nvfp4 = True
 
     def config(self):
-        return {"workload": "nvfp4_prefill A bf16 8192x8192 (quantized on the fly), B NVFP4 28672x8192",
-                "M": 8192, "N": 28672, "K": 8192, "l2": "inputs larger than L2 (A 134 MB bf16, B 132 MB)"}
+        return {"workload": f"nvfp4_prefill A bf16 {self.M}x{self.K} (quantized on the fly), B NVFP4 {self.N}x{self.K}",
+                "M": self.M, "N": self.N, "K": self.K, "l2": "inputs larger than L2 (A 134 MB bf16, B 132 MB)"}
 
-    def setup(self, q4, dev, seed):
-        a, b = workloads.prefill(seed)
+    def setup(self, q4, dev, seed, shape=None):
+        a, b = workloads.prefill(seed, *(shape or ()))
         self.setup_common(q4, dev, a, b)
 
     def units_per_step(self):
@@ -377,11 +379,11 @@ class Moe(W4A4):
     nvfp4 = False
 
     def config(self):
-        return {"workload": "mxfp4_moe A bf16 256x7168 (0.5% channels x20, quantized on the fly), B MXFP4 2048x7168",
-                "M": 256, "N": 2048, "K": 7168, "l2": "rotating 8 A and 16 B copies (> L2)"}
+        return {"workload": f"mxfp4_moe A bf16 {self.M}x{self.K} (0.5% channels x20, quantized on the fly), B MXFP4 {self.N}x{self.K}",
+                "M": self.M, "N": self.N, "K": self.K, "l2": "rotating 8 A and 16 B copies (> L2)"}
 
-    def setup(self, q4, dev, seed):
-        a, b = workloads.moe(seed)
+    def setup(self, q4, dev, seed, shape=None):
+        a, b = workloads.moe(seed, *(shape or ()))
         self.setup_common(q4, dev, a, b, a_copies=8, b_copies=16)
 
     def units_per_step(self):
@@ -411,7 +413,7 @@ class Grouped:
                 "T": self.T, "E": self.E, "N": self.N, "K": self.K, "top_k": self.top,
                 "l2": "inputs larger than L2 (528 MB of expert weights)"}
 
-    def setup(self, q4, dev, seed):
+    def setup(self, q4, dev, seed, shape=None):
         self.q4 = q4
         tok, _, offs, rt = workloads.grouped(seed, T=self.T, E=self.E, N=self.N, K=self.K,
                                              top_k=self.top, experts=False)
@@ -578,6 +580,8 @@ def main():
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K override (a smaller case of the same code path, e.g. for profiling)")
     args = ap.parse_args()
     if args.seed is None:
         args.seed = SEEDS[args.workload]
@@ -592,7 +596,8 @@ def main():
     import int4_gemm_gb300 as q4
     q4.load()
     wl = WORKLOADS[args.workload]()
-    wl.setup(q4, dev, args.seed)
+    shape = tuple(int(v) for v in args.shape.split(",")) if args.shape else None
+    wl.setup(q4, dev, args.seed, shape)
     K = args.steps or wl.default_steps
     W = max(3, args.warmup)
     for i in range(W):
