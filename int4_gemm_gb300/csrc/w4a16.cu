@@ -26,29 +26,52 @@
 namespace q4 {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRows = 128;      // weight rows (n) per CTA: 4 warps x 2 tiles x 16
+constexpr int kRows = 256;      // weight rows (n) per CTA: 8 warps x 2 tiles x 16
 constexpr int kTok = 16;        // tokens per CTA (two n8 MMA tiles)
 constexpr int kChunk = 8;       // groups of 128 staged per activation chunk
-constexpr int kActBytes = kChunk * 4 * kTok * 4 * 16;  // 32 KiB
-constexpr int kRedBytes = kRows * kTok * 4;           // 8 KiB
+constexpr int kRing = 4;        // weight groups in flight per thread (cp.async ring)
+constexpr int kActBytes = kChunk * 4 * kTok * 4 * 16;   // 32 KiB
+constexpr int kRingBytes = kRing * 4 * kThreads * 16;   // 64 KiB: [slot][chunk][thread] x 16 B
+constexpr int kRedBytes = kRows * kTok * 4;             // 16 KiB (aliases the ring at the end)
+constexpr int kSumBytes = kChunk * kTok * 4;            // 512 B: 136 * sum of a per group, token
+static_assert(kRedBytes <= kRingBytes, "");
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(dst),
+      "l"(src), "r"((int)pred)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Two nibbles at bits 0..3 and 16..19 of w -> bf16x2 of 136 + q, exactly:
+// (n ^ 8) | 0x4300 is the bf16 of 128 + (q + 8).  The offset 136 is removed
+// after the MMA, per group and token, as 136 * sum_k a[m, k].
+__device__ __forceinline__ uint32_t nib_pair_to_bf16x2(uint32_t w) {
+  uint32_t t;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43084308, 0x6A;" : "=r"(t) : "r"(w));
+  return t;
 }
 
-// Two nibbles at bits 0..3 and 16..19 of w -> bf16x2 holding the signed
-// values: (n ^ 8) | 0x4300 is the bf16 of 128 + (q + 8); minus 136 leaves q.
-__device__ __forceinline__ uint32_t nib_pair_to_bf16x2(uint32_t w) {
-  uint32_t t, r;
-  asm("lop3.b32 %0, %1, 0x000F000F, 0x43084308, 0x6A;" : "=r"(t) : "r"(w));
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
-  return r;
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t a, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  return ra;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -70,31 +93,31 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  uint32_t a = smem_u32(local), ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-  return v;
-}
 
-// grid = (CS, ceil(N / 128), ceil(M / 16)), cluster = (CS, 1, 1).
-__global__ void __launch_bounds__(kThreads)
+// grid = (CS, ceil(N / 256), ceil(M / 16)), cluster = (CS, 1, 1).  TS = token
+// sets of 8 (1 when at most 8 tokens per block, else 2).
+template <int TS>
+__global__ void __launch_bounds__(kThreads, 2)
     w4a16_kernel(const __nv_bfloat16* __restrict__ A, const uint8_t* __restrict__ Wq,
                  const uint16_t* __restrict__ Ws, __nv_bfloat16* __restrict__ C, int M, int N,
                  int K, int groups_per_cta) {
+  constexpr int kTp = 8 * TS;  // tokens staged per CTA
   extern __shared__ __align__(16) uint8_t smem[];
-  uint4* act = reinterpret_cast<uint4*>(smem);                    // [kChunk][4][kTok][4] x 16B
-  float* red = reinterpret_cast<float*>(smem + kActBytes);       // [kRows][kTok]
+  uint8_t* ring = smem;                                              // [slot][chunk][thread] x 16 B
+  uint4* act = reinterpret_cast<uint4*>(smem + kRingBytes);         // [kChunk][4][kTp][4] x 16 B
+  float* csum = reinterpret_cast<float*>(smem + kRingBytes + kActBytes);  // [kChunk][kTok]
+  float* red = reinterpret_cast<float*>(smem);                       // [kRows][kTok], at the end
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quad = lane & 3, lrow = lane >> 2;
   const int cs = gridDim.x, rank = blockIdx.x;
   const int n_base = blockIdx.y * kRows;
   const int m0 = blockIdx.z * kTok;
+  const int mt = min(M - m0, kTp);  // tokens present in this CTA
   const int ngroups = K / 128;
   const int g_begin = min(ngroups, rank * groups_per_cta);
   const int g_end = min(ngroups, g_begin + groups_per_cta);
+  const int ng = g_end - g_begin;
   const int64_t wrow_bytes = K / 2;
 
   // this thread's four weight rows: tile t (0,1) x half h (0: lrow, 1: lrow + 8)
@@ -105,110 +128,179 @@ __global__ void __launch_bounds__(kThreads)
     wrow[i] = n_base + warp * 32 + (i >> 1) * 16 + (i & 1) * 8 + lrow;
     wok[i] = wrow[i] < N;
   }
+  const uint32_t ring_base = smem_u32(ring);
+  // group gi of this CTA's slice -> ring slot gi % kRing; a commit group per call
+  auto issue = [&](int gi) {
+    const int slot = gi % kRing;
+    const bool live = gi < ng;
+    const int g = g_begin + (live ? gi : 0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      cp_async16(ring_base + (uint32_t)(((slot * 4 + i) * kThreads + tid) * 16),
+                 Wq + (int64_t)(wok[i] ? wrow[i] : 0) * wrow_bytes + g * 64 + quad * 16,
+                 live && wok[i]);
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int gi = 0; gi < kRing; ++gi) issue(gi);
 
-  float acc[2][2][4];  // [tile][token set][fragment]
+  float acc[2][TS][4];  // [tile][token set][fragment]
 #pragma unroll
   for (int t = 0; t < 2; ++t)
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
+    for (int s = 0; s < TS; ++s)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[t][s][i] = 0.f;
 
-  for (int c0 = g_begin; c0 < g_end; c0 += kChunk) {
-    const int gc = min(kChunk, g_end - c0);
-    // ---- stage the activations of groups [c0, c0 + gc), permuted per fragment
-    __syncthreads();
-    const int slots = gc * 16 * kTok;  // 16-byte global chunks
-    for (int s = tid; s < slots; s += kThreads) {
-      const int tok = s / (gc * 16), q = s % (gc * 16);
-      const int gi = q >> 4, cq = (q >> 2) & 3, w = q & 3;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (m0 + tok < M) {
-        const uint4 x = *reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K +
-                                                        (int64_t)c0 * 128 + q * 8);
-        // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}
-        v.x = __byte_perm(x.x, x.z, 0x5410);
-        v.y = __byte_perm(x.x, x.z, 0x7632);
-        v.z = __byte_perm(x.y, x.w, 0x5410);
-        v.w = __byte_perm(x.y, x.w, 0x7632);
+  for (int gi0 = 0; gi0 < ng; gi0 += kChunk) {
+    const int gc = min(kChunk, ng - gi0);
+    const int c0 = g_begin + gi0;
+    // ---- FP16 scales of this thread's rows for the chunk (eight per row)
+    uint32_t spk[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t* src = Ws + (int64_t)(wok[i] ? wrow[i] : 0) * ngroups + c0;
+      if (gc == kChunk && (ngroups & 7) == 0) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+        spk[i][0] = v.x; spk[i][1] = v.y; spk[i][2] = v.z; spk[i][3] = v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = 2 * e < gc ? __ldg(src + 2 * e) : 0u;
+          const uint32_t hi = 2 * e + 1 < gc ? __ldg(src + 2 * e + 1) : 0u;
+          spk[i][e] = lo | (hi << 16);
+        }
       }
-      act[((gi * 4 + w) * kTok + tok) * 4 + cq] = v;
+    }
+
+    // ---- stage the present tokens' activations, permuted per fragment
+    __syncthreads();
+    const int per_tok = gc * 16;  // 16-byte chunks per token
+    const int slots = mt * per_tok;
+    for (int base = 0; base < slots; base += 4 * kThreads) {
+      uint4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sl = base + u * kThreads + tid;
+        if (sl < slots) {
+          const int tok = sl / per_tok, q = sl % per_tok;
+          x[u] = *reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K + (int64_t)c0 * 128 + q * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sl = base + u * kThreads + tid;
+        if (sl < slots) {
+          const int tok = sl / per_tok, q = sl % per_tok;
+          const int gi = q >> 4, cq = (q >> 2) & 3, w = q & 3;
+          uint4 v;
+          // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}
+          v.x = __byte_perm(x[u].x, x[u].z, 0x5410);
+          v.y = __byte_perm(x[u].x, x[u].z, 0x7632);
+          v.z = __byte_perm(x[u].y, x[u].w, 0x5410);
+          v.w = __byte_perm(x[u].y, x[u].w, 0x7632);
+          act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
+        }
+      }
+    }
+    __syncthreads();
+    // 136 * sum_k a[tok, k] per group, summed in a fixed order (deterministic)
+    if (tid < gc * kTp) {
+      const int gi = tid / kTp, tok = tid % kTp;
+      float sum = 0.f;
+      if (tok < mt) {
+#pragma unroll 4
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+          for (int cq = 0; cq < 4; ++cq) {
+            const uint4 v = act[((gi * 4 + w) * kTp + tok) * 4 + cq];
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              sum += __uint_as_float(u[e] << 16) + __uint_as_float(u[e] & 0xFFFF0000u);
+          }
+      }
+      csum[gi * kTok + tok] = 136.0f * sum;
     }
     __syncthreads();
 
-    // ---- stream the weights: a three-deep register ring, two groups ahead
-    uint4 wr[3][4];
-    uint16_t sr[3][4];
-    auto load_group = [&](int gi, int slot) {
-      const int g = c0 + gi;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (gi < gc && wok[i]) {
-          wr[slot][i] = ldg_stream(Wq + (int64_t)wrow[i] * wrow_bytes + g * 64 + quad * 16);
-          sr[slot][i] = __ldg(Ws + (int64_t)wrow[i] * ngroups + g);
-        } else {
-          wr[slot][i] = make_uint4(0, 0, 0, 0);
-          sr[slot][i] = 0;
-        }
-      }
-    };
-    load_group(0, 0);
-    load_group(1, 1);
+    for (int gl = 0; gl < kChunk; ++gl) {
+      if (gl < gc) {
+        const int gi = gi0 + gl;
+        cp_async_wait<kRing - 1>();  // this thread's copies of group gi have landed
+        const int slot = gi % kRing;
+        uint4 wv[4];
 #pragma unroll
-    for (int gi = 0; gi < kChunk; ++gi) {
-      if (gi + 2 < kChunk) load_group(gi + 2, (gi + 2) % 3);
-      if (gi < gc) {
-        const int slot = gi % 3;
-        float part[2][2][4];
+        for (int i = 0; i < 4; ++i)
+          wv[i] = *reinterpret_cast<const uint4*>(ring + ((slot * 4 + i) * kThreads + tid) * 16);
+        float part[2][TS][4];
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int s = 0; s < 2; ++s)
+          for (int s = 0; s < TS; ++s)
 #pragma unroll
             for (int i = 0; i < 4; ++i) part[t][s][i] = 0.f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const uint4 b0 = act[((gi * 4 + w) * kTok + lrow) * 4 + quad];
-          const uint4 b1 = act[((gi * 4 + w) * kTok + lrow + 8) * 4 + quad];
+          uint4 bf[TS];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t bb0 = h ? b0.z : b0.x, bb1 = h ? b0.w : b0.y;
-            const uint32_t bc0 = h ? b1.z : b1.x, bc1 = h ? b1.w : b1.y;
+          for (int s = 0; s < TS; ++s) bf[s] = act[((gl * 4 + w) * kTp + lrow + 8 * s) * 4 + quad];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const uint32_t wlo = word(wr[slot][2 * t], w) >> (8 * h);
-              const uint32_t whi = word(wr[slot][2 * t + 1], w) >> (8 * h);
-              const uint32_t a0 = nib_pair_to_bf16x2(wlo);
-              const uint32_t a1 = nib_pair_to_bf16x2(whi);
-              const uint32_t a2 = nib_pair_to_bf16x2(wlo >> 4);
-              const uint32_t a3 = nib_pair_to_bf16x2(whi >> 4);
-              mma_bf16_16816(part[t][0], a0, a1, a2, a3, bb0, bb1);
-              if (M - m0 > 8) mma_bf16_16816(part[t][1], a0, a1, a2, a3, bc0, bc1);
-            }
+          for (int t = 0; t < 2; ++t) {
+            // nibble pairs (i, i + 4) of the row's word sit at bits 4i.. and 16 + 4i..
+            const uint32_t lo = word(wv[2 * t], w), hi = word(wv[2 * t + 1], w);
+            uint32_t pl[4], ph[4];
+            pl[0] = nib_pair_to_bf16x2(lo);
+            pl[1] = nib_pair_to_bf16x2(lo >> 4);
+            pl[2] = nib_pair_to_bf16x2(lo >> 8);
+            pl[3] = nib_pair_to_bf16x2(lo >> 12);
+            ph[0] = nib_pair_to_bf16x2(hi);
+            ph[1] = nib_pair_to_bf16x2(hi >> 4);
+            ph[2] = nib_pair_to_bf16x2(hi >> 8);
+            ph[3] = nib_pair_to_bf16x2(hi >> 12);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int s = 0; s < TS; ++s)
+                mma_bf16_16816(part[t][s], pl[2 * h], ph[2 * h], pl[2 * h + 1], ph[2 * h + 1],
+                               h ? bf[s].z : bf[s].x, h ? bf[s].w : bf[s].y);
           }
         }
-        // per-group promotion: FP32 multiply by the FP16 scale of each row
+        issue(gi + kRing);  // refill the slot just read (the registers hold its data)
+        // per-group promotion: remove the offset, then one FP32 multiply by the
+        // FP16 scale of each row
+        float c0v[TS], c1v[TS];
+#pragma unroll
+        for (int s = 0; s < TS; ++s) {
+          const float2 cc = *reinterpret_cast<const float2*>(&csum[gl * kTok + s * 8 + 2 * quad]);
+          c0v[s] = cc.x;
+          c1v[s] = cc.y;
+        }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const float slo = __half2float(__ushort_as_half(sr[slot][2 * t]));
-          const float shi = __half2float(__ushort_as_half(sr[slot][2 * t + 1]));
+          const uint32_t plo = spk[2 * t][gl >> 1], phi = spk[2 * t + 1][gl >> 1];
+          const float slo = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? plo >> 16 : plo)));
+          const float shi = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? phi >> 16 : phi)));
 #pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            acc[t][s][0] = fmaf(part[t][s][0], slo, acc[t][s][0]);
-            acc[t][s][1] = fmaf(part[t][s][1], slo, acc[t][s][1]);
-            acc[t][s][2] = fmaf(part[t][s][2], shi, acc[t][s][2]);
-            acc[t][s][3] = fmaf(part[t][s][3], shi, acc[t][s][3]);
+          for (int s = 0; s < TS; ++s) {
+            acc[t][s][0] = fmaf(part[t][s][0] - c0v[s], slo, acc[t][s][0]);
+            acc[t][s][1] = fmaf(part[t][s][1] - c1v[s], slo, acc[t][s][1]);
+            acc[t][s][2] = fmaf(part[t][s][2] - c0v[s], shi, acc[t][s][2]);
+            acc[t][s][3] = fmaf(part[t][s][3] - c1v[s], shi, acc[t][s][3]);
           }
         }
       }
     }
   }
+  cp_async_wait<0>();
+  __syncthreads();  // every thread is done with the ring before it becomes red
 
   // ---- partial sums to shared memory: red[row][token]
 #pragma unroll
   for (int t = 0; t < 2; ++t)
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < TS; ++s) {
       const int r = warp * 32 + t * 16 + lrow;
       const int tk = s * 8 + quad * 2;
       red[r * kTok + tk] = acc[t][s][0];
@@ -221,12 +313,23 @@ __global__ void __launch_bounds__(kThreads)
   // ---- rank q reduces rows [q * per, (q + 1) * per) over all ranks, in rank order
   const int per = (kRows + cs - 1) / cs;
   const int r_lo = rank * per, r_hi = min(kRows, r_lo + per);
-  for (int e = tid; e < (r_hi - r_lo) * kTok; e += kThreads) {
-    const int tk = e % kTok, r = r_lo + e / kTok;
-    float s = 0.f;
-    for (int q = 0; q < cs; ++q) s += ld_dsmem_f32(&red[r * kTok + tk], (uint32_t)q);
-    const int n = n_base + r, m = m0 + tk;
-    if (n < N && m < M) C[(int64_t)m * N + n] = __float2bfloat16_rn(s);
+  const int tq = (mt + 3) / 4;  // groups of four tokens
+  const uint32_t red_base = smem_u32(red);
+  for (int e = tid; e < (r_hi - r_lo) * tq; e += kThreads) {
+    const int t4 = e / (r_hi - r_lo), r = r_lo + e % (r_hi - r_lo);
+    const uint32_t off = (uint32_t)(r * kTok + 4 * t4) * 4u;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < cs; ++q) {
+      const float4 v = ld_dsmem_f32x4(mapa_u32(red_base, (uint32_t)q) + off);
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    }
+    const int n = n_base + r;
+    if (n < N) {
+      const float vv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * t4 + i < mt) C[(int64_t)(m0 + 4 * t4 + i) * N + n] = __float2bfloat16_rn(vv[i]);
+    }
   }
   cluster_sync();
 }
@@ -238,14 +341,19 @@ q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int
   if (M == 0 || N == 0) return Q4_OK;
   const int ngroups = (int)(K / 128);
   // split K over a cluster of up to 8 CTAs, at least one group each
-  const int cs = std::max(1, std::min(8, ngroups));
-  const int gpc = (int)ceil_div(ngroups, cs);
-  const size_t smem = kActBytes + kRedBytes;
+  // groups per CTA: a multiple of 8 (aligned 16-byte scale loads), at most 8
+  // CTAs per cluster
+  int cs = std::max(1, std::min(8, (int)ceil_div(ngroups, 8)));
+  const int gpc = (int)(ceil_div(ceil_div(ngroups, cs), 8) * 8);
+  cs = (int)ceil_div(ngroups, gpc);
+  const size_t smem = kRingBytes + kActBytes + kSumBytes;
   static int attr_done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!attr_done[dev]) {
-    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem));
+    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem));
     attr_done[dev] = 1;
   }
@@ -261,8 +369,13 @@ q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel, (const __nv_bfloat16*)A, Wq, Ws,
-                                 (__nv_bfloat16*)C, (int)M, (int)N, (int)K, gpc));
+  // one token set of 8 when every token block has at most 8 tokens
+  if (M <= 8)
+    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel<1>, (const __nv_bfloat16*)A, Wq, Ws,
+                                   (__nv_bfloat16*)C, (int)M, (int)N, (int)K, gpc));
+  else
+    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel<2>, (const __nv_bfloat16*)A, Wq, Ws,
+                                   (__nv_bfloat16*)C, (int)M, (int)N, (int)K, gpc));
   return Q4_OK;
 }
 
