@@ -86,13 +86,19 @@ struct Params {
   KernelCtl ctl;
 };
 
-__device__ __forceinline__ TileInfo dense_tile(const Params& p, int t) {
-  constexpr int GM = 16;  // m tiles per band: a band's A tiles stay in L2 while B streams
+// Dense tiles for a cluster of CM CTAs stacked along M (they share the B tile):
+// cluster tile t -> (m group, n) in bands of 16 M tiles, so a band's A tiles
+// stay in L2 while B streams; CTA rank r takes M tile group * CM + r.
+template <int CM>
+__device__ __forceinline__ TileInfo dense_tile(const Params& p, int t, int crank) {
+  constexpr int GMG = 16 / CM;  // m groups per band
+  const int num_mg = (p.num_m + CM - 1) / CM;
   TileInfo ti;
-  const int band_tiles = GM * p.num_n;
+  const int band_tiles = GMG * p.num_n;
   const int band = t / band_tiles, r = t % band_tiles;
-  const int gm = min(GM, p.num_m - band * GM);
-  const int m = band * GM + r % gm, n = r / gm;
+  const int gm = min(GMG, num_mg - band * GMG);
+  const int mg = band * GMG + r % gm, n = r / gm;
+  const int m = mg * CM + crank;
   ti.m_row0 = m * BM;
   ti.m_end = (int)p.M;
   ti.n0 = n * BN;
@@ -120,7 +126,7 @@ __device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sch
 }
 
 
-template <bool NV, bool GROUPED>
+template <bool NV, bool GROUPED, int CM>
 __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -134,6 +140,10 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (int)(p.K / BK);
+  static_assert(!GROUPED || CM == 1, "");
+  const int crank = CM > 1 ? (int)cluster_ctarank() : 0;  // rank along M in the cluster
+  const int cid = blockIdx.x / CM, ncl = gridDim.x / CM;   // cluster index and count
+  constexpr uint16_t kMask = (uint16_t)((1u << CM) - 1u);
 
   int total_tiles;
   if constexpr (GROUPED) {
@@ -141,13 +151,13 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     __syncthreads();
     total_tiles = s_sched[p.E] * p.num_n;
   } else {
-    total_tiles = p.num_m * p.num_n;
+    total_tiles = ((p.num_m + CM - 1) / CM) * p.num_n;
   }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm->full[s]), GROUPED ? 1 + kGatherThreads : 1);
-      mbar_init(smem_u32(&sm->empty[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), CM);  // every CTA of the cluster releases
     }
     mbar_init(smem_u32(&sm->acc_full), 1);
     mbar_init(smem_u32(&sm->acc_empty), 4);
@@ -163,13 +173,14 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CM > 1) cluster_barrier_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort_flag = &sm->abort;
 
   auto tile_at = [&](int t) -> TileInfo {
     if constexpr (GROUPED) return grouped_tile(p, s_sched, t);
-    else return dense_tile(p, t);
+    else return dense_tile<CM>(p, t, crank);
   };
 
   if (warp == 0) {
@@ -181,14 +192,15 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     bool alive = true;
     const int nsf4_a = (int)((p.K / (NV ? 16 : 32) + 3) / 4);
     const int nblk_b = (int)((p.N + 127) / 128);
-    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
+      const bool a_sf_ok = ti.sf_block < (GROUPED ? (1 << 30) : p.num_m);  // a CTA past M loads no scales
       const uint8_t* sfa = p.a_sf + (int64_t)ti.sf_block * nsf4_a * 512;
       const uint8_t* sfb = p.b_sf + (int64_t)ti.e * p.b_sf_expert_bytes;
       const int nb0 = ti.n0 / 128;
       const bool b_hi = nb0 + 1 < nblk_b;
-      const uint32_t bytes = (GROUPED ? 0u : kABytes) + kBBytes + C_::kSfaBytes +
+      const uint32_t bytes = (GROUPED ? 0u : kABytes) + kBBytes + (a_sf_ok ? C_::kSfaBytes : 0u) +
                              C_::kSfaBytes * (b_hi ? 2 : 1);
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
       for (int kb = 0; kb < nkb; ++kb) {
@@ -201,14 +213,25 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
           if constexpr (!GROUPED) tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
-          tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2), b_row, full);
           const int64_t jsf = (int64_t)kb * C_::kSfChunks * 512;
-          bulk_load(smem_u32(st + kABytes + kBBytes), sfa + jsf, C_::kSfaBytes, full);
+          if (a_sf_ok) bulk_load(smem_u32(st + kABytes + kBBytes), sfa + jsf, C_::kSfaBytes, full);
           const uint8_t* sfb0 = sfb + (int64_t)nb0 * nsf4_a * 512 + jsf;
-          bulk_load(smem_u32(st + kABytes + kBBytes + C_::kSfaBytes), sfb0, C_::kSfaBytes, full);
-          if (b_hi)
-            bulk_load(smem_u32(st + kABytes + kBBytes + 2 * C_::kSfaBytes), sfb0 + nsf4_a * 512,
-                      C_::kSfaBytes, full);
+          const uint32_t sfb_s = smem_u32(st + kABytes + kBBytes + C_::kSfaBytes);
+          if constexpr (CM == 1) {
+            tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2), b_row, full);
+            bulk_load(sfb_s, sfb0, C_::kSfaBytes, full);
+            if (b_hi) bulk_load(sfb_s + C_::kSfaBytes, sfb0 + nsf4_a * 512, C_::kSfaBytes, full);
+          } else {
+            // this rank's slice of the shared B tile and of its scales, to every CTA
+            constexpr int kSlice = BN / CM;
+            tma_load_2d_mc(smem_u32(st + kABytes + crank * kSlice * (BK / 2)), &tmap_b, kb * (BK / 2),
+                           b_row + crank * kSlice, full, kMask);
+            constexpr uint32_t kPart = C_::kSfaBytes * 2 / CM;  // scale bytes per rank
+            const int h = (int)(crank * kPart / C_::kSfaBytes);  // 128-row half of the B tile
+            const uint32_t off = crank * kPart - (uint32_t)h * C_::kSfaBytes;
+            if (h == 0 || b_hi)
+              bulk_load_mc(sfb_s + crank * kPart, sfb0 + (int64_t)h * nsf4_a * 512 + off, kPart, full, kMask);
+          }
         }
         issued[stage] = 1;
         issued_phase[stage] = phase;
@@ -227,7 +250,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     uint32_t stage = 0, phase = 0, tcount = 0;
     bool alive = true;
     if (lane == 0) {
-      for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x, ++tcount) {
+      for (int t = cid; t < total_tiles && alive; t += ncl, ++tcount) {
         const TileInfo ti = tile_at(t);
         if (!ti.ok) { --tcount; continue; }
         if (!mbar_wait(smem_u32(&sm->acc_empty), (tcount & 1) ^ 1, p.ctl, abort_flag)) {
@@ -262,7 +285,8 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
             tc_mma_fp4<NV ? 4 : 2>(tmem, ad, bd, idesc, sf_t + 4 * j, sf_t + 16 + 8 * j,
                                    (kb | k) != 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&sm->empty[stage]));
+          if constexpr (CM == 1) tc_commit(smem_u32(&sm->empty[stage]));
+          else tc_commit_mc(smem_u32(&sm->empty[stage]), kMask);
           if (++stage == kStages) stage = 0, phase ^= 1;
         }
         if (!alive) break;
@@ -282,7 +306,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     const int i = threadIdx.x - kThreads;
     uint32_t stage = 0, phase = 0;
     bool alive = true;
-    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
       const int r = ti.m_row0 + i;
@@ -310,7 +334,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint32_t tcount = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    for (int t = cid; t < total_tiles; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
       if (!mbar_wait(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
@@ -376,6 +400,8 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // no CTA leaves while a peer may still multicast into it or arrive on its barriers
+  if constexpr (CM > 1) cluster_barrier_sync();
 }
 
 // ------------------------------------------------------------------ grouped prep
@@ -421,13 +447,13 @@ __global__ void __launch_bounds__(128)
 
 namespace {
 
-template <bool NV, bool GROUPED>
+template <bool NV, bool GROUPED, int CM>
 q4_status set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!done[dev]) {
-    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED>,
+    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, CM>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)Cfg<NV>::kSmemBytes));
     done[dev] = 1;
@@ -435,14 +461,59 @@ q4_status set_smem_attr() {
   return Q4_OK;
 }
 
+template <bool NV, int CM>
+q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                       cudaStream_t stream) {
+  q4_status st;
+  if ((st = set_smem_attr<NV, false, CM>()) != Q4_OK) return st;
+  const int ctiles = ((p.num_m + CM - 1) / CM) * p.num_n;  // cluster tiles
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<NV>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent clusters: exactly as many as can be resident at once, so no
+  // cluster waits for a second wave with its whole share of tiles
+  static int max_active[64][5] = {{0}};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
+  if (!max_active[dev][CM]) {
+    int n = 0;
+    cfg.gridDim = dim3((unsigned)(num_sms() / CM * CM), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, fp4_gemm_kernel<NV, false, CM>, &cfg) != cudaSuccess || n <= 0)
+      n = num_sms() / CM;
+    max_active[dev][CM] = std::min(n, num_sms() / CM);
+  }
+  const int clusters = std::max(1, std::min(ctiles, max_active[dev][CM]));
+  cfg.gridDim = dim3((unsigned)(clusters * CM), 1, 1);
+  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, CM>, ta, tb, p));
+  return Q4_OK;
+}
+
+// CTAs stacked along M can share (multicast) each B tile.  Measured on GB300
+// at 8192 x 28672 x 8192 and 4096 x 8192 x 8192, clusters of 2 and 4 run no
+// faster than single CTAs (the limit is the operand feed of the one-SM MMA,
+// not L2 bandwidth), so single CTAs are used.
+int cluster_m(int64_t M) {
+  (void)M;
+  return 1;
+}
+
 }  // namespace
 
 q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0) return Q4_OK;
+  const int cm = cluster_m(a.M);
   CUtensorMap ta, tb;
   q4_status st;
   if ((st = make_tmap_2d_u8(&ta, a.a_codes, a.K / 2, a.M, a.K / 2, BK / 2, BM, true)) != Q4_OK) return st;
-  if ((st = make_tmap_2d_u8(&tb, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN, true)) != Q4_OK) return st;
+  if ((st = make_tmap_2d_u8(&tb, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN / cm, true)) != Q4_OK) return st;
   Params p = {};
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.a_sf = a.a_scales; p.b_sf = a.b_scales; p.b_sf_expert_bytes = 0;
@@ -451,16 +522,14 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   p.num_m = (int)ceil_div(a.M, BM); p.num_n = (int)ceil_div(a.N, BN);
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
-  const int tiles = p.num_m * p.num_n;
-  const unsigned grid = (unsigned)std::min(tiles, num_sms());
   if (a.nvfp4) {
-    if ((st = set_smem_attr<true, false>()) != Q4_OK) return st;
-    fp4_gemm_kernel<true, false><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(ta, tb, p);
-  } else {
-    if ((st = set_smem_attr<false, false>()) != Q4_OK) return st;
-    fp4_gemm_kernel<false, false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(ta, tb, p);
+    if (cm == 4) return launch_dense<true, 4>(ta, tb, p, stream);
+    if (cm == 2) return launch_dense<true, 2>(ta, tb, p, stream);
+    return launch_dense<true, 1>(ta, tb, p, stream);
   }
-  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  if (cm == 4) return launch_dense<false, 4>(ta, tb, p, stream);
+  if (cm == 2) return launch_dense<false, 2>(ta, tb, p, stream);
+  return launch_dense<false, 1>(ta, tb, p, stream);
 }
 
 q4_status launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int E,
@@ -495,8 +564,8 @@ q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
   p.a_codes = a.a_codes;
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
-  if ((st = set_smem_attr<true, true>()) != Q4_OK) return st;
-  fp4_gemm_kernel<true, true><<<(unsigned)num_sms(), kThreads + kGatherThreads, Cfg<true>::kSmemBytes,
+  if ((st = set_smem_attr<true, true, 1>()) != Q4_OK) return st;
+  fp4_gemm_kernel<true, true, 1><<<(unsigned)num_sms(), kThreads + kGatherThreads, Cfg<true>::kSmemBytes,
                                 stream>>>(tb, tb, p);
   return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
