@@ -45,7 +45,11 @@ FP4_OVER_BF16 = 6.0
 
 # ncu-measured DRAM traffic per launch of the dominant kernel (bytes), keyed by
 # workload; None until a capture of the current kernel exists.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # prof_w4a16_decode (profiles/w4a16_decode.md): mean dram__bytes_read + write of the
+    # M = 1, 4, 16 launches of the current w4a16_kernel at N = K = 8192
+    "decode": 34.8e6,
+}
 
 
 def peaks():
