@@ -143,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
 #pragma unroll
   for (int gi = 0; gi < kRing; ++gi) issue(gi);
+  // Weights and scales are never written by an earlier kernel, so their loads
+  // go out before waiting on the previous grid in the stream (programmatic
+  // dependent launch); activations and the output wait for it.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   float acc[2][TS][4];  // [tile][token set][fragment]
 #pragma unroll
@@ -173,52 +177,38 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
 
-    // ---- stage the present tokens' activations, permuted per fragment
+    // ---- stage the present tokens' activations, permuted per fragment: thread
+    // (group gi, token tok) copies that token's 128 values of the group and sums
+    // them in a fixed order (deterministic) for the offset correction
+    if (gi0 == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
-    const int per_tok = gc * 16;  // 16-byte chunks per token
-    const int slots = mt * per_tok;
-    for (int base = 0; base < slots; base += 4 * kThreads) {
-      uint4 x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int sl = base + u * kThreads + tid;
-        if (sl < slots) {
-          const int tok = sl / per_tok, q = sl % per_tok;
-          x[u] = *reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K + (int64_t)c0 * 128 + q * 8);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int sl = base + u * kThreads + tid;
-        if (sl < slots) {
-          const int tok = sl / per_tok, q = sl % per_tok;
-          const int gi = q >> 4, cq = (q >> 2) & 3, w = q & 3;
-          uint4 v;
-          // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}
-          v.x = __byte_perm(x[u].x, x[u].z, 0x5410);
-          v.y = __byte_perm(x[u].x, x[u].z, 0x7632);
-          v.z = __byte_perm(x[u].y, x[u].w, 0x5410);
-          v.w = __byte_perm(x[u].y, x[u].w, 0x7632);
-          act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
-        }
-      }
-    }
-    __syncthreads();
-    // 136 * sum_k a[tok, k] per group, summed in a fixed order (deterministic)
     if (tid < gc * kTp) {
       const int gi = tid / kTp, tok = tid % kTp;
       float sum = 0.f;
       if (tok < mt) {
-#pragma unroll 4
-        for (int w = 0; w < 4; ++w)
+        const uint4* src =
+            reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K + (int64_t)(c0 + gi) * 128);
 #pragma unroll
-          for (int cq = 0; cq < 4; ++cq) {
-            const uint4 v = act[((gi * 4 + w) * kTp + tok) * 4 + cq];
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        for (int b = 0; b < 2; ++b) {
+          uint4 x[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              sum += __uint_as_float(u[e] << 16) + __uint_as_float(u[e] & 0xFFFF0000u);
+          for (int u = 0; u < 8; ++u) x[u] = src[8 * b + u];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int q = 8 * b + u, cq = q >> 2, w = q & 3;
+            uint4 v;
+            // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}
+            v.x = __byte_perm(x[u].x, x[u].z, 0x5410);
+            v.y = __byte_perm(x[u].x, x[u].z, 0x7632);
+            v.z = __byte_perm(x[u].y, x[u].w, 0x5410);
+            v.w = __byte_perm(x[u].y, x[u].w, 0x7632);
+            act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
+            const uint32_t e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              sum += __uint_as_float(e[i] << 16) + __uint_as_float(e[i] & 0xFFFF0000u);
           }
+        }
       }
       csum[gi * kTok + tok] = 136.0f * sum;
     }
@@ -318,10 +308,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int e = tid; e < (r_hi - r_lo) * tq; e += kThreads) {
     const int t4 = e / (r_hi - r_lo), r = r_lo + e % (r_hi - r_lo);
     const uint32_t off = (uint32_t)(r * kTok + 4 * t4) * 4u;
+    // all remote loads are issued before any is used; summed in rank order
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = q < cs ? ld_dsmem_f32x4(mapa_u32(red_base, (uint32_t)q) + off) : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < cs; ++q) {
-      const float4 v = ld_dsmem_f32x4(mapa_u32(red_base, (uint32_t)q) + off);
-      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      sum.x += v[q].x; sum.y += v[q].y; sum.z += v[q].z; sum.w += v[q].w;
     }
     const int n = n_base + r;
     if (n < N) {
@@ -362,13 +357,17 @@ q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: may start while the previous kernel in the
+  // stream finishes; the kernel waits for it before touching activations or C
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // one token set of 8 when every token block has at most 8 tokens
   if (M <= 8)
     Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel<1>, (const __nv_bfloat16*)A, Wq, Ws,
