@@ -36,6 +36,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = BN;             // 256 FP32 columns
 constexpr uint32_t kSfColsPerStage = 48;      // 16 (A) + 32 (B)
 constexpr int kMaxExperts = 1024;
+constexpr int kPartStride = BN + 4;  // FP32 partial tile row stride (split-K), padded against bank conflicts
+
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
 
 template <bool NV>
 struct Cfg {
@@ -126,7 +138,10 @@ __device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sch
 }
 
 
-template <bool NV, bool GROUPED, int CM>
+// KS > 1: split-K -- a cluster of KS CTAs owns one output tile, each CTA a
+// slice of the K blocks; the FP32 partial tiles are reduced through
+// distributed shared memory in rank order (deterministic).
+template <bool NV, bool GROUPED, int CM, int KS = 1>
 __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -139,10 +154,15 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
   __shared__ int s_sched[GROUPED ? kMaxExperts + 1 : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = (int)(p.K / BK);
   static_assert(!GROUPED || CM == 1, "");
+  static_assert(KS == 1 || (CM == 1 && !GROUPED), "");
+  constexpr int CL = CM * KS;                                // CTAs per cluster
   const int crank = CM > 1 ? (int)cluster_ctarank() : 0;  // rank along M in the cluster
-  const int cid = blockIdx.x / CM, ncl = gridDim.x / CM;   // cluster index and count
+  const int krank = KS > 1 ? (int)cluster_ctarank() : 0;  // rank along K (split-K)
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;   // cluster index and count
+  const int nkb_all = (int)(p.K / BK);
+  const int kbs = (nkb_all + KS - 1) / KS;
+  const int kb_begin = min(nkb_all, krank * kbs), kb_end = min(nkb_all, kb_begin + kbs);
   constexpr uint16_t kMask = (uint16_t)((1u << CM) - 1u);
 
   int total_tiles;
@@ -173,7 +193,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CM > 1) cluster_barrier_sync();  // peers' barriers exist before any multicast
+  if constexpr (CL > 1) cluster_barrier_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort_flag = &sm->abort;
@@ -203,7 +223,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
       const uint32_t bytes = (GROUPED ? 0u : kABytes) + kBBytes + (a_sf_ok ? C_::kSfaBytes : 0u) +
                              C_::kSfaBytes * (b_hi ? 2 : 1);
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
         if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
@@ -258,7 +278,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
             alive = false;
             break;
@@ -283,7 +303,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
             const uint32_t sf_id = NV ? 0u : (k & 1) * 2;
             const uint32_t idesc = fp4_idesc(BM, BN, !NV, sf_id, sf_id);
             tc_mma_fp4<NV ? 4 : 2>(tmem, ad, bd, idesc, sf_t + 4 * j, sf_t + 16 + 8 * j,
-                                   (kb | k) != 0 ? 1u : 0u);
+                                   (kb != kb_begin || k != 0) ? 1u : 0u);
           }
           if constexpr (CM == 1) tc_commit(smem_u32(&sm->empty[stage]));
           else tc_commit_mc(smem_u32(&sm->empty[stage]), kMask);
@@ -312,7 +332,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
       const int r = ti.m_row0 + i;
       const int tokr = __ldg(p.row_token + (r < ti.m_end ? r : ti.m_row0));
       const uint8_t* src = p.a_codes + (int64_t)tokr * (p.K / 2);
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
         if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
@@ -339,6 +359,27 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
       if (!ti.ok) continue;
       if (!mbar_wait(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
       tc_fence_after();
+      if constexpr (KS > 1) {
+        // split-K: this CTA's FP32 partial tile -> shared memory (the ring is idle:
+        // every copy of this CTA's K slice was consumed before acc_full)
+        float* part = reinterpret_cast<float*>(smem) + (q * 32 + lane) * kPartStride;
+        const bool has_k = kb_end > kb_begin;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<float4*>(part + c * 32)[v] =
+                has_k ? make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        tc_fence_before();
+        ++tcount;
+        continue;
+      }
       float alpha = 1.f;
       if constexpr (NV) alpha = __ldg(p.a_g) * __ldg(p.b_g + ti.e);
       const int row = ti.m_row0 + q * 32 + lane;
@@ -400,8 +441,49 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // no CTA leaves while a peer may still multicast into it or arrive on its barriers
-  if constexpr (CM > 1) cluster_barrier_sync();
+  if constexpr (KS > 1) {
+    // rank q reduces rows [q * 128 / KS, (q + 1) * 128 / KS) of the tile over all
+    // ranks' partials, in rank order, then applies gA * gB and stores
+    cluster_barrier_sync();
+    const int t = cid;  // one tile per cluster
+    if (t < total_tiles && !*abort_flag) {
+      const TileInfo ti = tile_at(t);
+      float alpha = 1.f;
+      if constexpr (NV) alpha = __ldg(p.a_g) * __ldg(p.b_g);
+      const int rows = (BM + KS - 1) / KS;
+      const int r_lo = krank * rows, r_hi = min(BM, r_lo + rows);
+      const uint32_t base = smem_u32(smem);
+      for (int e = threadIdx.x; e < (r_hi - r_lo) * (BN / 4); e += blockDim.x) {
+        const int r = r_lo + e / (BN / 4), c4 = e % (BN / 4);
+        const uint32_t off = (uint32_t)(r * kPartStride + 4 * c4) * 4u;
+        float4 v[KS];
+#pragma unroll
+        for (int qq = 0; qq < KS; ++qq) v[qq] = ld_dsmem_v4(base + off, (uint32_t)qq);
+        float4 sum = v[0];
+#pragma unroll
+        for (int qq = 1; qq < KS; ++qq) {
+          sum.x += v[qq].x; sum.y += v[qq].y; sum.z += v[qq].z; sum.w += v[qq].w;
+        }
+        const int row = ti.m_row0 + r, col = ti.n0 + 4 * c4;
+        if (row >= ti.m_end || col >= p.N) continue;
+        const float o[4] = {sum.x * alpha, sum.y * alpha, sum.z * alpha, sum.w * alpha};
+        if (p.c_dtype == Q4_BF16) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.N + col;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (col + i < p.N) out[i] = __float2bfloat16_rn(o[i]);
+        } else {
+          float* out = reinterpret_cast<float*>(p.C) + (int64_t)row * p.N + col;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (col + i < p.N) out[i] = o[i];
+        }
+      }
+    }
+  }
+  // no CTA leaves while a peer may still multicast into it, arrive on its
+  // barriers or read its shared memory
+  if constexpr (CL > 1) cluster_barrier_sync();
 }
 
 // ------------------------------------------------------------------ grouped prep
@@ -447,13 +529,13 @@ __global__ void __launch_bounds__(128)
 
 namespace {
 
-template <bool NV, bool GROUPED, int CM>
+template <bool NV, bool GROUPED, int CM, int KS = 1>
 q4_status set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!done[dev]) {
-    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, CM>,
+    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, CM, KS>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)Cfg<NV>::kSmemBytes));
     done[dev] = 1;
@@ -500,6 +582,45 @@ q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Param
 // at 8192 x 28672 x 8192 and 4096 x 8192 x 8192, clusters of 2 and 4 run no
 // faster than single CTAs (the limit is the operand feed of the one-SM MMA,
 // not L2 bandwidth), so single CTAs are used.
+// Split-K for problems with few output tiles: KS CTAs (one cluster) per tile,
+// launched as exactly tiles x KS CTAs (one tile per cluster).
+template <bool NV, int KS>
+q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                        cudaStream_t stream) {
+  static_assert(KS * 0 + (BM * (BN + 4) * 4) <= kStages * Cfg<NV>::kStageBytes, "partial tile fits");
+  q4_status st;
+  if ((st = set_smem_attr<NV, false, 1, KS>()) != Q4_OK) return st;
+  const int tiles = p.num_m * p.num_n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * KS), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<NV>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = KS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, 1, KS>, ta, tb, p));
+  return Q4_OK;
+}
+
+template <bool NV>
+q4_status dispatch_splitk(int ks, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                          cudaStream_t stream) {
+  switch (ks) {
+    case 2: return launch_splitk<NV, 2>(ta, tb, p, stream);
+    case 3: return launch_splitk<NV, 3>(ta, tb, p, stream);
+    case 4: return launch_splitk<NV, 4>(ta, tb, p, stream);
+    case 5: return launch_splitk<NV, 5>(ta, tb, p, stream);
+    case 6: return launch_splitk<NV, 6>(ta, tb, p, stream);
+    case 7: return launch_splitk<NV, 7>(ta, tb, p, stream);
+    default: return launch_splitk<NV, 8>(ta, tb, p, stream);
+  }
+}
+
 int cluster_m(int64_t M) {
   (void)M;
   return 1;
@@ -522,6 +643,20 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   p.num_m = (int)ceil_div(a.M, BM); p.num_n = (int)ceil_div(a.N, BN);
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
+  // few output tiles: split K over a cluster so that the grid fills the GPU.
+  // At most 4 CTAs per cluster: measured on GB300 (256 x 2048 x 7168,
+  // 128 x 4096 x 8192) 4 is fastest and 8 is slower than no split, since
+  // clusters of 8 one-CTA-per-SM blocks are not all resident at once.
+  const int tiles = p.num_m * p.num_n, nkb = (int)(a.K / BK);
+  if (tiles * 2 <= num_sms() && nkb >= 2) {
+    const int ks = std::min(4, std::min(num_sms() / tiles, nkb));
+    if (ks >= 2) {
+      CUtensorMap tb1;
+      if ((st = make_tmap_2d_u8(&tb1, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN, true)) != Q4_OK) return st;
+      return a.nvfp4 ? dispatch_splitk<true>(ks, ta, tb1, p, stream)
+                     : dispatch_splitk<false>(ks, ta, tb1, p, stream);
+    }
+  }
   if (a.nvfp4) {
     if (cm == 4) return launch_dense<true, 4>(ta, tb, p, stream);
     if (cm == 2) return launch_dense<true, 2>(ta, tb, p, stream);
