@@ -1,13 +1,14 @@
 // Block-scaled 4-bit quantizers: NVFP4 (tensor amax + per-16 E4M3 scales),
 // MXFP4 (per-32 E8M0 scales) and INT4 g128 (per-128 FP16 scales).
 //
-// Every element is loaded once with 128-bit loads; the threads that share a
-// scale block reduce its amax with warp shuffles; codes leave as packed 32-bit
-// words (8 codes per thread).  The arithmetic follows "Quantization in
+// Every element is loaded once with 128-bit loads, sixteen per thread; the
+// threads that share a scale block reduce its amax with warp shuffles; codes
+// leave as packed 64-bit words (16 codes per thread).  The arithmetic follows "Quantization in
 // deployment", section "Fake quantization" (fp4, mxfp4, nvfp4) and "Low-bit
 // inference for very large MoE", section "Why quantization-aware training"
 // (fake_int4): float32, IEEE-rounded divisions, E2M1 ties to the smaller
-// magnitude.
+// magnitude.  The FP4 kernels reach the same codes without a per-element
+// division (the argument is at each kernel).
 #include "common.cuh"
 #include "internal.h"
 
@@ -50,14 +51,39 @@ __device__ __forceinline__ void load8<__half>(const __half* __restrict__ x, int6
   load8_16bit(x, e, v);
 }
 
+// Sixteen consecutive elements starting at element index e (e % 16 == 0).
+template <typename T>
+__device__ __forceinline__ void load16(const T* __restrict__ x, int64_t e, float (&v)[16]) {
+  float a[8], b[8];
+  load8<T>(x, e, a);
+  load8<T>(x, e + 8, b);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { v[j] = a[j]; v[j + 8] = b[j]; }
+}
+
 // ------------------------------------------------------------------ amax
+// Grid-stride over 8-element units, four independent 16-byte loads in flight
+// per thread and iteration.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t n8,
                                                         unsigned* amax_bits, int* status) {
   float m = 0.f;
   bool bad = false;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n8; u += stride) {
+  int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; u + 3 * stride < n8; u += 4 * stride) {
+    float v[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) load8<T>(x, (u + i * stride) * 8, v[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        bad |= nonfinite(v[i][j]);
+        m = fmaxf(m, fabsf(v[i][j]));
+      }
+  }
+  for (; u < n8; u += stride) {
     float v[8];
     load8<T>(x, u * 8, v);
 #pragma unroll
@@ -81,25 +107,55 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
   }
 }
 
+// E2M1 magnitude code of |x| from its seven decision bounds: the number of
+// bounds it reaches.
+__device__ __forceinline__ uint32_t code_from_bounds(float a, const float (&B)[7], bool strict) {
+  uint32_t c = 0;
+#pragma unroll
+  for (int k = 0; k < 7; ++k) c += strict ? (a > B[k]) : (a >= B[k]);
+  return c;
+}
+
+// Magnitude-and-sign E2M1 codes of two floats, RNE, saturating at 6: the
+// code of lo in bits 0..3, of hi in bits 4..7.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ------------------------------------------------------------------ NVFP4
-// One thread per 8 elements; a thread pair shares one 16-element block.
+// One thread per 16-element block.
+//
+// The pages' rule is y = x / S in float32 (rounded to nearest), clamped to
+// [-6, 6], then rounded to the nearest E2M1 value with ties to the smaller
+// magnitude.  Here:
+//  * y0 = |x| * RN(1/S) is within 1.5 ulp of |x| / S.  The E2M1 decision
+//    points t_k in {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5} have three
+//    significant bits, so when y0 is more than 8 ulp away from every float
+//    with three significant bits, RN(|x| / S) and y0 lie strictly inside the
+//    same E2M1 rounding cell, and no tie can occur: the hardware RNE convert of
+//    y0 gives the pages' code.
+//  * Otherwise (rare for real data) y = RN(|x| / S) is computed by an IEEE
+//    division.  If y itself has three significant bits it may be a tie; its
+//    predecessor lies in the cell that ties-to-smaller selects, and any other
+//    three-bit y lies inside its cell, so the predecessor converts correctly.
+// The sign goes in bit 3 when x < 0, also for codes of magnitude 0.
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 5)
     nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4,
                  const unsigned* __restrict__ amax_bits, float* tensor_scale) {
-  const int64_t units = rows * (K / 8);
+  const int64_t units = rows * (K / 16);
   const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const bool live = u < units;
-  float v[8];
+  if (u >= units) return;
+  float v[16];
+  load16<T>(x, u * 16, v);
   float amax = 0.f;
-  if (live) {
-    load8<T>(x, u * 8, v);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-  }
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  if (!live) return;
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
 
   // per-tensor scale g = max(amax_t, 1e-12) / (448 * 6)
   const float g = __fdiv_rn(fmaxf(__uint_as_float(*amax_bits), 1e-12f), 2688.0f);
@@ -109,65 +165,87 @@ __global__ void __launch_bounds__(kThreads)
   const float bsf = __half2float(__half(__nv_cvt_fp8_to_halfraw(bs, __NV_E4M3)));
   const float S = __fmul_rn(fmaxf(bsf, 1e-12f), g);
 
-  uint32_t packed = 0;
+  uint2 packed = make_uint2(0u, 0u);
   if (bs != 0) {
+    const float R = __frcp_rn(S);
+    float y[16];
+    bool near = false;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float y = __fdiv_rn(v[j], S);
-      y = fminf(fmaxf(y, -6.0f), 6.0f);
-      const uint32_t c = e2m1_index(fabsf(y)) | (v[j] < 0.f ? 8u : 0u);
-      packed |= c << (4 * j);
+    for (int j = 0; j < 16; ++j) {
+      y[j] = __fmul_rn(fabsf(v[j]), R);
+      const uint32_t b = __float_as_uint(y[j]);
+      // |y| in [0.125, 5.5) and within 8 ulp of a float with 3 significant bits
+      near |= (((b + 8u) & 0x1FFFFFu) <= 16u) & (b - 0x3E000000u < 0x02B00000u);
+    }
+    if (near) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t b0 = __float_as_uint(y[j]);
+        if ((((b0 + 8u) & 0x1FFFFFu) <= 16u) & (b0 - 0x3E000000u < 0x02B00000u)) {
+          uint32_t b = __float_as_uint(__fdiv_rn(fabsf(v[j]), S));
+          if ((b & 0x1FFFFFu) == 0u) b -= 1u;  // |y| >= 0.12 here, so b > 0
+          y[j] = __uint_as_float(b);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) y[j] = v[j] < 0.f ? -y[j] : y[j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      packed.x |= cvt_e2m1x2(y[2 * j], y[2 * j + 1]) << (8 * j);
+      packed.y |= cvt_e2m1x2(y[8 + 2 * j], y[8 + 2 * j + 1]) << (8 * j);
     }
   }
-  reinterpret_cast<uint32_t*>(codes)[u] = packed;
+  reinterpret_cast<uint2*>(codes)[u] = packed;
 
-  if ((u & 1) == 0) {
-    const int64_t row = u / (K / 8);
-    const int64_t blk = (u % (K / 8)) >> 1;
-    const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
-                                                : row * (K / 16) + blk;
-    scales[off] = (uint8_t)bs;
-  }
+  const int64_t row = u / (K / 16);
+  const int64_t blk = u % (K / 16);
+  const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
+                                              : row * (K / 16) + blk;
+  scales[off] = (uint8_t)bs;
   if (u == 0 && tensor_scale) *tensor_scale = g;
 }
 
 // ------------------------------------------------------------------ MXFP4
-// One thread per 8 elements; four threads share one 32-element block.
+// One thread per 16 elements; a thread pair shares one 32-element block.
+//
+// y = x / 2^e is exact whenever it is a normal float, and a subnormal y lies
+// far below the smallest midpoint, so RN(|x| / 2^e) > t_k <=> |x| > t_k * 2^e,
+// and t_k * 2^e is itself an exact float (e is in [-42, 125]).
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4) {
-  const int64_t units = rows * (K / 8);
+  const int64_t units = rows * (K / 16);
   const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < units;
-  float v[8];
+  float v[16];
   float amax = 0.f;
   if (live) {
-    load8<T>(x, u * 8, v);
+    load16<T>(x, u * 16, v);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
   }
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   if (!live) return;
 
   amax = fmaxf(amax, 1e-12f);  // normal, so floor(log2) is its exponent field
   const int e = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 2;
-  // x / 2^e and x * 2^-e round the same real number, so they are equal
-  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
-  uint32_t packed = 0;
+  const float p2 = __uint_as_float((uint32_t)(127 + e) << 23);  // 2^e
+  const float B[7] = {0.25f * p2, 0.75f * p2, 1.25f * p2, 1.75f * p2,
+                      2.5f * p2,  3.5f * p2,  5.0f * p2};
+  uint2 packed = make_uint2(0u, 0u);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float y = __fmul_rn(v[j], inv);
-    y = fminf(fmaxf(y, -6.0f), 6.0f);
-    const uint32_t c = e2m1_index(fabsf(y)) | (v[j] < 0.f ? 8u : 0u);
-    packed |= c << (4 * j);
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t c = code_from_bounds(fabsf(v[j]), B, true) | (v[j] < 0.f ? 8u : 0u);
+    if (j < 8) packed.x |= c << (4 * j);
+    else packed.y |= c << (4 * (j - 8));
   }
-  reinterpret_cast<uint32_t*>(codes)[u] = packed;
+  reinterpret_cast<uint2*>(codes)[u] = packed;
 
-  if ((u & 3) == 0) {
-    const int64_t row = u / (K / 8);
-    const int64_t blk = (u % (K / 8)) >> 2;
+  if ((u & 1) == 0) {
+    const int64_t row = u / (K / 16);
+    const int64_t blk = (u % (K / 16)) >> 1;
     const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
                                                 : row * (K / 32) + blk;
     scales[off] = (uint8_t)(e + 127);
@@ -175,40 +253,42 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ------------------------------------------------------------------ INT4 g128
-// One thread per 8 elements; sixteen threads share one 128-element group.
+// One thread per 16 elements; eight threads share one 128-element group.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     int4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
                 uint16_t* __restrict__ scales) {
-  const int64_t units = rows * (K / 8);
+  const int64_t units = rows * (K / 16);
   const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < units;
-  float v[8];
+  float v[16];
   float amax = 0.f;
   if (live) {
-    load8<T>(x, u * 8, v);
+    load16<T>(x, u * 16, v);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
   }
 #pragma unroll
-  for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if (!live) return;
 
   const __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
   const float sf = __half2float(s16);
-  uint32_t packed = 0;
+  uint2 packed = make_uint2(0u, 0u);
   if (sf != 0.f) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 16; ++j) {
       float q = rintf(__fdiv_rn(v[j], sf));
       q = fminf(fmaxf(q, -8.0f), 7.0f);
-      packed |= ((uint32_t)(int)q & 0xFu) << (4 * j);
+      const uint32_t c = (uint32_t)(int)q & 0xFu;
+      if (j < 8) packed.x |= c << (4 * j);
+      else packed.y |= c << (4 * (j - 8));
     }
   }
-  reinterpret_cast<uint32_t*>(codes)[u] = packed;
-  if ((u & 15) == 0) {
-    const int64_t row = u / (K / 8);
-    const int64_t grp = (u % (K / 8)) >> 4;
+  reinterpret_cast<uint2*>(codes)[u] = packed;
+  if ((u & 7) == 0) {
+    const int64_t row = u / (K / 16);
+    const int64_t grp = (u % (K / 16)) >> 3;
     scales[row * (K / 128) + grp] = __half_as_ushort(s16);
   }
 }
@@ -233,7 +313,7 @@ q4_status launch_amax(const void* x, int dtype, int64_t n, unsigned* amax_bits,
                       cudaStream_t stream) {
   const int64_t n8 = n / 8;
   if (n8 == 0) return Q4_OK;
-  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n8, kThreads), (int64_t)num_sms() * 8);
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n8, kThreads), (int64_t)num_sms() * 4);
   int* st = device_status_ptr();
   switch (dtype) {
     case Q4_F32: amax_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, n8, amax_bits, st); break;
@@ -247,9 +327,10 @@ q4_status launch_amax(const void* x, int dtype, int64_t n, unsigned* amax_bits,
 q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                              uint8_t* scales, int layout, const unsigned* amax_bits,
                              float* tensor_scale, cudaStream_t stream) {
-  const int64_t units = rows * (K / 8);
+  const int64_t units = rows * (K / 16);
   const int64_t nsf4 = ceil_div(K / 16, 4);
-  if (layout == Q4_SCALES_MMA)
+  // every byte of an unpadded MMA layout is written by the kernel
+  if (layout == Q4_SCALES_MMA && (rows % 128 || (K / 16) % 4))
     Q4_CUDA_TRY(cudaMemsetAsync(scales, 0, mma_scales_bytes(rows, K / 16), stream));
   if (units == 0) {
     // an empty tensor still reports g = 1e-12 / 2688
@@ -267,9 +348,9 @@ q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, 
 
 q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                              uint8_t* scales, int layout, cudaStream_t stream) {
-  const int64_t units = rows * (K / 8);
+  const int64_t units = rows * (K / 16);
   const int64_t nsf4 = ceil_div(K / 32, 4);
-  if (layout == Q4_SCALES_MMA)
+  if (layout == Q4_SCALES_MMA && (rows % 128 || (K / 32) % 4))
     Q4_CUDA_TRY(cudaMemsetAsync(scales, 0, mma_scales_bytes(rows, K / 32), stream));
   if (units == 0) return Q4_OK;
   const unsigned grid = blocks_for(units);
@@ -284,7 +365,7 @@ q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, 
 
 q4_status launch_quant_int4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                             uint16_t* scales, cudaStream_t stream) {
-  const int64_t units = rows * (K / 8);
+  const int64_t units = rows * (K / 16);
   if (units == 0) return Q4_OK;
   const unsigned grid = blocks_for(units);
   switch (dtype) {

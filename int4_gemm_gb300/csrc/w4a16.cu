@@ -15,9 +15,11 @@
 //    promotion), so the only rounding to bf16 is the final store.
 //  * The activations of a CTA's K-slice sit in shared memory, permuted so that
 //    every B fragment is one conflict-free 16-byte load.
-//  * K is split across a thread-block cluster of up to 8 CTAs; their partial
-//    sums are reduced through distributed shared memory in rank order, so the
-//    result is deterministic and nothing but C goes back to HBM.
+//  * K is split across a thread-block cluster of up to 8 CTAs.  Each CTA
+//    pushes the partial sums of the rows that rank q owns into rank q's
+//    receive buffer (distributed shared memory stores), one cluster barrier
+//    follows, and each owner adds its buffers in rank order: deterministic,
+//    and nothing but C goes back to HBM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -34,9 +36,10 @@ constexpr int kChunk = 8;       // groups of 128 staged per activation chunk
 constexpr int kRing = 4;        // weight groups in flight per thread (cp.async ring)
 constexpr int kActBytes = kChunk * 4 * kTok * 4 * 16;   // 32 KiB
 constexpr int kRingBytes = kRing * 4 * kThreads * 16;   // 64 KiB: [slot][chunk][thread] x 16 B
-constexpr int kRedBytes = kRows * kTok * 4;             // 16 KiB (aliases the ring at the end)
 constexpr int kSumBytes = kChunk * kTok * 4;            // 512 B: 136 * sum of a per group, token
-static_assert(kRedBytes <= kRingBytes, "");
+// receive buffer of the cluster reduction: [source rank][owned row][token] FP32,
+// at most 8 ranks x ceil(256 / ranks) rows
+__host__ __device__ constexpr int recv_bytes(int tokens) { return (kRows + 7) * tokens * 4; }
 
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
@@ -65,13 +68,8 @@ __device__ __forceinline__ uint32_t mapa_u32(uint32_t a, uint32_t rank) {
   return ra;
 }
 
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
+__device__ __forceinline__ void st_dsmem_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -106,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* ring = smem;                                              // [slot][chunk][thread] x 16 B
   uint4* act = reinterpret_cast<uint4*>(smem + kRingBytes);         // [kChunk][4][kTp][4] x 16 B
   float* csum = reinterpret_cast<float*>(smem + kRingBytes + kActBytes);  // [kChunk][kTok]
-  float* red = reinterpret_cast<float*>(smem);                       // [kRows][kTok], at the end
+  float* recv = reinterpret_cast<float*>(smem + kRingBytes + kActBytes + kSumBytes);  // [cs][per][kTp]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quad = lane & 3, lrow = lane >> 2;
@@ -177,40 +175,45 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
 
-    // ---- stage the present tokens' activations, permuted per fragment: thread
-    // (group gi, token tok) copies that token's 128 values of the group and sums
-    // them in a fixed order (deterministic) for the offset correction
+    // ---- stage the present tokens' activations, permuted per fragment.  kSplit
+    // threads share one (group, token): each loads its 16 / kSplit pieces of 16
+    // bytes at once, stores them permuted and sums its values in a fixed
+    // order; the partial sums meet in a fixed shuffle order (deterministic).
+    // Columns of absent tokens are left as they are: their results are never
+    // stored.
     if (gi0 == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-    __syncthreads();
-    if (tid < gc * kTp) {
-      const int gi = tid / kTp, tok = tid % kTp;
+    else __syncthreads();  // every warp is done with the previous chunk
+    {
+      constexpr int kSplit = kThreads / (kChunk * kTp);  // 4 (TS = 1) or 2 (TS = 2)
+      constexpr int kPer = 16 / kSplit;                   // pieces per thread
+      const int pair = tid / kSplit, part = tid % kSplit;
+      const int gi = pair / kTp, tok = pair % kTp;
       float sum = 0.f;
-      if (tok < mt) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K + (int64_t)(c0 + gi) * 128);
+      if (gi < gc && tok < mt) {
+        const uint4* src = reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K +
+                                                          (int64_t)(c0 + gi) * 128) + part * kPer;
+        uint4 x[kPer];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          uint4 x[8];
+        for (int u = 0; u < kPer; ++u) x[u] = src[u];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) x[u] = src[8 * b + u];
+        for (int u = 0; u < kPer; ++u) {
+          const int q = part * kPer + u, cq = q >> 2, w = q & 3;
+          uint4 v;
+          // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}
+          v.x = __byte_perm(x[u].x, x[u].z, 0x5410);
+          v.y = __byte_perm(x[u].x, x[u].z, 0x7632);
+          v.z = __byte_perm(x[u].y, x[u].w, 0x5410);
+          v.w = __byte_perm(x[u].y, x[u].w, 0x7632);
+          act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
+          const uint32_t e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int q = 8 * b + u, cq = q >> 2, w = q & 3;
-            uint4 v;
-            // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}
-            v.x = __byte_perm(x[u].x, x[u].z, 0x5410);
-            v.y = __byte_perm(x[u].x, x[u].z, 0x7632);
-            v.z = __byte_perm(x[u].y, x[u].w, 0x5410);
-            v.w = __byte_perm(x[u].y, x[u].w, 0x7632);
-            act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
-            const uint32_t e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              sum += __uint_as_float(e[i] << 16) + __uint_as_float(e[i] & 0xFFFF0000u);
-          }
+          for (int i = 0; i < 4; ++i)
+            sum += __uint_as_float(e[i] << 16) + __uint_as_float(e[i] & 0xFFFF0000u);
         }
       }
-      csum[gi * kTok + tok] = 136.0f * sum;
+#pragma unroll
+      for (int o = 1; o < kSplit; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (part == 0 && gi < gc && tok < mt) csum[gi * kTok + tok] = 136.0f * sum;
     }
     __syncthreads();
 
@@ -283,42 +286,38 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   }
-  cp_async_wait<0>();
-  __syncthreads();  // every thread is done with the ring before it becomes red
+  cp_async_wait<0>();  // no copy may still target this CTA's shared memory at exit
 
-  // ---- partial sums to shared memory: red[row][token]
+  // ---- push the partial sums of each owned row slice to its owner rank:
+  // recv[src rank][row - owner * per][token] in the owner's shared memory
+  const int per = (kRows + cs - 1) / cs;
+  const uint32_t recv_base = smem_u32(recv);
 #pragma unroll
   for (int t = 0; t < 2; ++t)
 #pragma unroll
-    for (int s = 0; s < TS; ++s) {
-      const int r = warp * 32 + t * 16 + lrow;
-      const int tk = s * 8 + quad * 2;
-      red[r * kTok + tk] = acc[t][s][0];
-      red[r * kTok + tk + 1] = acc[t][s][1];
-      red[(r + 8) * kTok + tk] = acc[t][s][2];
-      red[(r + 8) * kTok + tk + 1] = acc[t][s][3];
+    for (int h = 0; h < 2; ++h) {
+      const int r = warp * 32 + t * 16 + h * 8 + lrow;
+      const int owner = r / per;
+      const uint32_t dst = mapa_u32(recv_base, (uint32_t)owner) +
+                           (uint32_t)(((rank * per + r - owner * per) * kTp) * 4);
+#pragma unroll
+      for (int s = 0; s < TS; ++s)
+        st_dsmem_f32x2(dst + (uint32_t)((s * 8 + quad * 2) * 4), acc[t][s][2 * h],
+                       acc[t][s][2 * h + 1]);
     }
-  cluster_sync();
+  cluster_sync();  // every push has landed; nothing remote is touched afterwards
 
-  // ---- rank q reduces rows [q * per, (q + 1) * per) over all ranks, in rank order
-  const int per = (kRows + cs - 1) / cs;
+  // ---- rank q adds rows [q * per, (q + 1) * per) over the source ranks in order
   const int r_lo = rank * per, r_hi = min(kRows, r_lo + per);
   const int tq = (mt + 3) / 4;  // groups of four tokens
-  const uint32_t red_base = smem_u32(red);
   for (int e = tid; e < (r_hi - r_lo) * tq; e += kThreads) {
-    const int t4 = e / (r_hi - r_lo), r = r_lo + e % (r_hi - r_lo);
-    const uint32_t off = (uint32_t)(r * kTok + 4 * t4) * 4u;
-    // all remote loads are issued before any is used; summed in rank order
-    float4 v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      v[q] = q < cs ? ld_dsmem_f32x4(mapa_u32(red_base, (uint32_t)q) + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int t4 = e / (r_hi - r_lo), rl = e % (r_hi - r_lo);
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      sum.x += v[q].x; sum.y += v[q].y; sum.z += v[q].z; sum.w += v[q].w;
+    for (int q = 0; q < cs; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(&recv[((q * per + rl) * kTp) + 4 * t4]);
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
-    const int n = n_base + r;
+    const int n = n_base + r_lo + rl;
     if (n < N) {
       const float vv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
@@ -326,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (4 * t4 + i < mt) C[(int64_t)(m0 + 4 * t4 + i) * N + n] = __float2bfloat16_rn(vv[i]);
     }
   }
-  cluster_sync();
 }
 
 }  // namespace
@@ -341,21 +339,22 @@ q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int
   int cs = std::max(1, std::min(8, (int)ceil_div(ngroups, 8)));
   const int gpc = (int)(ceil_div(ceil_div(ngroups, cs), 8) * 8);
   cs = (int)ceil_div(ngroups, gpc);
-  const size_t smem = kRingBytes + kActBytes + kSumBytes;
+  const size_t smem1 = kRingBytes + kActBytes + kSumBytes + recv_bytes(8);
+  const size_t smem2 = kRingBytes + kActBytes + kSumBytes + recv_bytes(16);
   static int attr_done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!attr_done[dev]) {
     Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem));
+                                     (int)smem1));
     Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem));
+                                     (int)smem2));
     attr_done[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cs, (unsigned)ceil_div(N, kRows), (unsigned)ceil_div(M, kTok));
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = M <= 8 ? smem1 : smem2;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

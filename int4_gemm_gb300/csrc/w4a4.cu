@@ -11,11 +11,15 @@
 //              copies of the scale tiles into a 4-stage shared-memory ring.
 //   warps 6-9  (grouped variant only) gather the routed A rows: plain loads,
 //              swizzled shared stores, proxy fence, mbarrier arrive.
-//   warp 1     allocates TMEM; one lane copies each stage's scales into TMEM
-//              (tcgen05.cp) and issues tcgen05.mma ... block_scale, 128x256x64
-//              per instruction, FP32 accumulation in TMEM.
+//   warp 1     allocates TMEM; one lane issues tcgen05.mma ... block_scale,
+//              128x256x64 per instruction, FP32 accumulation in TMEM.
 //   warps 2-5  epilogue: tcgen05.ld of the 128x256 FP32 accumulator, times
 //              gA * gB (NVFP4), rounded to bf16 (or kept FP32), stored.
+//   4 warps    scale writers: each stage's scale tiles go from shared memory
+//              to TMEM through registers (tcgen05.st, one warp per TMEM lane
+//              quarter).  Unlike tcgen05.cp these stores do not queue behind
+//              the MMAs in the tensor pipe, so the MMA thread issues nothing
+//              but MMAs.
 // Every wait is bounded: on timeout the CTA latches Q4_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -29,7 +33,12 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of codes)
 constexpr int kStages = 4;
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
+constexpr int kWriterThreads = 128;    // 4 scale-writer warps
 constexpr int kGatherThreads = 128;    // grouped variant: 4 more warps gather A rows
+constexpr int kWriterWarp0 = (kThreads + kWriterThreads) / 32 - 4;  // warps 6-9
+constexpr int kGatherWarp0 = (kThreads + kWriterThreads) / 32;      // warps 10-13 (grouped)
+template <bool GROUPED>
+constexpr int block_threads() { return kThreads + kWriterThreads + (GROUPED ? kGatherThreads : 0); }
 constexpr uint32_t kABytes = BM * BK / 2;     // 16 KiB
 constexpr uint32_t kBBytes = BN * BK / 2;     // 32 KiB
 constexpr uint32_t kTmemCols = 512;
@@ -63,6 +72,7 @@ static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory");
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t sf_full[kStages];  // the stage's scales are in TMEM
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_done;
@@ -142,7 +152,7 @@ __device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sch
 // slice of the K blocks; the FP32 partial tiles are reduced through
 // distributed shared memory in rank order (deterministic).
 template <bool NV, bool GROUPED, int CM, int KS = 1>
-__global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
+__global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
   using C_ = Cfg<NV>;
@@ -178,6 +188,7 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm->full[s]), GROUPED ? 1 + kGatherThreads : 1);
       mbar_init(smem_u32(&sm->empty[s]), CM);  // every CTA of the cluster releases
+      mbar_init(smem_u32(&sm->sf_full[s]), 4);  // one arrival per scale-writer warp
     }
     mbar_init(smem_u32(&sm->acc_full), 1);
     mbar_init(smem_u32(&sm->acc_empty), 4);
@@ -283,18 +294,13 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
             alive = false;
             break;
           }
+          if (!mbar_wait(smem_u32(&sm->sf_full[stage]), phase, p.ctl, abort_flag)) {
+            alive = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * C_::kStageBytes);
-          const uint32_t sfa_s = st + kABytes + kBBytes;
-          const uint32_t sfb_s = sfa_s + C_::kSfaBytes;
           const uint32_t sf_t = tmem + kAccCols + stage * kSfColsPerStage;
-          // scales -> TMEM: chunk j of A at columns 4j, chunk (h, j) of B at 16 + 8j + 4h
-#pragma unroll
-          for (uint32_t j = 0; j < C_::kSfChunks; ++j) {
-            tc_cp_32x128b_x4(sf_t + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_x4(sf_t + 16 + 8 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
-            tc_cp_32x128b_x4(sf_t + 16 + 8 * j + 4, smem_desc(sfb_s + C_::kSfaBytes + 512 * j, 0, 128, 0));
-          }
 #pragma unroll
           for (uint32_t k = 0; k < BK / 64; ++k) {
             const uint64_t ad = smem_desc(st + 32 * k, 16, 1024, 2);
@@ -318,12 +324,52 @@ __global__ void __launch_bounds__(kThreads + (GROUPED ? kGatherThreads : 0), 1)
       mbar_wait(smem_u32(&sm->mma_done), 0, drain, nullptr);
     }
     __syncwarp();
-  } else if (GROUPED && warp >= kThreads / 32) {
+  } else if (warp >= kWriterWarp0 && warp < kWriterWarp0 + 4) {
+    // ------------------------------------------------------------ scale writers
+    // TMEM scale layout (the one tcgen05.cp .32x128b.warpx4 produces): chunk j
+    // of A (512 bytes: 32 rows of 16) at columns 4j..4j+3, chunk j of B rows
+    // h*128.. at columns 16 + 8j + 4h..; lane 32 q + l of every lane quarter q
+    // holds the chunk's row l.  This warp writes its quarter's lanes.
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t stage = 0, phase = 0;
+    bool alive = true;
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
+      const TileInfo ti = tile_at(t);
+      if (!ti.ok) continue;
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        // the MMAs that last read this stage's scale columns completed before
+        // the stage was refilled (empty -> producer -> full)
+        tc_fence_after();
+        const uint8_t* sfa_s = smem + stage * C_::kStageBytes + kABytes + kBBytes;
+        const uint8_t* sfb_s = sfa_s + C_::kSfaBytes;
+        const uint32_t sf_t = tmem + lane_base + kAccCols + stage * kSfColsPerStage;
+#pragma unroll
+        for (uint32_t j = 0; j < C_::kSfChunks; ++j) {
+          const uint4 va = *reinterpret_cast<const uint4*>(sfa_s + 512 * j + 16 * lane);
+          const uint4 vb0 = *reinterpret_cast<const uint4*>(sfb_s + 512 * j + 16 * lane);
+          const uint4 vb1 = *reinterpret_cast<const uint4*>(sfb_s + C_::kSfaBytes + 512 * j + 16 * lane);
+          tmem_st_32x32b_x4(sf_t + 4 * j, va);
+          tmem_st_32x32b_x4(sf_t + 16 + 8 * j, vb0);
+          tmem_st_32x32b_x4(sf_t + 16 + 8 * j + 4, vb1);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->sf_full[stage]));
+        if (++stage == kStages) stage = 0, phase ^= 1;
+      }
+    }
+  } else if (GROUPED && warp >= kGatherWarp0) {
     // ------------------------------------------------------------ A-row gather (grouped)
     // Thread i copies routed row i of the tile (its token's 128 code bytes of
     // this K block) into the 128-byte-swizzled A tile, then makes the writes
     // visible to the tensor core's async proxy before arriving.
-    const int i = threadIdx.x - kThreads;
+    const int i = threadIdx.x - kGatherWarp0 * 32;
     uint32_t stage = 0, phase = 0;
     bool alive = true;
     for (int t = cid; t < total_tiles && alive; t += ncl) {
@@ -550,7 +596,7 @@ q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Param
   if ((st = set_smem_attr<NV, false, CM>()) != Q4_OK) return st;
   const int ctiles = ((p.num_m + CM - 1) / CM) * p.num_n;  // cluster tiles
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(block_threads<false>(), 1, 1);
   cfg.dynamicSmemBytes = Cfg<NV>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -593,7 +639,7 @@ q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Para
   const int tiles = p.num_m * p.num_n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * KS), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(block_threads<false>(), 1, 1);
   cfg.dynamicSmemBytes = Cfg<NV>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -700,7 +746,7 @@ q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
   if ((st = set_smem_attr<true, true, 1>()) != Q4_OK) return st;
-  fp4_gemm_kernel<true, true, 1><<<(unsigned)num_sms(), kThreads + kGatherThreads, Cfg<true>::kSmemBytes,
+  fp4_gemm_kernel<true, true, 1><<<(unsigned)num_sms(), block_threads<true>(), Cfg<true>::kSmemBytes,
                                 stream>>>(tb, tb, p);
   return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }

@@ -148,3 +148,55 @@ def test_empty_rows(lib):
     c, s = lib.quantize_mxfp4(x)
     c, s = lib.quantize_int4_g128(torch.empty((0, 128), device="cuda"))
     assert lib.sync_status() == 0
+
+
+def _neighbours(c, n=2):
+    """float32 values c-n ulp .. c+n ulp around the float32 nearest to c."""
+    f = np.float32(c)
+    out = [f]
+    lo = hi = f
+    for _ in range(n):
+        lo = np.nextafter(lo, np.float32(0))
+        hi = np.nextafter(hi, np.float32(np.inf))
+        out += [lo, hi]
+    return out
+
+
+def test_nvfp4_decisions_next_to_midpoints(lib):
+    """Values within two ulps of m_k * S, the real numbers whose float32
+    quotients by S sit on the E2M1 midpoints, for block scales that are not
+    powers of two.  The tensor scale is 1 (tensor amax 2688), so S is the E4M3
+    block scale itself."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    s0s = [1.125, 1.375, 2.75, 0.8125, 13.0, 208.0, 0.0390625, 0.001953125 * 5]
+    rows = [[2688.0] + [0.0] * 15]
+    for s0 in s0s:
+        for t in mids:
+            ulp_half = 2.0 ** (np.floor(np.log2(t)) - 24)
+            c = (t + ulp_half) * s0            # exact in float64
+            near = _neighbours(c) + _neighbours(t * s0)
+            vals = [6.0 * s0] + [float(v) for v in near[:7]] + [-float(v) for v in near[:7]]
+            rows.append(vals + [0.0] * (16 - len(vals)))
+    x = np.array(rows, np.float32).reshape(1, -1)
+    xd, xh = _dev(x, torch.float32)
+    c, s, g = lib.quantize_nvfp4(xd)
+    oc, os_, og = oracle.quantize_nvfp4(xh)
+    assert g.item() == 1.0 == float(og)
+    assert np.array_equal(s.cpu().numpy(), os_)
+    assert np.array_equal(c.cpu().numpy(), oc)
+
+
+def test_mxfp4_decisions_next_to_midpoints(lib):
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    rows = []
+    for e in (-40, -7, 0, 3, 60, 120):
+        for t in mids:
+            near = _neighbours(t * 2.0 ** e, 3)
+            vals = [6.0 * 2.0 ** e] + [float(v) for v in near] + [-float(v) for v in near]
+            rows.append(vals + [0.0] * (32 - len(vals)))
+    x = np.array(rows, np.float32).reshape(1, -1)
+    xd, xh = _dev(x, torch.float32)
+    c, s = lib.quantize_mxfp4(xd)
+    oc, os_ = oracle.quantize_mxfp4(xh)
+    assert np.array_equal(s.cpu().numpy(), os_)
+    assert np.array_equal(c.cpu().numpy(), oc)
