@@ -19,6 +19,35 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// A launch covers rows [row0, row0 + units / nblk) of the tensor, one unit of
+// 16 elements per thread (nblk units per row, units < 2^32).  The row of unit
+// u comes from a multiply-high by a precomputed constant instead of a
+// division (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, unsigned case).
+struct UnitMap {
+  uint32_t units;  // units in this launch
+  uint32_t nblk;   // units per row (K / 16)
+  uint32_t magic;  // 2^32 (2^l - nblk) / nblk + 1, l = ceil(log2 nblk)
+  uint32_t shift;  // l - 1 (unused when nblk == 1)
+  int64_t row0;    // first row of this launch
+  __device__ __forceinline__ uint32_t row_of(uint32_t u) const {
+    if (nblk == 1) return u;
+    const uint32_t t = __umulhi(magic, u);
+    return (t + ((u - t) >> 1)) >> shift;
+  }
+};
+
+UnitMap make_unit_map(uint32_t units, uint32_t nblk, int64_t row0) {
+  UnitMap m{units, nblk, 0u, 0u, row0};
+  if (nblk > 1) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < nblk) ++l;
+    m.magic = (uint32_t)(((uint64_t(1) << 32) * ((uint64_t(1) << l) - nblk)) / nblk + 1);
+    m.shift = l - 1;
+  }
+  return m;
+}
+
 // Eight consecutive elements starting at element index e (e % 8 == 0) as
 // floats, with 128-bit loads.
 template <typename T>
@@ -142,68 +171,135 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 //    division.  If y itself has three significant bits it may be a tie; its
 //    predecessor lies in the cell that ties-to-smaller selects, and any other
 //    three-bit y lies inside its cell, so the predecessor converts correctly.
-// The sign goes in bit 3 when x < 0, also for codes of magnitude 0.
+// The sign goes in bit 3 when x < 0, also for codes of magnitude 0; the
+// hardware convert keeps the sign of a negative zero.
+// Persistent: each CTA walks tiles of 256 units (one per thread), a 4-slot
+// ring of bulk copies (one thread issues them) keeping three tiles in flight
+// while the threads work on the fourth.
+constexpr int kQStages = 4;
+constexpr int kQUnits = kThreads;
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 5)
-    nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(kThreads, 4)
+    nvfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4,
-                 const unsigned* __restrict__ amax_bits, float* tensor_scale) {
-  const int64_t units = rows * (K / 16);
-  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= units) return;
-  float v[16];
-  load16<T>(x, u * 16, v);
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+                 const unsigned* __restrict__ amax_bits, float* tensor_scale, KernelCtl ctl) {
+  // x and codes start at row um.row0; scales are indexed by the global row
+  constexpr uint32_t kTileBytes = kQUnits * 16 * sizeof(T);
+  extern __shared__ __align__(128) uint8_t qring[];  // [kQStages][kTileBytes]
+  __shared__ __align__(8) uint64_t full[kQStages];
+  __shared__ float s_g;
+  __shared__ int s_abort;
+  const uint32_t ntiles = (um.units + kQUnits - 1) / kQUnits;
+  const uint32_t tid = threadIdx.x;
+  auto tile_of = [&](uint32_t i) { return blockIdx.x + i * gridDim.x; };
+  auto issue = [&](uint32_t i) {  // the CTA's i-th tile into slot i % kQStages
+    const uint32_t tile = tile_of(i);
+    if (tile >= ntiles) return;
+    const uint32_t n = min((uint32_t)kQUnits, um.units - tile * kQUnits);
+    const uint32_t bar = smem_u32(&full[i % kQStages]);
+    mbar_arrive_expect_tx(bar, n * 16 * (uint32_t)sizeof(T));
+    bulk_load(smem_u32(qring + (i % kQStages) * kTileBytes), x + (int64_t)tile * kQUnits * 16,
+              n * 16 * (uint32_t)sizeof(T), bar);
+  };
+  if (tid == 0) {
+    for (int i = 0; i < kQStages; ++i) mbar_init(smem_u32(&full[i]), 1);
+    fence_mbar_init();
+    // per-tensor scale g = max(amax_t, 1e-12) / (448 * 6), once per CTA
+    s_g = __fdiv_rn(fmaxf(__uint_as_float(*amax_bits), 1e-12f), 2688.0f);
+    s_abort = 0;
+    for (uint32_t i = 0; i + 1 < kQStages; ++i) issue(i);
+  }
+  __syncthreads();
+  const float g = s_g;
 
-  // per-tensor scale g = max(amax_t, 1e-12) / (448 * 6)
-  const float g = __fdiv_rn(fmaxf(__uint_as_float(*amax_bits), 1e-12f), 2688.0f);
-  // block scale: E4M3 of (amax_b / 6) / g, round to nearest even
-  const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
-  const __nv_fp8_storage_t bs = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
-  const float bsf = __half2float(__half(__nv_cvt_fp8_to_halfraw(bs, __NV_E4M3)));
-  const float S = __fmul_rn(fmaxf(bsf, 1e-12f), g);
-
-  uint2 packed = make_uint2(0u, 0u);
-  if (bs != 0) {
-    const float R = __frcp_rn(S);
-    float y[16];
-    bool near = false;
+  uint32_t i = 0;
+  for (; tile_of(i) < ntiles; ++i) {
+    if (tid == 0 && !mbar_wait(smem_u32(&full[i % kQStages]), (i / kQStages) & 1, ctl, &s_abort))
+      s_abort = 1;
+    __syncthreads();  // the tile has landed; every thread is done with slot (i - 1) % kQStages
+    if (s_abort) break;
+    if (tid == 0) issue(i + kQStages - 1);
+    const uint32_t u = tile_of(i) * kQUnits + tid;
+    if (u >= um.units) continue;
+    float v[16];
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(qring + (i % kQStages) * kTileBytes +
+                                                        tid * 16 * sizeof(T));
+      if constexpr (sizeof(T) == 4) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      y[j] = __fmul_rn(fabsf(v[j]), R);
-      const uint32_t b = __float_as_uint(y[j]);
-      // |y| in [0.125, 5.5) and within 8 ulp of a float with 3 significant bits
-      near |= (((b + 8u) & 0x1FFFFFu) <= 16u) & (b - 0x3E000000u < 0x02B00000u);
-    }
-    if (near) {
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = src[q];
+          v[4 * q] = __uint_as_float(w.x); v[4 * q + 1] = __uint_as_float(w.y);
+          v[4 * q + 2] = __uint_as_float(w.z); v[4 * q + 3] = __uint_as_float(w.w);
+        }
+      } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t b0 = __float_as_uint(y[j]);
-        if ((((b0 + 8u) & 0x1FFFFFu) <= 16u) & (b0 - 0x3E000000u < 0x02B00000u)) {
-          uint32_t b = __float_as_uint(__fdiv_rn(fabsf(v[j]), S));
-          if ((b & 0x1FFFFFu) == 0u) b -= 1u;  // |y| >= 0.12 here, so b > 0
-          y[j] = __uint_as_float(b);
+        for (int q = 0; q < 2; ++q) {
+          const uint4 w = src[q];
+          const T* h = reinterpret_cast<const T*>(&w);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[8 * q + e] = Elem<T>::to_f(h[e]);
         }
       }
     }
+    float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) y[j] = v[j] < 0.f ? -y[j] : y[j];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      packed.x |= cvt_e2m1x2(y[2 * j], y[2 * j + 1]) << (8 * j);
-      packed.y |= cvt_e2m1x2(y[8 + 2 * j], y[8 + 2 * j + 1]) << (8 * j);
-    }
-  }
-  reinterpret_cast<uint2*>(codes)[u] = packed;
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
 
-  const int64_t row = u / (K / 16);
-  const int64_t blk = u % (K / 16);
-  const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
-                                              : row * (K / 16) + blk;
-  scales[off] = (uint8_t)bs;
-  if (u == 0 && tensor_scale) *tensor_scale = g;
+    // block scale: E4M3 of (amax_b / 6) / g, round to nearest even
+    const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+    const __nv_fp8_storage_t bs = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+    const float bsf = __half2float(__half(__nv_cvt_fp8_to_halfraw(bs, __NV_E4M3)));
+    const float S = __fmul_rn(fmaxf(bsf, 1e-12f), g);
+
+    uint2 packed = make_uint2(0u, 0u);
+    if (bs != 0) {
+      const float R = __frcp_rn(S);
+      // y = x * R + 0 rounds once like x * R, keeps the sign of a negative x
+      // (so its code carries the sign bit even when its magnitude rounds to 0)
+      // and turns x = -0 into +0, whose code is 0.
+      float y[16];
+      bool near = false;
+  #pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        y[j] = __fmaf_rn(v[j], R, 0.0f);
+        // |y| in [0.125, 5.5) and within 8 ulp of a float with 3 significant bits
+        const uint32_t d = (__float_as_uint(y[j]) & 0x7FFFFFFFu) - 0x3E000000u + 8u;
+        near |= ((d & 0x1FFFF0u) == 0u) & (d < 0x02B00008u);
+      }
+      if (near) {
+  #pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t d = (__float_as_uint(y[j]) & 0x7FFFFFFFu) - 0x3E000000u + 8u;
+          if (((d & 0x1FFFF0u) == 0u) & (d < 0x02B00008u)) {
+            uint32_t b = __float_as_uint(__fdiv_rn(fabsf(v[j]), S));
+            if ((b & 0x1FFFFFu) == 0u) b -= 1u;  // |y| >= 0.12 here, so b > 0
+            y[j] = __uint_as_float(b | (__float_as_uint(y[j]) & 0x80000000u));
+          }
+        }
+      }
+  #pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        packed.x |= cvt_e2m1x2(y[2 * j], y[2 * j + 1]) << (8 * j);
+        packed.y |= cvt_e2m1x2(y[8 + 2 * j], y[8 + 2 * j + 1]) << (8 * j);
+      }
+    }
+    reinterpret_cast<uint2*>(codes)[u] = packed;
+
+    const uint32_t rl = um.row_of(u);
+    const int64_t row = um.row0 + rl, blk = u - rl * um.nblk;
+    const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
+                                                : row * um.nblk + blk;
+    scales[off] = (uint8_t)bs;
+    if (u == 0 && um.row0 == 0 && tensor_scale) *tensor_scale = g;
+  }
+  // after an abort, copies already issued must land before the CTA exits
+  if (tid == 0 && s_abort) {
+    KernelCtl drain = ctl;
+    for (uint32_t k = i; k < i + kQStages - 1; ++k)
+      if (tile_of(k) < ntiles) mbar_wait(smem_u32(&full[k % kQStages]), (k / kQStages) & 1, drain, nullptr);
+  }
 }
 
 // ------------------------------------------------------------------ MXFP4
@@ -214,15 +310,14 @@ __global__ void __launch_bounds__(kThreads, 5)
 // and t_k * 2^e is itself an exact float (e is in [-42, 125]).
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-    mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
+    mxfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4) {
-  const int64_t units = rows * (K / 16);
-  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const bool live = u < units;
+  const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = u < um.units;
   float v[16];
   float amax = 0.f;
   if (live) {
-    load16<T>(x, u * 16, v);
+    load16<T>(x, (int64_t)u * 16, v);
 #pragma unroll
     for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
   }
@@ -244,10 +339,10 @@ __global__ void __launch_bounds__(kThreads)
   reinterpret_cast<uint2*>(codes)[u] = packed;
 
   if ((u & 1) == 0) {
-    const int64_t row = u / (K / 16);
-    const int64_t blk = (u % (K / 16)) >> 1;
+    const uint32_t rl = um.row_of(u);
+    const int64_t row = um.row0 + rl, blk = (u - rl * um.nblk) >> 1;
     const int64_t off = layout == Q4_SCALES_MMA ? mma_scale_offset(row, blk, nsf4)
-                                                : row * (K / 32) + blk;
+                                                : row * (um.nblk / 2) + blk;
     scales[off] = (uint8_t)(e + 127);
   }
 }
@@ -256,15 +351,14 @@ __global__ void __launch_bounds__(kThreads)
 // One thread per 16 elements; eight threads share one 128-element group.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-    int4_kernel(const T* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ codes,
+    int4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                 uint16_t* __restrict__ scales) {
-  const int64_t units = rows * (K / 16);
-  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const bool live = u < units;
+  const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = u < um.units;
   float v[16];
   float amax = 0.f;
   if (live) {
-    load16<T>(x, u * 16, v);
+    load16<T>(x, (int64_t)u * 16, v);
 #pragma unroll
     for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
   }
@@ -287,9 +381,9 @@ __global__ void __launch_bounds__(kThreads)
   }
   reinterpret_cast<uint2*>(codes)[u] = packed;
   if ((u & 7) == 0) {
-    const int64_t row = u / (K / 16);
-    const int64_t grp = (u % (K / 16)) >> 3;
-    scales[row * (K / 128) + grp] = __half_as_ushort(s16);
+    const uint32_t rl = um.row_of(u);
+    const int64_t grp = (u - rl * um.nblk) >> 3;
+    scales[(int64_t)rl * (um.nblk / 8) + grp] = __half_as_ushort(s16);  // scales start at row0
   }
 }
 
@@ -324,57 +418,93 @@ q4_status launch_amax(const void* x, int dtype, int64_t n, unsigned* amax_bits,
   return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
+// Launches `launch(um, grid, row0)` over chunks of whole rows (multiples of 128)
+// holding fewer than 2^32 units each.
+template <typename F>
+q4_status for_row_chunks(int64_t rows, int64_t nblk, F&& launch) {
+  const int64_t cap = ((int64_t)0xFFFFFE00 / nblk) / 128 * 128;
+  if (cap <= 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+  for (int64_t r0 = 0; r0 < rows; r0 += cap) {
+    const int64_t nr = std::min(cap, rows - r0);
+    const UnitMap um = make_unit_map((uint32_t)(nr * nblk), (uint32_t)nblk, r0);
+    launch(um, (unsigned)ceil_div(nr * nblk, kThreads), r0);
+    if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+  }
+  return Q4_OK;
+}
+
+template <typename T>
+const T* rows_from(const void* x, int64_t r0, int64_t K) {
+  return static_cast<const T*>(x) + r0 * K;
+}
+
 q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                              uint8_t* scales, int layout, const unsigned* amax_bits,
                              float* tensor_scale, cudaStream_t stream) {
-  const int64_t units = rows * (K / 16);
-  const int64_t nsf4 = ceil_div(K / 16, 4);
+  const int64_t nblk = K / 16;
+  const int64_t nsf4 = ceil_div(nblk, 4);
   // every byte of an unpadded MMA layout is written by the kernel
-  if (layout == Q4_SCALES_MMA && (rows % 128 || (K / 16) % 4))
-    Q4_CUDA_TRY(cudaMemsetAsync(scales, 0, mma_scales_bytes(rows, K / 16), stream));
-  if (units == 0) {
-    // an empty tensor still reports g = 1e-12 / 2688
-    return Q4_OK;
+  if (layout == Q4_SCALES_MMA && (rows % 128 || nblk % 4))
+    Q4_CUDA_TRY(cudaMemsetAsync(scales, 0, mma_scales_bytes(rows, nblk), stream));
+  if (rows * nblk == 0) return Q4_OK;  // the API reports g of an empty tensor itself
+  if (dtype != Q4_F32 && dtype != Q4_BF16 && dtype != Q4_F16) return Q4_ERR_INVALID_ARG;
+  const KernelCtl ctl{device_status_ptr(), wait_budget_ns()};
+  const size_t ring = (size_t)kQStages * kQUnits * 16 * (dtype == Q4_F32 ? 4 : 2);
+  static int attr_done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
+  if (!attr_done[dev]) {
+    Q4_CUDA_TRY(cudaFuncSetAttribute(nvfp4_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kQStages * kQUnits * 16 * 4));
+    attr_done[dev] = 1;
   }
-  const unsigned grid = blocks_for(units);
-  switch (dtype) {
-    case Q4_F32: nvfp4_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, rows, K, codes, scales, layout, nsf4, amax_bits, tensor_scale); break;
-    case Q4_BF16: nvfp4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, rows, K, codes, scales, layout, nsf4, amax_bits, tensor_scale); break;
-    case Q4_F16: nvfp4_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, rows, K, codes, scales, layout, nsf4, amax_bits, tensor_scale); break;
-    default: return Q4_ERR_INVALID_ARG;
-  }
-  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  const int64_t max_ctas = (int64_t)num_sms() * 4;
+  return for_row_chunks(rows, nblk, [&](const UnitMap& um, unsigned, int64_t r0) {
+    uint8_t* c = codes + r0 * (K / 2);
+    const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(um.units, kQUnits), max_ctas);
+    if (dtype == Q4_F32)
+      nvfp4_kernel<float><<<grid, kThreads, ring, stream>>>(rows_from<float>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+    else if (dtype == Q4_BF16)
+      nvfp4_kernel<__nv_bfloat16><<<grid, kThreads, ring, stream>>>(rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+    else
+      nvfp4_kernel<__half><<<grid, kThreads, ring, stream>>>(rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+  });
 }
 
 q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                              uint8_t* scales, int layout, cudaStream_t stream) {
-  const int64_t units = rows * (K / 16);
+  const int64_t nblk = K / 16;
   const int64_t nsf4 = ceil_div(K / 32, 4);
   if (layout == Q4_SCALES_MMA && (rows % 128 || (K / 32) % 4))
     Q4_CUDA_TRY(cudaMemsetAsync(scales, 0, mma_scales_bytes(rows, K / 32), stream));
-  if (units == 0) return Q4_OK;
-  const unsigned grid = blocks_for(units);
-  switch (dtype) {
-    case Q4_F32: mxfp4_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, rows, K, codes, scales, layout, nsf4); break;
-    case Q4_BF16: mxfp4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, rows, K, codes, scales, layout, nsf4); break;
-    case Q4_F16: mxfp4_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, rows, K, codes, scales, layout, nsf4); break;
-    default: return Q4_ERR_INVALID_ARG;
-  }
-  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  if (rows * nblk == 0) return Q4_OK;
+  if (dtype != Q4_F32 && dtype != Q4_BF16 && dtype != Q4_F16) return Q4_ERR_INVALID_ARG;
+  return for_row_chunks(rows, nblk, [&](const UnitMap& um, unsigned grid, int64_t r0) {
+    uint8_t* c = codes + r0 * (K / 2);
+    if (dtype == Q4_F32)
+      mxfp4_kernel<float><<<grid, kThreads, 0, stream>>>(rows_from<float>(x, r0, K), um, c, scales, layout, nsf4);
+    else if (dtype == Q4_BF16)
+      mxfp4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4);
+    else
+      mxfp4_kernel<__half><<<grid, kThreads, 0, stream>>>(rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4);
+  });
 }
 
 q4_status launch_quant_int4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                             uint16_t* scales, cudaStream_t stream) {
-  const int64_t units = rows * (K / 16);
-  if (units == 0) return Q4_OK;
-  const unsigned grid = blocks_for(units);
-  switch (dtype) {
-    case Q4_F32: int4_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, rows, K, codes, scales); break;
-    case Q4_BF16: int4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, rows, K, codes, scales); break;
-    case Q4_F16: int4_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, rows, K, codes, scales); break;
-    default: return Q4_ERR_INVALID_ARG;
-  }
-  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  const int64_t nblk = K / 16;
+  if (rows * nblk == 0) return Q4_OK;
+  if (dtype != Q4_F32 && dtype != Q4_BF16 && dtype != Q4_F16) return Q4_ERR_INVALID_ARG;
+  return for_row_chunks(rows, nblk, [&](const UnitMap& um, unsigned grid, int64_t r0) {
+    uint8_t* c = codes + r0 * (K / 2);
+    uint16_t* sc = scales + r0 * (K / 128);
+    if (dtype == Q4_F32)
+      int4_kernel<float><<<grid, kThreads, 0, stream>>>(rows_from<float>(x, r0, K), um, c, sc);
+    else if (dtype == Q4_BF16)
+      int4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(rows_from<__nv_bfloat16>(x, r0, K), um, c, sc);
+    else
+      int4_kernel<__half><<<grid, kThreads, 0, stream>>>(rows_from<__half>(x, r0, K), um, c, sc);
+  });
 }
 
 q4_status launch_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, uint8_t* dst,

@@ -61,6 +61,21 @@ def test_w4a4_mxfp4_raw_operands(lib, shape):
     assert_gemm_close(C.float().cpu().numpy(), R)
 
 
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("shape", [(128, 256, 4096), (256, 2048, 2048), (1000, 2048, 1024)])
+def test_w4a4_bitwise_repeatable(lib, fmt, shape):
+    """Split-K (few tiles) and persistent (many tiles) launches reduce in a fixed
+    order: two runs give the same bits."""
+    M, N, K = shape
+    a, b = (_nv_pair if fmt == "nvfp4" else workloads.mxfp4_pair)(M, N, K, seed=M + N)
+    f = lib.gemm_w4a4_nvfp4 if fmt == "nvfp4" else lib.gemm_w4a4_mxfp4
+    ad, bd = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    C1 = f(ad, bd, K, out_dtype=torch.float32)
+    C2 = f(ad, bd, K, out_dtype=torch.float32)
+    assert torch.equal(C1, C2)
+    assert lib.sync_status() == 0
+
+
 @pytest.mark.parametrize("layout", ["rowmajor", "mma"])
 def test_w4a4_mxfp4_prequantized(lib, layout):
     M, N, K = 200, 600, 1280
