@@ -6,7 +6,8 @@
 // formats).  Also the grouped routed-MoE variant (same section: one low-bit
 // weight matrix per expert, grouped by routing).
 //
-// Structure (one persistent CTA per SM, 6 warps):
+// Structure (one persistent CTA per SM; on large problems the CTAs work in
+// pairs, see P2 below):
 //   warp 0     producer: TMA tiles of packed codes (128-byte swizzle) and bulk
 //              copies of the scale tiles into a 4-stage shared-memory ring.
 //   warps 6-9  (grouped variant only) gather the routed A rows: plain loads,
@@ -20,6 +21,13 @@
 //              quarter).  Unlike tcgen05.cp these stores do not queue behind
 //              the MMAs in the tensor pipe, so the MMA thread issues nothing
 //              but MMAs.
+// P2 (pairs): a cluster of 2 CTAs computes one 256x256 tile with the 2-SM MMA
+// (tcgen05 ... cta_group::2, 256x256x64 per instruction): each CTA holds its
+// 128 rows of A and its 128-row half of B in shared memory, and all 256 rows
+// of B's scales with its own A scales in its TMEM; the even CTA issues the
+// MMAs and each CTA's accumulator receives its 128 rows.  Each SM thus
+// receives half of the B tile per stage.  The odd CTA's scale writers and
+// epilogue warps report to the even CTA's barriers.
 // Every wait is bounded: on timeout the CTA latches Q4_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -31,7 +39,7 @@ namespace q4 {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of codes)
-constexpr int kStages = 4;
+constexpr int kMaxStages = 5;
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
 constexpr int kWriterThreads = 128;    // 4 scale-writer warps
 constexpr int kGatherThreads = 128;    // grouped variant: 4 more warps gather A rows
@@ -58,21 +66,29 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank
   return v;
 }
 
-template <bool NV>
+// Stage: [A codes | B codes (all BN rows, or this CTA's half in pairs) |
+// A scales (128 rows) | B scales (256 rows)]
+template <bool NV, bool P2 = false>
 struct Cfg {
+  static constexpr int kStages = P2 ? 5 : 4;
   static constexpr uint32_t kSfaBytes = NV ? 2048u : 1024u;  // 128 rows x (16 | 8) scales
   static constexpr uint32_t kSfbBytes = 2 * kSfaBytes;        // 256 rows
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr uint32_t kBLoad = P2 ? kBBytes / 2 : kBBytes;
+  static constexpr uint32_t kSfaOff = kABytes + kBLoad;
+  static constexpr uint32_t kSfbOff = kSfaOff + kSfaBytes;
+  static constexpr uint32_t kStageBytes = kSfbOff + kSfbBytes;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr uint32_t kSfChunks = NV ? 4u : 2u;  // 512-byte chunks per 128 rows per stage
 };
 static_assert(Cfg<true>::kStageBytes % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0, "");
-static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory");
+static_assert(Cfg<true, true>::kStageBytes % 1024 == 0 && Cfg<false, true>::kStageBytes % 1024 == 0, "");
+static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<true, true>::kSmemBytes <= 232448, "shared memory");
+static_assert(kAccCols + kMaxStages * kSfColsPerStage <= kTmemCols, "TMEM columns");
 
 struct Smem {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t sf_full[kStages];  // the stage's scales are in TMEM
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t sf_full[kMaxStages];  // the stage's scales are in TMEM
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t mma_done;
@@ -108,9 +124,10 @@ struct Params {
   KernelCtl ctl;
 };
 
-// Dense tiles for a cluster of CM CTAs stacked along M (they share the B tile):
-// cluster tile t -> (m group, n) in bands of 16 M tiles, so a band's A tiles
-// stay in L2 while B streams; CTA rank r takes M tile group * CM + r.
+// Dense tiles for CM CTAs stacked along M (CM = 2: a CTA pair sharing one
+// 256-wide N tile): cluster tile t -> (m group, n) in bands of 16 M tiles, so
+// a band's A tiles stay in L2 while B streams; CTA rank r takes M tile
+// group * CM + r.
 template <int CM>
 __device__ __forceinline__ TileInfo dense_tile(const Params& p, int t, int crank) {
   constexpr int GMG = 16 / CM;  // m groups per band
@@ -151,11 +168,12 @@ __device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sch
 // KS > 1: split-K -- a cluster of KS CTAs owns one output tile, each CTA a
 // slice of the K blocks; the FP32 partial tiles are reduced through
 // distributed shared memory in rank order (deterministic).
-template <bool NV, bool GROUPED, int CM, int KS = 1>
+template <bool NV, bool GROUPED, int KS = 1, bool P2 = false>
 __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-  using C_ = Cfg<NV>;
+  using C_ = Cfg<NV, P2>;
+  constexpr int kStages = C_::kStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -164,16 +182,17 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
   __shared__ int s_sched[GROUPED ? kMaxExperts + 1 : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  static_assert(!GROUPED || CM == 1, "");
-  static_assert(KS == 1 || (CM == 1 && !GROUPED), "");
-  constexpr int CL = CM * KS;                                // CTAs per cluster
-  const int crank = CM > 1 ? (int)cluster_ctarank() : 0;  // rank along M in the cluster
+  static_assert(!P2 || (KS == 1 && !GROUPED), "");
+  static_assert(KS == 1 || !GROUPED, "");
+  constexpr int TM = P2 ? 2 : 1;                           // CTAs along M per tile
+  constexpr int CL = TM * KS;                              // CTAs per cluster
+  const int crank = P2 ? (int)cluster_ctarank() : 0;      // rank in the pair
   const int krank = KS > 1 ? (int)cluster_ctarank() : 0;  // rank along K (split-K)
+  const bool leader = crank == 0;                          // issues the pair's MMAs
   const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;   // cluster index and count
   const int nkb_all = (int)(p.K / BK);
   const int kbs = (nkb_all + KS - 1) / KS;
   const int kb_begin = min(nkb_all, krank * kbs), kb_end = min(nkb_all, kb_begin + kbs);
-  constexpr uint16_t kMask = (uint16_t)((1u << CM) - 1u);
 
   int total_tiles;
   if constexpr (GROUPED) {
@@ -181,17 +200,17 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     __syncthreads();
     total_tiles = s_sched[p.E] * p.num_n;
   } else {
-    total_tiles = ((p.num_m + CM - 1) / CM) * p.num_n;
+    total_tiles = ((p.num_m + TM - 1) / TM) * p.num_n;
   }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm->full[s]), GROUPED ? 1 + kGatherThreads : 1);
-      mbar_init(smem_u32(&sm->empty[s]), CM);  // every CTA of the cluster releases
-      mbar_init(smem_u32(&sm->sf_full[s]), 4);  // one arrival per scale-writer warp
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+      mbar_init(smem_u32(&sm->sf_full[s]), P2 ? 8 : 4);  // one arrival per scale-writer warp
     }
     mbar_init(smem_u32(&sm->acc_full), 1);
-    mbar_init(smem_u32(&sm->acc_empty), 4);
+    mbar_init(smem_u32(&sm->acc_empty), P2 ? 8 : 4);  // one arrival per epilogue warp
     mbar_init(smem_u32(&sm->mma_done), 1);
     sm->abort = 0;
     fence_mbar_init();
@@ -199,19 +218,29 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     prefetch_tmap(&tmap_b);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (P2) {
+      tmem_alloc_pair(smem_u32(&sm->tmem_base), kTmemCols);  // both CTAs of the pair, same columns
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL > 1) cluster_barrier_sync();  // peers' barriers exist before any multicast
+  if constexpr (CL > 1) cluster_barrier_sync();  // peers' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort_flag = &sm->abort;
 
+  // arrive on the pair leader's copy of a barrier (this CTA's own when not paired)
+  auto arrive_leader = [&](uint64_t* bar) {
+    if constexpr (P2) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
+    else mbar_arrive(smem_u32(bar));
+  };
   auto tile_at = [&](int t) -> TileInfo {
     if constexpr (GROUPED) return grouped_tile(p, s_sched, t);
-    else return dense_tile<CM>(p, t, crank);
+    else return dense_tile<TM>(p, t, crank);
   };
 
   if (warp == 0) {
@@ -231,11 +260,11 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const uint8_t* sfb = p.b_sf + (int64_t)ti.e * p.b_sf_expert_bytes;
       const int nb0 = ti.n0 / 128;
       const bool b_hi = nb0 + 1 < nblk_b;
-      const uint32_t bytes = (GROUPED ? 0u : kABytes) + kBBytes + (a_sf_ok ? C_::kSfaBytes : 0u) +
+      const uint32_t bytes = (GROUPED ? 0u : kABytes) + C_::kBLoad + (a_sf_ok ? C_::kSfaBytes : 0u) +
                              C_::kSfaBytes * (b_hi ? 2 : 1);
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+        if (!mbar_wait<P2>(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
@@ -245,24 +274,14 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
           mbar_arrive_expect_tx(full, bytes);
           if constexpr (!GROUPED) tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
           const int64_t jsf = (int64_t)kb * C_::kSfChunks * 512;
-          if (a_sf_ok) bulk_load(smem_u32(st + kABytes + kBBytes), sfa + jsf, C_::kSfaBytes, full);
+          if (a_sf_ok) bulk_load(smem_u32(st + C_::kSfaOff), sfa + jsf, C_::kSfaBytes, full);
           const uint8_t* sfb0 = sfb + (int64_t)nb0 * nsf4_a * 512 + jsf;
-          const uint32_t sfb_s = smem_u32(st + kABytes + kBBytes + C_::kSfaBytes);
-          if constexpr (CM == 1) {
-            tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2), b_row, full);
-            bulk_load(sfb_s, sfb0, C_::kSfaBytes, full);
-            if (b_hi) bulk_load(sfb_s + C_::kSfaBytes, sfb0 + nsf4_a * 512, C_::kSfaBytes, full);
-          } else {
-            // this rank's slice of the shared B tile and of its scales, to every CTA
-            constexpr int kSlice = BN / CM;
-            tma_load_2d_mc(smem_u32(st + kABytes + crank * kSlice * (BK / 2)), &tmap_b, kb * (BK / 2),
-                           b_row + crank * kSlice, full, kMask);
-            constexpr uint32_t kPart = C_::kSfaBytes * 2 / CM;  // scale bytes per rank
-            const int h = (int)(crank * kPart / C_::kSfaBytes);  // 128-row half of the B tile
-            const uint32_t off = crank * kPart - (uint32_t)h * C_::kSfaBytes;
-            if (h == 0 || b_hi)
-              bulk_load_mc(sfb_s + crank * kPart, sfb0 + (int64_t)h * nsf4_a * 512 + off, kPart, full, kMask);
-          }
+          const uint32_t sfb_s = smem_u32(st + C_::kSfbOff);
+          // B codes: the whole tile, or this CTA's 128-row half of the pair's tile
+          tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2),
+                      b_row + (P2 ? crank * (BN / 2) : 0), full);
+          bulk_load(sfb_s, sfb0, C_::kSfaBytes, full);
+          if (b_hi) bulk_load(sfb_s + C_::kSfaBytes, sfb0 + nsf4_a * 512, C_::kSfaBytes, full);
         }
         issued[stage] = 1;
         issued_phase[stage] = phase;
@@ -273,28 +292,29 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     if (lane == 0) {
       KernelCtl drain = p.ctl;
       for (int s = 0; s < kStages; ++s)
-        if (issued[s]) mbar_wait(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
+        if (issued[s]) mbar_wait<P2>(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // (in a pair only the even CTA issues; the odd CTA's warp 1 only holds TMEM)
     uint32_t stage = 0, phase = 0, tcount = 0;
     bool alive = true;
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       for (int t = cid; t < total_tiles && alive; t += ncl, ++tcount) {
         const TileInfo ti = tile_at(t);
         if (!ti.ok) { --tcount; continue; }
-        if (!mbar_wait(smem_u32(&sm->acc_empty), (tcount & 1) ^ 1, p.ctl, abort_flag)) {
+        if (!mbar_wait<P2>(smem_u32(&sm->acc_empty), (tcount & 1) ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
         tc_fence_after();
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+          if (!mbar_wait<P2>(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
             alive = false;
             break;
           }
-          if (!mbar_wait(smem_u32(&sm->sf_full[stage]), phase, p.ctl, abort_flag)) {
+          if (!mbar_wait<P2>(smem_u32(&sm->sf_full[stage]), phase, p.ctl, abort_flag)) {
             alive = false;
             break;
           }
@@ -307,21 +327,27 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
             const uint64_t bd = smem_desc(st + kABytes + 32 * k, 16, 1024, 2);
             const uint32_t j = NV ? k : k >> 1;
             const uint32_t sf_id = NV ? 0u : (k & 1) * 2;
-            const uint32_t idesc = fp4_idesc(BM, BN, !NV, sf_id, sf_id);
-            tc_mma_fp4<NV ? 4 : 2>(tmem, ad, bd, idesc, sf_t + 4 * j, sf_t + 16 + 8 * j,
-                                   (kb != kb_begin || k != 0) ? 1u : 0u);
+            const uint32_t idesc = fp4_idesc(BM * TM, BN, !NV, sf_id, sf_id);
+            const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
+            if constexpr (P2)
+              tc_mma_fp4_pair<NV ? 4 : 2>(tmem, ad, bd, idesc, sf_t + 4 * j, sf_t + 16 + 8 * j, acc);
+            else
+              tc_mma_fp4<NV ? 4 : 2>(tmem, ad, bd, idesc, sf_t + 4 * j, sf_t + 16 + 8 * j, acc);
           }
-          if constexpr (CM == 1) tc_commit(smem_u32(&sm->empty[stage]));
-          else tc_commit_mc(smem_u32(&sm->empty[stage]), kMask);
+          // the stage is free in both CTAs once these MMAs are done
+          if constexpr (P2) tc_commit_pair_mc(smem_u32(&sm->empty[stage]), 3);
+          else tc_commit(smem_u32(&sm->empty[stage]));
           if (++stage == kStages) stage = 0, phase ^= 1;
         }
         if (!alive) break;
-        tc_commit(smem_u32(&sm->acc_full));
+        if constexpr (P2) tc_commit_pair_mc(smem_u32(&sm->acc_full), 3);
+        else tc_commit(smem_u32(&sm->acc_full));
       }
       // all MMAs this thread issued are complete before TMEM is released
-      tc_commit(smem_u32(&sm->mma_done));
+      if constexpr (P2) tc_commit_pair_mc(smem_u32(&sm->mma_done), 1);
+      else tc_commit(smem_u32(&sm->mma_done));
       KernelCtl drain = p.ctl;
-      mbar_wait(smem_u32(&sm->mma_done), 0, drain, nullptr);
+      mbar_wait<P2>(smem_u32(&sm->mma_done), 0, drain, nullptr);
     }
     __syncwarp();
   } else if (warp >= kWriterWarp0 && warp < kWriterWarp0 + 4) {
@@ -338,15 +364,15 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+        if (!mbar_wait<P2>(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
         // the MMAs that last read this stage's scale columns completed before
         // the stage was refilled (empty -> producer -> full)
         tc_fence_after();
-        const uint8_t* sfa_s = smem + stage * C_::kStageBytes + kABytes + kBBytes;
-        const uint8_t* sfb_s = sfa_s + C_::kSfaBytes;
+        const uint8_t* sfa_s = smem + stage * C_::kStageBytes + C_::kSfaOff;
+        const uint8_t* sfb_s = smem + stage * C_::kStageBytes + C_::kSfbOff;
         const uint32_t sf_t = tmem + lane_base + kAccCols + stage * kSfColsPerStage;
 #pragma unroll
         for (uint32_t j = 0; j < C_::kSfChunks; ++j) {
@@ -360,7 +386,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->sf_full[stage]));
+        if (lane == 0) arrive_leader(&sm->sf_full[stage]);
         if (++stage == kStages) stage = 0, phase ^= 1;
       }
     }
@@ -379,7 +405,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const int tokr = __ldg(p.row_token + (r < ti.m_end ? r : ti.m_row0));
       const uint8_t* src = p.a_codes + (int64_t)tokr * (p.K / 2);
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+        if (!mbar_wait<P2>(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
@@ -403,7 +429,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     for (int t = cid; t < total_tiles; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
-      if (!mbar_wait(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
+      if (!mbar_wait<P2>(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
       tc_fence_after();
       if constexpr (KS > 1) {
         // split-K: this CTA's FP32 partial tile -> shared memory (the ring is idle:
@@ -476,16 +502,18 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm->acc_empty));
+      if (lane == 0) arrive_leader(&sm->acc_empty);
       ++tcount;
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (P2) cluster_barrier_sync();  // the pair's MMAs are complete in both CTAs
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (P2) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
   if constexpr (KS > 1) {
     // rank q reduces rows [q * 128 / KS, (q + 1) * 128 / KS) of the tile over all
@@ -575,67 +603,65 @@ __global__ void __launch_bounds__(128)
 
 namespace {
 
-template <bool NV, bool GROUPED, int CM, int KS = 1>
+template <bool NV, bool GROUPED, int KS = 1, bool P2 = false>
 q4_status set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!done[dev]) {
-    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, CM, KS>,
+    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, KS, P2>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)Cfg<NV>::kSmemBytes));
+                                     (int)Cfg<NV, P2>::kSmemBytes));
     done[dev] = 1;
   }
   return Q4_OK;
 }
 
-template <bool NV, int CM>
+// Persistent dense launch: single CTAs, or CTA pairs (P2) on 256x256 tiles.
+template <bool NV, bool P2>
 q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                        cudaStream_t stream) {
   q4_status st;
-  if ((st = set_smem_attr<NV, false, CM>()) != Q4_OK) return st;
-  const int ctiles = ((p.num_m + CM - 1) / CM) * p.num_n;  // cluster tiles
+  if ((st = set_smem_attr<NV, false, 1, P2>()) != Q4_OK) return st;
+  constexpr int CL = P2 ? 2 : 1;
+  const int ctiles = ((p.num_m + CL - 1) / CL) * p.num_n;  // cluster tiles
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(block_threads<false>(), 1, 1);
-  cfg.dynamicSmemBytes = Cfg<NV>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<NV, P2>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // persistent clusters: exactly as many as can be resident at once, so no
   // cluster waits for a second wave with its whole share of tiles
-  static int max_active[64][5] = {{0}};
+  static int max_active[64][2] = {{0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
-  if (!max_active[dev][CM]) {
+  if (!max_active[dev][P2]) {
     int n = 0;
-    cfg.gridDim = dim3((unsigned)(num_sms() / CM * CM), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&n, fp4_gemm_kernel<NV, false, CM>, &cfg) != cudaSuccess || n <= 0)
-      n = num_sms() / CM;
-    max_active[dev][CM] = std::min(n, num_sms() / CM);
+    cfg.gridDim = dim3((unsigned)(num_sms() / CL * CL), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, fp4_gemm_kernel<NV, false, 1, P2>, &cfg) != cudaSuccess || n <= 0)
+      n = num_sms() / CL;
+    max_active[dev][P2] = std::min(n, num_sms() / CL);
   }
-  const int clusters = std::max(1, std::min(ctiles, max_active[dev][CM]));
-  cfg.gridDim = dim3((unsigned)(clusters * CM), 1, 1);
-  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, CM>, ta, tb, p));
+  const int clusters = std::max(1, std::min(ctiles, max_active[dev][P2]));
+  cfg.gridDim = dim3((unsigned)(clusters * CL), 1, 1);
+  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, 1, P2>, ta, tb, p));
   return Q4_OK;
 }
 
-// CTAs stacked along M can share (multicast) each B tile.  Measured on GB300
-// at 8192 x 28672 x 8192 and 4096 x 8192 x 8192, clusters of 2 and 4 run no
-// faster than single CTAs (the limit is the operand feed of the one-SM MMA,
-// not L2 bandwidth), so single CTAs are used.
 // Split-K for problems with few output tiles: KS CTAs (one cluster) per tile,
 // launched as exactly tiles x KS CTAs (one tile per cluster).
 template <bool NV, int KS>
 q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                         cudaStream_t stream) {
-  static_assert(KS * 0 + (BM * (BN + 4) * 4) <= kStages * Cfg<NV>::kStageBytes, "partial tile fits");
+  static_assert(KS * 0 + (BM * (BN + 4) * 4) <= Cfg<NV>::kStages * Cfg<NV>::kStageBytes, "partial tile fits");
   q4_status st;
-  if ((st = set_smem_attr<NV, false, 1, KS>()) != Q4_OK) return st;
+  if ((st = set_smem_attr<NV, false, KS>()) != Q4_OK) return st;
   const int tiles = p.num_m * p.num_n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * KS), 1, 1);
@@ -649,7 +675,7 @@ q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Para
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, 1, KS>, ta, tb, p));
+  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, KS>, ta, tb, p));
   return Q4_OK;
 }
 
@@ -667,20 +693,15 @@ q4_status dispatch_splitk(int ks, const CUtensorMap& ta, const CUtensorMap& tb, 
   }
 }
 
-int cluster_m(int64_t M) {
-  (void)M;
-  return 1;
-}
 
 }  // namespace
 
 q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0) return Q4_OK;
-  const int cm = cluster_m(a.M);
   CUtensorMap ta, tb;
   q4_status st;
   if ((st = make_tmap_2d_u8(&ta, a.a_codes, a.K / 2, a.M, a.K / 2, BK / 2, BM, true)) != Q4_OK) return st;
-  if ((st = make_tmap_2d_u8(&tb, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN / cm, true)) != Q4_OK) return st;
+  if ((st = make_tmap_2d_u8(&tb, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN, true)) != Q4_OK) return st;
   Params p = {};
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.a_sf = a.a_scales; p.b_sf = a.b_scales; p.b_sf_expert_bytes = 0;
@@ -696,21 +717,18 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   const int tiles = p.num_m * p.num_n, nkb = (int)(a.K / BK);
   if (tiles * 2 <= num_sms() && nkb >= 2) {
     const int ks = std::min(4, std::min(num_sms() / tiles, nkb));
-    if (ks >= 2) {
-      CUtensorMap tb1;
-      if ((st = make_tmap_2d_u8(&tb1, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN, true)) != Q4_OK) return st;
-      return a.nvfp4 ? dispatch_splitk<true>(ks, ta, tb1, p, stream)
-                     : dispatch_splitk<false>(ks, ta, tb1, p, stream);
-    }
+    if (ks >= 2)
+      return a.nvfp4 ? dispatch_splitk<true>(ks, ta, tb, p, stream)
+                     : dispatch_splitk<false>(ks, ta, tb, p, stream);
   }
-  if (a.nvfp4) {
-    if (cm == 4) return launch_dense<true, 4>(ta, tb, p, stream);
-    if (cm == 2) return launch_dense<true, 2>(ta, tb, p, stream);
-    return launch_dense<true, 1>(ta, tb, p, stream);
+  // CTA pairs (2-SM MMA on 256x256 tiles) whenever M spans two tiles: each SM
+  // then receives half of each B tile
+  if (p.num_m >= 2) {
+    CUtensorMap tb2;  // 128-row boxes: each CTA loads its half of the B tile
+    if ((st = make_tmap_2d_u8(&tb2, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN / 2, true)) != Q4_OK) return st;
+    return a.nvfp4 ? launch_dense<true, true>(ta, tb2, p, stream) : launch_dense<false, true>(ta, tb2, p, stream);
   }
-  if (cm == 4) return launch_dense<false, 4>(ta, tb, p, stream);
-  if (cm == 2) return launch_dense<false, 2>(ta, tb, p, stream);
-  return launch_dense<false, 1>(ta, tb, p, stream);
+  return a.nvfp4 ? launch_dense<true, false>(ta, tb, p, stream) : launch_dense<false, false>(ta, tb, p, stream);
 }
 
 q4_status launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int E,
@@ -745,8 +763,8 @@ q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
   p.a_codes = a.a_codes;
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
-  if ((st = set_smem_attr<true, true, 1>()) != Q4_OK) return st;
-  fp4_gemm_kernel<true, true, 1><<<(unsigned)num_sms(), block_threads<true>(), Cfg<true>::kSmemBytes,
+  if ((st = set_smem_attr<true, true>()) != Q4_OK) return st;
+  fp4_gemm_kernel<true, true><<<(unsigned)num_sms(), block_threads<true>(), Cfg<true>::kSmemBytes,
                                 stream>>>(tb, tb, p);
   return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }

@@ -33,6 +33,31 @@ def test_w4a4_nvfp4_raw_operands(lib, shape):
     assert lib.sync_status() == 0
 
 
+# More than 76 output tiles of 128 x 256 and M above one tile: CTA pairs
+# (2-SM MMA, 256 x 256 tiles).  1100 rows = 9 M tiles (the last pair's second
+# CTA lies past M); N = 2350 ends in a tile whose upper 128-row B half is
+# entirely past N; N = 2600 ends in a partial half.
+PAIR_SHAPES = [(1100, 2350, 768), (1024, 2600, 512)]
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_w4a4_cta_pairs(lib, fmt, shape):
+    M, N, K = shape
+    if fmt == "nvfp4":
+        a, b = _nv_pair(M, N, K, seed=M + 7)
+        C = lib.gemm_w4a4_nvfp4(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), K,
+                                out_dtype=torch.float32)
+        R = oracle.gemm_w4a4_nvfp4(*oracle.quantize_nvfp4(a), *oracle.quantize_nvfp4(b))
+    else:
+        a, b = workloads.mxfp4_pair(M, N, K, seed=M + 9)
+        C = lib.gemm_w4a4_mxfp4(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), K,
+                                out_dtype=torch.float32)
+        R = oracle.gemm_w4a4_mxfp4(*oracle.quantize_mxfp4(a), *oracle.quantize_mxfp4(b))
+    assert_gemm_close(C.cpu().numpy(), R)
+    assert lib.sync_status() == 0
+
+
 @pytest.mark.parametrize("layout", ["rowmajor", "mma"])
 @pytest.mark.parametrize("shape", [(130, 300, 768), (512, 768, 1024)])
 def test_w4a4_nvfp4_prequantized_bf16(lib, layout, shape):
@@ -62,7 +87,8 @@ def test_w4a4_mxfp4_raw_operands(lib, shape):
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
-@pytest.mark.parametrize("shape", [(128, 256, 4096), (256, 2048, 2048), (1000, 2048, 1024)])
+@pytest.mark.parametrize("shape", [(128, 256, 4096), (256, 2048, 2048), (1000, 2048, 1024),
+                                   (1100, 2350, 768)])
 def test_w4a4_bitwise_repeatable(lib, fmt, shape):
     """Split-K (few tiles) and persistent (many tiles) launches reduce in a fixed
     order: two runs give the same bits."""
