@@ -46,9 +46,9 @@ FP4_OVER_BF16 = 6.0
 # ncu-measured DRAM traffic per launch of the dominant kernel (bytes), keyed by
 # workload; None until a capture of the current kernel exists.
 NCU_TRAFFIC = {
-    # prof_w4a16_decode (profiles/w4a16_decode.md): mean dram__bytes_read + write of the
-    # M = 1, 4, 16 launches of the current w4a16_kernel at N = K = 8192
-    "decode": 34.8e6,
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum, mean over the M = 1, 4, 16
+    # launches of the current w4a16_kernel at N = K = 8192
+    "decode": 34.76e6,
 }
 
 
