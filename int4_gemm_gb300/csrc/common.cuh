@@ -331,9 +331,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier given by its shared::cluster address (possibly a peer's).
+// Arrive on an mbarrier given by its shared::cluster address (possibly a
+// peer's).  CTA-scope release: what these arrivals order is TMEM traffic,
+// which tcgen05 fences order; a cluster-scope release would also wait for all
+// of the thread's outstanding global stores.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 

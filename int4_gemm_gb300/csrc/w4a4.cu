@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
                              C_::kSfaBytes * (b_hi ? 2 : 1);
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait<P2>(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     if (lane == 0) {
       KernelCtl drain = p.ctl;
       for (int s = 0; s < kStages; ++s)
-        if (issued[s]) mbar_wait<P2>(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
+        if (issued[s]) mbar_wait(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -304,17 +304,17 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       for (int t = cid; t < total_tiles && alive; t += ncl, ++tcount) {
         const TileInfo ti = tile_at(t);
         if (!ti.ok) { --tcount; continue; }
-        if (!mbar_wait<P2>(smem_u32(&sm->acc_empty), (tcount & 1) ^ 1, p.ctl, abort_flag)) {
+        if (!mbar_wait(smem_u32(&sm->acc_empty), (tcount & 1) ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
         tc_fence_after();
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait<P2>(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
             alive = false;
             break;
           }
-          if (!mbar_wait<P2>(smem_u32(&sm->sf_full[stage]), phase, p.ctl, abort_flag)) {
+          if (!mbar_wait(smem_u32(&sm->sf_full[stage]), phase, p.ctl, abort_flag)) {
             alive = false;
             break;
           }
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       if constexpr (P2) tc_commit_pair_mc(smem_u32(&sm->mma_done), 1);
       else tc_commit(smem_u32(&sm->mma_done));
       KernelCtl drain = p.ctl;
-      mbar_wait<P2>(smem_u32(&sm->mma_done), 0, drain, nullptr);
+      mbar_wait(smem_u32(&sm->mma_done), 0, drain, nullptr);
     }
     __syncwarp();
   } else if (warp >= kWriterWarp0 && warp < kWriterWarp0 + 4) {
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait<P2>(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+        if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const int tokr = __ldg(p.row_token + (r < ti.m_end ? r : ti.m_row0));
       const uint8_t* src = p.a_codes + (int64_t)tokr * (p.K / 2);
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait<P2>(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
         }
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     for (int t = cid; t < total_tiles; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
-      if (!mbar_wait<P2>(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
+      if (!mbar_wait(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
       tc_fence_after();
       if constexpr (KS > 1) {
         // split-K: this CTA's FP32 partial tile -> shared memory (the ring is idle:
@@ -721,9 +721,13 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
       return a.nvfp4 ? dispatch_splitk<true>(ks, ta, tb, p, stream)
                      : dispatch_splitk<false>(ks, ta, tb, p, stream);
   }
-  // Single-CTA tiles.  The CTA-pair variant (launch_dense<NV, true>, B tile
-  // boxes of BN / 2 rows) is parity-green but measured 1.40 ms against 0.75 ms
-  // at 8192 x 28672 x 8192 on GB300, so it is not selected.
+  // CTA pairs (2-SM MMA on 256x256 tiles) whenever M spans two tiles: each SM
+  // then receives half of each B tile
+  if (p.num_m >= 2) {
+    CUtensorMap tb2;  // 128-row boxes: each CTA loads its half of the B tile
+    if ((st = make_tmap_2d_u8(&tb2, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN / 2, true)) != Q4_OK) return st;
+    return a.nvfp4 ? launch_dense<true, true>(ta, tb2, p, stream) : launch_dense<false, true>(ta, tb2, p, stream);
+  }
   return a.nvfp4 ? launch_dense<true, false>(ta, tb, p, stream) : launch_dense<false, false>(ta, tb, p, stream);
 }
 

@@ -33,15 +33,16 @@ def test_w4a4_nvfp4_raw_operands(lib, shape):
     assert lib.sync_status() == 0
 
 
-# More than 76 output tiles of 128 x 256, so the persistent (not split-K)
-# launch: 1100 rows end in a partial M tile; N = 2350 ends in a tile whose
-# upper 128-row B block lies entirely past N, N = 2600 in a partial block.
-RAGGED_SHAPES = [(1100, 2350, 768), (1024, 2600, 512)]
+# More than 76 output tiles of 128 x 256 and M above one tile: CTA pairs
+# (2-SM MMA, 256 x 256 tiles).  1100 rows = 9 M tiles (the last pair's second
+# CTA lies past M); N = 2350 ends in a tile whose upper 128-row B half lies
+# entirely past N, N = 2600 in a partial half.
+PAIR_SHAPES = [(1100, 2350, 768), (1024, 2600, 512)]
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
-@pytest.mark.parametrize("shape", RAGGED_SHAPES)
-def test_w4a4_persistent_ragged(lib, fmt, shape):
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_w4a4_cta_pairs(lib, fmt, shape):
     M, N, K = shape
     if fmt == "nvfp4":
         a, b = _nv_pair(M, N, K, seed=M + 7)
