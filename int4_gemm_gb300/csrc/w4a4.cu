@@ -10,13 +10,14 @@
 // pairs, see P2 below):
 //   warp 0     producer: TMA tiles of packed codes (128-byte swizzle) and bulk
 //              copies of the scale tiles into a 4-stage shared-memory ring.
-//   warps 6-9  (grouped variant only) gather the routed A rows: plain loads,
-//              swizzled shared stores, proxy fence, mbarrier arrive.
 //   warp 1     allocates TMEM; one lane issues tcgen05.mma ... block_scale,
 //              128x256x64 per instruction, FP32 accumulation in TMEM.
 //   warps 2-5  epilogue: tcgen05.ld of the 128x256 FP32 accumulator, times
 //              gA * gB (NVFP4), rounded to bf16 (or kept FP32), stored.
-//   4 warps    scale writers: each stage's scale tiles go from shared memory
+//   warps 10-17 (grouped variant only) gather the routed A rows, two threads
+//              per row: plain loads up to four K blocks ahead, swizzled
+//              shared stores, proxy fence, one mbarrier arrival per warp.
+//   warps 6-9  scale writers: each stage's scale tiles go from shared memory
 //              to TMEM through registers (tcgen05.st, one warp per TMEM lane
 //              quarter).  Unlike tcgen05.cp these stores do not queue behind
 //              the MMAs in the tensor pipe, so the MMA thread issues nothing
@@ -42,9 +43,9 @@ constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of co
 constexpr int kMaxStages = 5;
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
 constexpr int kWriterThreads = 128;    // 4 scale-writer warps
-constexpr int kGatherThreads = 128;    // grouped variant: 4 more warps gather A rows
+constexpr int kGatherThreads = 256;    // grouped variant: 8 more warps gather A rows (2 threads per row)
 constexpr int kWriterWarp0 = (kThreads + kWriterThreads) / 32 - 4;  // warps 6-9
-constexpr int kGatherWarp0 = (kThreads + kWriterThreads) / 32;      // warps 10-13 (grouped)
+constexpr int kGatherWarp0 = (kThreads + kWriterThreads) / 32;      // warps 10-17 (grouped)
 template <bool GROUPED>
 constexpr int block_threads() { return kThreads + kWriterThreads + (GROUPED ? kGatherThreads : 0); }
 constexpr uint32_t kABytes = BM * BK / 2;     // 16 KiB
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm->full[s]), GROUPED ? 1 + kGatherThreads : 1);
+      mbar_init(smem_u32(&sm->full[s]), GROUPED ? 1 + kGatherThreads / 32 : 1);  // producer (+ gather warps)
       mbar_init(smem_u32(&sm->empty[s]), 1);
       mbar_init(smem_u32(&sm->sf_full[s]), P2 ? 8 : 4);  // one arrival per scale-writer warp
     }
@@ -392,34 +393,73 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     }
   } else if (GROUPED && warp >= kGatherWarp0) {
     // ------------------------------------------------------------ A-row gather (grouped)
-    // Thread i copies routed row i of the tile (its token's 128 code bytes of
-    // this K block) into the 128-byte-swizzled A tile, then makes the writes
-    // visible to the tensor core's async proxy before arriving.
+    // Threads 2r, 2r + 1 copy routed row r of the tile (its token's 128 code
+    // bytes of this K block, 64 each) into the 128-byte-swizzled A tile, then
+    // make the writes
+    // visible to the tensor core's async proxy before arriving.  Loads run
+    // kStages jobs ahead of the stores (a register ring, one entry per slot),
+    // so the L2 latency of the routed rows overlaps the pipeline.
     const int i = threadIdx.x - kGatherWarp0 * 32;
+    const int row = i >> 1, half = i & 1;
     uint32_t stage = 0, phase = 0;
-    bool alive = true;
-    for (int t = cid; t < total_tiles && alive; t += ncl) {
+    // this thread's 64 source bytes of routed row `row` in tile t (the tile's
+    // first row for rows past its end)
+    auto row_src = [&](int t) -> const uint8_t* {
       const TileInfo ti = tile_at(t);
-      if (!ti.ok) continue;
-      const int r = ti.m_row0 + i;
+      const int r = ti.m_row0 + row;
       const int tokr = __ldg(p.row_token + (r < ti.m_end ? r : ti.m_row0));
-      const uint8_t* src = p.a_codes + (int64_t)tokr * (p.K / 2);
-      for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
-          alive = false;
-          break;
+      return p.a_codes + (int64_t)tokr * (p.K / 2) + half * 64;
+    };
+    auto next_tile = [&](int t) {
+      while (t < total_tiles && !tile_at(t).ok) t += ncl;
+      return t;
+    };
+    auto load_blk = [&](const uint8_t* src, int kb, uint4 (&v)[4]) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = __ldg(reinterpret_cast<const uint4*>(src + kb * (BK / 2)) + c);
+    };
+    // jobs (tile, K block) in order; buf[j] holds the rows of the job that
+    // will fill the j-th slot of the next round of kStages slots
+    int jt = next_tile(cid), jkb = kb_begin;  // the last job handed out
+    const uint8_t* jsrc = jt < total_tiles ? row_src(jt) : nullptr;
+    bool first = true;
+    auto next_job = [&]() {  // advance (jt, jkb, jsrc); false when no job is left
+      if (first) {
+        first = false;
+      } else if (++jkb == kb_end) {
+        jkb = kb_begin;
+        jt = next_tile(jt + ncl);
+        if (jt < total_tiles) jsrc = row_src(jt);
+      }
+      return jt < total_tiles && jkb < kb_end;
+    };
+    uint4 buf[kStages][4];
+    bool valid[kStages];
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) {
+      valid[j] = next_job();
+      if (valid[j]) load_blk(jsrc, jkb, buf[j]);
+    }
+    bool go = true;
+    while (go) {
+#pragma unroll
+      for (int j = 0; j < kStages; ++j) {
+        if (!go || !valid[j]) { go = false; continue; }
+        // warp-uniform outcome: the lanes meet at __syncwarp below
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag))) {
+          go = false;
+          continue;
         }
-        uint4 v[8];
+        uint8_t* dst = smem + stage * C_::kStageBytes + row * (BK / 2);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          v[c] = __ldg(reinterpret_cast<const uint4*>(src + kb * (BK / 2)) + c);
-        uint8_t* dst = smem + stage * C_::kStageBytes + i * (BK / 2);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(dst + ((c ^ (i & 7)) << 4)) = v[c];
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&sm->full[stage]));
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(dst + (((4 * half + c) ^ (row & 7)) << 4)) = buf[j][c];
+        fence_proxy_async_smem();  // each thread's stores, then one arrival per warp
+        __syncwarp();
+        if ((i & 31) == 0) mbar_arrive(smem_u32(&sm->full[stage]));
         if (++stage == kStages) stage = 0, phase ^= 1;
+        valid[j] = next_job();  // refill with the job kStages ahead
+        if (valid[j]) load_blk(jsrc, jkb, buf[j]);
       }
     }
   } else {
