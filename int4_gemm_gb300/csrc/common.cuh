@@ -32,6 +32,14 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: wait until the previous kernel in the stream
+// has completed and its writes are visible (a no-op without a programmatic
+// dependency); let the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers
 // ---------------------------------------------------------------------------

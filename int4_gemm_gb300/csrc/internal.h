@@ -82,6 +82,27 @@ q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_byt
                           bool swizzle128);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Launch with programmatic dependent launch allowed: the kernel may start while
+// the previous kernel in the stream finishes; it calls pdl_wait() (common.cuh)
+// before its first global-memory access, so it sees all of that kernel's
+// writes.
+template <typename... KArgs, typename... Args>
+q4_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? Q4_OK
+                                                                                    : Q4_ERR_CUDA;
+}
 inline size_t mma_scales_bytes(int64_t rows, int64_t nsf) {
   return (size_t)(ceil_div(rows, 128) * 128) * (size_t)(ceil_div(nsf, 4) * 4);
 }

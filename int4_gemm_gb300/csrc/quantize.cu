@@ -96,6 +96,8 @@ __device__ __forceinline__ void load16(const T* __restrict__ x, int64_t e, float
 template <typename T>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t n8,
                                                         unsigned* amax_bits, int* status) {
+  pdl_wait();  // inputs may come from the previous kernel
+  pdl_trigger();
   float m = 0.f;
   bool bad = false;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -184,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     nvfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4,
                  const unsigned* __restrict__ amax_bits, float* tensor_scale, KernelCtl ctl) {
+  pdl_wait();  // inputs may come from the previous kernel
+  pdl_trigger();
   // x and codes start at row um.row0; scales are indexed by the global row
   constexpr uint32_t kTileBytes = kQUnits * 16 * sizeof(T);
   extern __shared__ __align__(128) uint8_t qring[];  // [kQStages][kTileBytes]
@@ -312,6 +316,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
     mxfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4) {
+  pdl_wait();  // inputs may come from the previous kernel
+  pdl_trigger();
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < um.units;
   float v[16];
@@ -353,6 +359,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
     int4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                 uint16_t* __restrict__ scales) {
+  pdl_wait();  // inputs may come from the previous kernel
+  pdl_trigger();
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < um.units;
   float v[16];
@@ -391,6 +399,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     scales_to_mma_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t nsf, int64_t nsf4,
                          uint8_t* __restrict__ dst, int64_t total) {
+  pdl_wait();  // inputs may come from the previous kernel
+  pdl_trigger();
   const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (d >= total) return;
   const int64_t tile = d >> 9, o = d & 511;
@@ -410,16 +420,15 @@ q4_status launch_amax(const void* x, int dtype, int64_t n, unsigned* amax_bits,
   const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n8, kThreads), (int64_t)num_sms() * 4);
   int* st = device_status_ptr();
   switch (dtype) {
-    case Q4_F32: amax_kernel<float><<<grid, kThreads, 0, stream>>>((const float*)x, n8, amax_bits, st); break;
-    case Q4_BF16: amax_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>((const __nv_bfloat16*)x, n8, amax_bits, st); break;
-    case Q4_F16: amax_kernel<__half><<<grid, kThreads, 0, stream>>>((const __half*)x, n8, amax_bits, st); break;
+    case Q4_F32: return launch_pdl(amax_kernel<float>, grid, kThreads, 0, stream, (const float*)x, n8, amax_bits, st);
+    case Q4_BF16: return launch_pdl(amax_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, (const __nv_bfloat16*)x, n8, amax_bits, st);
+    case Q4_F16: return launch_pdl(amax_kernel<__half>, grid, kThreads, 0, stream, (const __half*)x, n8, amax_bits, st);
     default: return Q4_ERR_INVALID_ARG;
   }
-  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
-// Launches `launch(um, grid, row0)` over chunks of whole rows (multiples of 128)
-// holding fewer than 2^32 units each.
+// Launches `launch(um, grid, row0)` (returning a q4_status) over chunks of
+// whole rows (multiples of 128) holding fewer than 2^32 units each.
 template <typename F>
 q4_status for_row_chunks(int64_t rows, int64_t nblk, F&& launch) {
   const int64_t cap = ((int64_t)0xFFFFFE00 / nblk) / 128 * 128;
@@ -427,8 +436,7 @@ q4_status for_row_chunks(int64_t rows, int64_t nblk, F&& launch) {
   for (int64_t r0 = 0; r0 < rows; r0 += cap) {
     const int64_t nr = std::min(cap, rows - r0);
     const UnitMap um = make_unit_map((uint32_t)(nr * nblk), (uint32_t)nblk, r0);
-    launch(um, (unsigned)ceil_div(nr * nblk, kThreads), r0);
-    if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+    if (launch(um, (unsigned)ceil_div(nr * nblk, kThreads), r0) != Q4_OK) return Q4_ERR_CUDA;
   }
   return Q4_OK;
 }
@@ -463,11 +471,11 @@ q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, 
     uint8_t* c = codes + r0 * (K / 2);
     const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(um.units, kQUnits), max_ctas);
     if (dtype == Q4_F32)
-      nvfp4_kernel<float><<<grid, kThreads, ring, stream>>>(rows_from<float>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+      return launch_pdl(nvfp4_kernel<float>, grid, kThreads, ring, stream, rows_from<float>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
     else if (dtype == Q4_BF16)
-      nvfp4_kernel<__nv_bfloat16><<<grid, kThreads, ring, stream>>>(rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+      return launch_pdl(nvfp4_kernel<__nv_bfloat16>, grid, kThreads, ring, stream, rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
     else
-      nvfp4_kernel<__half><<<grid, kThreads, ring, stream>>>(rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+      return launch_pdl(nvfp4_kernel<__half>, grid, kThreads, ring, stream, rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
   });
 }
 
@@ -482,11 +490,11 @@ q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, 
   return for_row_chunks(rows, nblk, [&](const UnitMap& um, unsigned grid, int64_t r0) {
     uint8_t* c = codes + r0 * (K / 2);
     if (dtype == Q4_F32)
-      mxfp4_kernel<float><<<grid, kThreads, 0, stream>>>(rows_from<float>(x, r0, K), um, c, scales, layout, nsf4);
+      return launch_pdl(mxfp4_kernel<float>, grid, kThreads, 0, stream, rows_from<float>(x, r0, K), um, c, scales, layout, nsf4);
     else if (dtype == Q4_BF16)
-      mxfp4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4);
+      return launch_pdl(mxfp4_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4);
     else
-      mxfp4_kernel<__half><<<grid, kThreads, 0, stream>>>(rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4);
+      return launch_pdl(mxfp4_kernel<__half>, grid, kThreads, 0, stream, rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4);
   });
 }
 
@@ -499,11 +507,11 @@ q4_status launch_quant_int4(const void* x, int dtype, int64_t rows, int64_t K, u
     uint8_t* c = codes + r0 * (K / 2);
     uint16_t* sc = scales + r0 * (K / 128);
     if (dtype == Q4_F32)
-      int4_kernel<float><<<grid, kThreads, 0, stream>>>(rows_from<float>(x, r0, K), um, c, sc);
+      return launch_pdl(int4_kernel<float>, grid, kThreads, 0, stream, rows_from<float>(x, r0, K), um, c, sc);
     else if (dtype == Q4_BF16)
-      int4_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(rows_from<__nv_bfloat16>(x, r0, K), um, c, sc);
+      return launch_pdl(int4_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, rows_from<__nv_bfloat16>(x, r0, K), um, c, sc);
     else
-      int4_kernel<__half><<<grid, kThreads, 0, stream>>>(rows_from<__half>(x, r0, K), um, c, sc);
+      return launch_pdl(int4_kernel<__half>, grid, kThreads, 0, stream, rows_from<__half>(x, r0, K), um, c, sc);
   });
 }
 
@@ -511,9 +519,8 @@ q4_status launch_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, ui
                                cudaStream_t stream) {
   const int64_t total = (int64_t)mma_scales_bytes(rows, nsf);
   if (total == 0) return Q4_OK;
-  scales_to_mma_kernel<<<blocks_for(total), kThreads, 0, stream>>>(src, rows, nsf, ceil_div(nsf, 4),
-                                                                   dst, total);
-  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return launch_pdl(scales_to_mma_kernel, blocks_for(total), kThreads, 0, stream, src, rows, nsf,
+                    ceil_div(nsf, 4), dst, total);
 }
 
 }  // namespace q4

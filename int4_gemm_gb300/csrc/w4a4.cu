@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
   using C_ = Cfg<NV, P2>;
   constexpr int kStages = C_::kStages;
   extern __shared__ uint8_t smem_raw[];
+  pdl_wait();  // operands, scales and the schedule may come from the previous kernel
+  pdl_trigger();
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -604,6 +606,8 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
 // sched[e] = first tile-row of expert e (prefix of ceil(M_e / 128)).
 __global__ void grouped_sched_kernel(const int32_t* __restrict__ offsets, int E,
                                      int32_t* __restrict__ sched) {
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0 && blockIdx.x == 0) {
     int acc = 0;
     sched[0] = 0;
@@ -623,6 +627,8 @@ __global__ void __launch_bounds__(128)
                       const int32_t* __restrict__ sched, int E,
                       const uint8_t* __restrict__ tok_sf, int64_t nsf,
                       uint8_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int tr = blockIdx.x;
   if (tr >= __ldg(sched + E)) return;
   int e = 0;
@@ -669,13 +675,17 @@ q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Param
   cfg.blockDim = dim3(block_threads<false>(), 1, 1);
   cfg.dynamicSmemBytes = Cfg<NV, P2>::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel waits (griddepcontrol.wait)
+  // before touching memory the previous kernel may have written
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // persistent clusters: exactly as many as can be resident at once, so no
   // cluster waits for a second wave with its whole share of tiles
   static int max_active[64][2] = {{0}};
@@ -708,13 +718,17 @@ q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Para
   cfg.blockDim = dim3(block_threads<false>(), 1, 1);
   cfg.dynamicSmemBytes = Cfg<NV>::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = KS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel waits (griddepcontrol.wait)
+  // before touching memory the previous kernel may have written
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, KS>, ta, tb, p));
   return Q4_OK;
 }
@@ -774,15 +788,13 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
 q4_status launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int E,
                               const uint8_t* tok_scales_rowmajor, int64_t nsf, int32_t* sched,
                               uint8_t* a_sf_routed, int64_t sf_rows_cap, cudaStream_t stream) {
-  grouped_sched_kernel<<<1, 32, 0, stream>>>(offsets, E, sched);
-  if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
+  q4_status st = launch_pdl(grouped_sched_kernel, 1, 32, 0, stream, offsets, E, sched);
+  if (st != Q4_OK) return st;
   const int64_t cap_blocks = sf_rows_cap / BM;
-  if (cap_blocks > 0) {
-    grouped_sf_kernel<<<(unsigned)cap_blocks, 128, 0, stream>>>(offsets, row_token, sched, E,
-                                                                 tok_scales_rowmajor, nsf, a_sf_routed);
-    if (cudaGetLastError() != cudaSuccess) return Q4_ERR_CUDA;
-  }
-  return Q4_OK;
+  if (cap_blocks > 0)
+    st = launch_pdl(grouped_sf_kernel, (unsigned)cap_blocks, 128, 0, stream, offsets, row_token, sched,
+                    E, tok_scales_rowmajor, nsf, a_sf_routed);
+  return st;
 }
 
 q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
@@ -804,9 +816,8 @@ q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
   if ((st = set_smem_attr<true, true>()) != Q4_OK) return st;
-  fp4_gemm_kernel<true, true><<<(unsigned)num_sms(), block_threads<true>(), Cfg<true>::kSmemBytes,
-                                stream>>>(tb, tb, p);
-  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+  return launch_pdl(fp4_gemm_kernel<true, true>, (unsigned)num_sms(), block_threads<true>(),
+                    Cfg<true>::kSmemBytes, stream, tb, tb, p);
 }
 
 }  // namespace q4
