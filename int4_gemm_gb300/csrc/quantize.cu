@@ -360,7 +360,8 @@ __global__ void __launch_bounds__(kThreads)
     int4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                 uint16_t* __restrict__ scales) {
   pdl_wait();  // inputs may come from the previous kernel
-  pdl_trigger();
+  // No early release of the next kernel: the W4A16 GEMM reads its weights
+  // and scales before it waits for its predecessor, and these are they.
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < um.units;
   float v[16];

@@ -4,10 +4,15 @@
 // weight reads in decode).
 //
 // Design (GB300):
-//  * The packed INT4 weights are the only large stream.  Each thread loads its
-//    own 16-byte pieces straight from HBM into registers (non-allocating in
-//    L1), two groups ahead of use, in exactly the register shape the bf16
-//    tensor-core fragment needs -- no shared-memory staging of weights.
+//  * The packed INT4 weights are the only large stream.  Each thread copies
+//    its own 16-byte pieces with cp.async into a private slot ring in shared
+//    memory (4 groups of 128 in flight) and reads them back in exactly the
+//    register shape of the bf16 tensor-core fragment.
+//  * Programmatic dependent launch: the first 4 groups of weights are
+//    requested before the kernel waits for the previous kernel in the stream
+//    (activations and the output come after the wait).  The weights must
+//    therefore not be written by a kernel that releases its successor early;
+//    this library's INT4 quantizer does not.
 //  * Nibbles become exact bf16 integers with one LOP3 (mask, flip the sign
 //    bit, OR the exponent of 128) and one bf16x2 subtraction of 136.
 //  * The products q * a are exact in the MMA and are summed in FP32; the FP16
@@ -141,9 +146,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
 #pragma unroll
   for (int gi = 0; gi < kRing; ++gi) issue(gi);
-  // Weights and scales are never written by an earlier kernel, so their loads
-  // go out before waiting on the previous grid in the stream (programmatic
-  // dependent launch); activations and the output wait for it.
+  // Weight loads go out before the wait on the previous kernel in the stream
+  // (see the note at the top); activations and the output wait for it.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   float acc[2][TS][4];  // [tile][token set][fragment]

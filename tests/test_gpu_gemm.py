@@ -154,6 +154,30 @@ def test_w4a16_int4(lib, shape):
     assert lib.sync_status() == 0
 
 
+def test_w4a16_right_after_quantizing_its_weights(lib):
+    """Weights quantized into poisoned buffers and read by the very next launch
+    on the same stream, with no host synchronization in between: the GEMM
+    starts early (programmatic dependent launch) but must see the new codes."""
+    N, K, M = 1024, 2048, 4
+    A = torch.randn(M, K, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
+    w = (torch.randn(N, K, generator=torch.Generator().manual_seed(5)) * 0.02).cuda()
+    wq0, ws0 = lib.quantize_int4_g128(w)
+    want = lib.gemm_w4a16_int4(A, wq0, ws0)
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(8):
+        wq = torch.full((N, K // 2), 0x77, dtype=torch.uint8, device="cuda")
+        ws = torch.full((N, K // 128), 0x7BFF, dtype=torch.int16, device="cuda")
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        assert lib.lib().quantize_int4_g128(w.data_ptr(), q4.F32, N, K, wq.data_ptr(),
+                                            ws.data_ptr(), stream) == 0
+        assert lib.lib().gemm_w4a16_int4(A.data_ptr(), wq.data_ptr(), ws.data_ptr(), M, N, K,
+                                         C.data_ptr(), None, 0, stream) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(C, want)
+    assert lib.sync_status() == 0
+
+
 def test_w4a16_repeatable(lib):
     A, W = workloads.decode(16, seed=9, N=1024, K=4096)
     wq, ws = lib.quantize_int4_g128(torch.from_numpy(W).cuda())
