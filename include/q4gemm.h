@@ -201,7 +201,9 @@ q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t*
  * W_codes: [E, N, K/2]; W_scales: E consecutive Q4_SCALES_MMA tensors of
  * q4_mma_scales_bytes(N, K/16) bytes; W_tensor_scales: device float [E].
  * C_bf16: [R, N].  K % 256 == 0.  An expert with no rows is legal.
- * ws: q4_workspace_size_moe(T, N, K, E, R) bytes.
+ * ws: q4_workspace_size_moe(T, N, K, E, R) bytes; it holds the quantized
+ * tokens, their codes copied in routed order (R * K/2 bytes), the routed
+ * scales and the expert schedule.
  */
 q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            const int32_t* expert_offsets, const int32_t* row_token, int64_t R,

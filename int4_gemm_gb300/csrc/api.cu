@@ -189,6 +189,7 @@ struct MoePlan {
   int32_t* sched;
   uint8_t* routed_sf;
   int64_t cap_rows;
+  uint8_t* routed_codes;  // [R, K/2]: the routed rows' codes, in routed order
 };
 
 MoePlan plan_moe(Carver& c, int64_t T, int64_t K, int E, int64_t R) {
@@ -201,6 +202,7 @@ MoePlan plan_moe(Carver& c, int64_t T, int64_t K, int E, int64_t R) {
   pl.sched = reinterpret_cast<int32_t*>(c.take((size_t)(E + 1) * 4));
   pl.cap_rows = (ceil_div(R, 128) + E) * 128;
   pl.routed_sf = c.take(mma_scales_bytes(pl.cap_rows, K / 16));
+  pl.routed_codes = c.take((size_t)R * (size_t)(K / 2));
   return pl;
 }
 
@@ -377,9 +379,11 @@ q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
   if ((st = launch_grouped_prep(expert_offsets, row_token, E, pl.tok_sf, K / 16, pl.sched,
                                 pl.routed_sf, pl.cap_rows, s)) != Q4_OK)
     return st;
+  if ((st = launch_gather_rows(pl.tok_codes, row_token, R, K / 2, pl.routed_codes, s)) != Q4_OK)
+    return st;
   GroupedArgs g = {};
-  g.a_codes = pl.tok_codes; g.a_sf_rows = pl.routed_sf; g.a_g = pl.g;
-  g.offsets = expert_offsets; g.row_token = row_token; g.sched = pl.sched;
+  g.a_routed = pl.routed_codes; g.a_sf_rows = pl.routed_sf; g.a_g = pl.g;
+  g.offsets = expert_offsets; g.sched = pl.sched;
   g.T = T; g.R = R; g.N = N; g.K = K; g.E = E;
   g.w_codes = W_codes; g.w_scales = W_scales; g.w_g = W_tensor_scales; g.C = C_bf16;
   return launch_grouped_gemm(g, s);

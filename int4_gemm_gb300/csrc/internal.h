@@ -55,11 +55,10 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream);
 
 // Grouped (routed MoE) NVFP4 GEMM on a pre-quantized token tensor.
 struct GroupedArgs {
-  const uint8_t* a_codes;    // [T, K/2] quantized tokens
+  const uint8_t* a_routed;   // [R, K/2] quantized codes of the routed rows (copied in routed order)
   const uint8_t* a_sf_rows;  // routed scales, MMA layout, per-expert 128-row padded blocks
   const float* a_g;
   const int32_t* offsets;    // [E+1]
-  const int32_t* row_token;  // [R]
   const int32_t* sched;      // [E+1] tile-row prefix (device, built by the prep kernel)
   int64_t T, R, N, K;
   int E;
@@ -71,6 +70,8 @@ struct GroupedArgs {
 q4_status launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int E,
                               const uint8_t* tok_scales_rowmajor, int64_t nsf, int32_t* sched,
                               uint8_t* a_sf_routed, int64_t sf_rows_cap, cudaStream_t stream);
+q4_status launch_gather_rows(const uint8_t* codes, const int32_t* row_token, int64_t R,
+                             int64_t row_bytes, uint8_t* out, cudaStream_t stream);
 q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream);
 
 q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int64_t M, int64_t N,

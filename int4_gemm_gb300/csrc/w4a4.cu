@@ -14,9 +14,6 @@
 //              128x256x64 per instruction, FP32 accumulation in TMEM.
 //   warps 2-5  epilogue: tcgen05.ld of the 128x256 FP32 accumulator, times
 //              gA * gB (NVFP4), rounded to bf16 (or kept FP32), stored.
-//   warps 10-17 (grouped variant only) gather the routed A rows, two threads
-//              per row: plain loads up to four K blocks ahead, swizzled
-//              shared stores, proxy fence, one mbarrier arrival per warp.
 //   warps 6-9  scale writers: each stage's scale tiles go from shared memory
 //              to TMEM through registers (tcgen05.st, one warp per TMEM lane
 //              quarter).  Unlike tcgen05.cp these stores do not queue behind
@@ -43,11 +40,9 @@ constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of co
 constexpr int kMaxStages = 5;
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
 constexpr int kWriterThreads = 128;    // 4 scale-writer warps
-constexpr int kGatherThreads = 256;    // grouped variant: 8 more warps gather A rows (2 threads per row)
 constexpr int kWriterWarp0 = (kThreads + kWriterThreads) / 32 - 4;  // warps 6-9
-constexpr int kGatherWarp0 = (kThreads + kWriterThreads) / 32;      // warps 10-17 (grouped)
 template <bool GROUPED>
-constexpr int block_threads() { return kThreads + kWriterThreads + (GROUPED ? kGatherThreads : 0); }
+constexpr int block_threads() { return kThreads + kWriterThreads; }
 constexpr uint32_t kABytes = BM * BK / 2;     // 16 KiB
 constexpr uint32_t kBBytes = BN * BK / 2;     // 32 KiB
 constexpr uint32_t kTmemCols = 512;
@@ -118,9 +113,7 @@ struct Params {
   int num_m, num_n;       // dense tile counts
   // grouped
   const int32_t* offsets;
-  const int32_t* row_token;
   const int32_t* sched;
-  const uint8_t* a_codes;  // grouped: quantized tokens [T, K/2]
   int E;
   KernelCtl ctl;
 };
@@ -208,7 +201,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm->full[s]), GROUPED ? 1 + kGatherThreads / 32 : 1);  // producer (+ gather warps)
+      mbar_init(smem_u32(&sm->full[s]), 1);
       mbar_init(smem_u32(&sm->empty[s]), 1);
       mbar_init(smem_u32(&sm->sf_full[s]), P2 ? 8 : 4);  // one arrival per scale-writer warp
     }
@@ -263,7 +256,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const uint8_t* sfb = p.b_sf + (int64_t)ti.e * p.b_sf_expert_bytes;
       const int nb0 = ti.n0 / 128;
       const bool b_hi = nb0 + 1 < nblk_b;
-      const uint32_t bytes = (GROUPED ? 0u : kABytes) + C_::kBLoad + (a_sf_ok ? C_::kSfaBytes : 0u) +
+      const uint32_t bytes = kABytes + C_::kBLoad + (a_sf_ok ? C_::kSfaBytes : 0u) +
                              C_::kSfaBytes * (b_hi ? 2 : 1);
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
@@ -275,7 +268,8 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         const uint32_t full = smem_u32(&sm->full[stage]);
         if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
-          if constexpr (!GROUPED) tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
+          // A rows: the tile's rows (grouped: rows of the routed copy of the codes)
+          tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
           const int64_t jsf = (int64_t)kb * C_::kSfChunks * 512;
           if (a_sf_ok) bulk_load(smem_u32(st + C_::kSfaOff), sfa + jsf, C_::kSfaBytes, full);
           const uint8_t* sfb0 = sfb + (int64_t)nb0 * nsf4_a * 512 + jsf;
@@ -391,77 +385,6 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         __syncwarp();
         if (lane == 0) arrive_leader(&sm->sf_full[stage]);
         if (++stage == kStages) stage = 0, phase ^= 1;
-      }
-    }
-  } else if (GROUPED && warp >= kGatherWarp0) {
-    // ------------------------------------------------------------ A-row gather (grouped)
-    // Threads 2r, 2r + 1 copy routed row r of the tile (its token's 128 code
-    // bytes of this K block, 64 each) into the 128-byte-swizzled A tile, then
-    // make the writes
-    // visible to the tensor core's async proxy before arriving.  Loads run
-    // kStages jobs ahead of the stores (a register ring, one entry per slot),
-    // so the L2 latency of the routed rows overlaps the pipeline.
-    const int i = threadIdx.x - kGatherWarp0 * 32;
-    const int row = i >> 1, half = i & 1;
-    uint32_t stage = 0, phase = 0;
-    // this thread's 64 source bytes of routed row `row` in tile t (the tile's
-    // first row for rows past its end)
-    auto row_src = [&](int t) -> const uint8_t* {
-      const TileInfo ti = tile_at(t);
-      const int r = ti.m_row0 + row;
-      const int tokr = __ldg(p.row_token + (r < ti.m_end ? r : ti.m_row0));
-      return p.a_codes + (int64_t)tokr * (p.K / 2) + half * 64;
-    };
-    auto next_tile = [&](int t) {
-      while (t < total_tiles && !tile_at(t).ok) t += ncl;
-      return t;
-    };
-    auto load_blk = [&](const uint8_t* src, int kb, uint4 (&v)[4]) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) v[c] = __ldg(reinterpret_cast<const uint4*>(src + kb * (BK / 2)) + c);
-    };
-    // jobs (tile, K block) in order; buf[j] holds the rows of the job that
-    // will fill the j-th slot of the next round of kStages slots
-    int jt = next_tile(cid), jkb = kb_begin;  // the last job handed out
-    const uint8_t* jsrc = jt < total_tiles ? row_src(jt) : nullptr;
-    bool first = true;
-    auto next_job = [&]() {  // advance (jt, jkb, jsrc); false when no job is left
-      if (first) {
-        first = false;
-      } else if (++jkb == kb_end) {
-        jkb = kb_begin;
-        jt = next_tile(jt + ncl);
-        if (jt < total_tiles) jsrc = row_src(jt);
-      }
-      return jt < total_tiles && jkb < kb_end;
-    };
-    uint4 buf[kStages][4];
-    bool valid[kStages];
-#pragma unroll
-    for (int j = 0; j < kStages; ++j) {
-      valid[j] = next_job();
-      if (valid[j]) load_blk(jsrc, jkb, buf[j]);
-    }
-    bool go = true;
-    while (go) {
-#pragma unroll
-      for (int j = 0; j < kStages; ++j) {
-        if (!go || !valid[j]) { go = false; continue; }
-        // warp-uniform outcome: the lanes meet at __syncwarp below
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag))) {
-          go = false;
-          continue;
-        }
-        uint8_t* dst = smem + stage * C_::kStageBytes + row * (BK / 2);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(dst + (((4 * half + c) ^ (row & 7)) << 4)) = buf[j][c];
-        fence_proxy_async_smem();  // each thread's stores, then one arrival per warp
-        __syncwarp();
-        if ((i & 31) == 0) mbar_arrive(smem_u32(&sm->full[stage]));
-        if (++stage == kStages) stage = 0, phase ^= 1;
-        valid[j] = next_job();  // refill with the job kStages ahead
-        if (valid[j]) load_blk(jsrc, jkb, buf[j]);
       }
     }
   } else {
@@ -649,6 +572,23 @@ __global__ void __launch_bounds__(128)
 
 namespace {
 
+// Routed copy of the token codes: out[r] = codes[row_token[r]], r < R, so that
+// each expert's routed rows are consecutive and reach the GEMM by TMA.
+// 16-byte vectors, grid-stride; row_bytes is a multiple of 16.
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint8_t* __restrict__ codes, const int32_t* __restrict__ row_token,
+                       int64_t R, int64_t row_bytes, uint8_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t vpr = row_bytes / 16, total = R * vpr;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = v / vpr, c = v - r * vpr;
+    const int64_t tok = __ldg(row_token + r);
+    reinterpret_cast<uint4*>(out)[v] = __ldg(reinterpret_cast<const uint4*>(codes + tok * row_bytes) + c);
+  }
+}
+
 template <bool NV, bool GROUPED, int KS = 1, bool P2 = false>
 q4_status set_smem_attr() {
   static int done[64] = {0};
@@ -797,13 +737,24 @@ q4_status launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, 
   return st;
 }
 
+q4_status launch_gather_rows(const uint8_t* codes, const int32_t* row_token, int64_t R,
+                             int64_t row_bytes, uint8_t* out, cudaStream_t stream) {
+  if (R == 0) return Q4_OK;
+  const int64_t total = R * (row_bytes / 16);
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(total, 256), (int64_t)num_sms() * 8);
+  return launch_pdl(gather_rows_kernel, grid, 256, 0, stream, codes, row_token, R, row_bytes, out);
+}
+
 q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
   if (a.R == 0 || a.N == 0 || a.E == 0) return Q4_OK;
   if (a.E > kMaxExperts) return Q4_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap tb;
   q4_status st;
-  // B: the E stacked expert weights as one tensor; A rows are gathered by threads
+  // B: the E stacked expert weights as one tensor; A: the routed copy of the
+  // token codes, so a tile's rows are consecutive
+  CUtensorMap ta;
   if ((st = make_tmap_2d_u8(&tb, a.w_codes, a.K / 2, (uint64_t)a.E * a.N, a.K / 2, BK / 2, BN, true)) != Q4_OK) return st;
+  if ((st = make_tmap_2d_u8(&ta, a.a_routed, a.K / 2, (uint64_t)a.R, a.K / 2, BK / 2, BM, true)) != Q4_OK) return st;
   Params p = {};
   p.M = a.R; p.N = a.N; p.K = a.K;
   p.a_sf = a.a_sf_rows; p.b_sf = a.w_scales;
@@ -811,13 +762,12 @@ q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
   p.a_g = a.a_g; p.b_g = a.w_g;
   p.C = a.C; p.c_dtype = Q4_BF16;
   p.num_m = 0; p.num_n = (int)ceil_div(a.N, BN);
-  p.offsets = a.offsets; p.row_token = a.row_token; p.sched = a.sched; p.E = a.E;
-  p.a_codes = a.a_codes;
+  p.offsets = a.offsets; p.sched = a.sched; p.E = a.E;
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
   if ((st = set_smem_attr<true, true>()) != Q4_OK) return st;
   return launch_pdl(fp4_gemm_kernel<true, true>, (unsigned)num_sms(), block_threads<true>(),
-                    Cfg<true>::kSmemBytes, stream, tb, tb, p);
+                    Cfg<true>::kSmemBytes, stream, ta, tb, p);
 }
 
 }  // namespace q4
