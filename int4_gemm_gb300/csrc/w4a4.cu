@@ -483,39 +483,63 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
   if constexpr (KS > 1) {
     // rank q reduces rows [q * 128 / KS, (q + 1) * 128 / KS) of the tile over all
     // ranks' partials, in rank order, then applies gA * gB and stores
+    float alpha = 1.f;
+    if constexpr (NV) alpha = __ldg(p.a_g) * __ldg(p.b_g);  // loaded before the barrier
     cluster_barrier_sync();
     const int t = cid;  // one tile per cluster
     if (t < total_tiles && !*abort_flag) {
       const TileInfo ti = tile_at(t);
-      float alpha = 1.f;
-      if constexpr (NV) alpha = __ldg(p.a_g) * __ldg(p.b_g);
       const int rows = (BM + KS - 1) / KS;
       const int r_lo = krank * rows, r_hi = min(BM, r_lo + rows);
       const uint32_t base = smem_u32(smem);
-      for (int e = threadIdx.x; e < (r_hi - r_lo) * (BN / 4); e += blockDim.x) {
-        const int r = r_lo + e / (BN / 4), c4 = e % (BN / 4);
-        const uint32_t off = (uint32_t)(r * kPartStride + 4 * c4) * 4u;
-        float4 v[KS];
+      const int items = (r_hi - r_lo) * (BN / 4);
+      // kBatch items per thread per round: all their remote loads are in flight
+      // together, so a round costs one distributed-shared-memory round trip
+      constexpr int kBatch = 4;
+      for (int e0 = threadIdx.x; e0 < items; e0 += kBatch * blockDim.x) {
+        float4 v[kBatch][KS];
 #pragma unroll
-        for (int qq = 0; qq < KS; ++qq) v[qq] = ld_dsmem_v4(base + off, (uint32_t)qq);
-        float4 sum = v[0];
+        for (int b = 0; b < kBatch; ++b) {
+          const int e = e0 + b * blockDim.x;
+          const int r = r_lo + (e < items ? e : 0) / (BN / 4), c4 = (e < items ? e : 0) % (BN / 4);
+          const uint32_t off = (uint32_t)(r * kPartStride + 4 * c4) * 4u;
 #pragma unroll
-        for (int qq = 1; qq < KS; ++qq) {
-          sum.x += v[qq].x; sum.y += v[qq].y; sum.z += v[qq].z; sum.w += v[qq].w;
+          for (int qq = 0; qq < KS; ++qq)  // this CTA's own partial by a plain shared load
+            v[b][qq] = qq == krank ? *reinterpret_cast<const float4*>(smem + off)
+                                   : ld_dsmem_v4(base + off, (uint32_t)qq);
         }
-        const int row = ti.m_row0 + r, col = ti.n0 + 4 * c4;
-        if (row >= ti.m_end || col >= p.N) continue;
-        const float o[4] = {sum.x * alpha, sum.y * alpha, sum.z * alpha, sum.w * alpha};
-        if (p.c_dtype == Q4_BF16) {
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.N + col;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (col + i < p.N) out[i] = __float2bfloat16_rn(o[i]);
-        } else {
-          float* out = reinterpret_cast<float*>(p.C) + (int64_t)row * p.N + col;
+        for (int b = 0; b < kBatch; ++b) {
+          const int e = e0 + b * blockDim.x;
+          if (e >= items) break;
+          const int r = r_lo + e / (BN / 4), c4 = e % (BN / 4);
+          float4 sum = v[b][0];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (col + i < p.N) out[i] = o[i];
+          for (int qq = 1; qq < KS; ++qq) {
+            sum.x += v[b][qq].x; sum.y += v[b][qq].y; sum.z += v[b][qq].z; sum.w += v[b][qq].w;
+          }
+          const int row = ti.m_row0 + r, col = ti.n0 + 4 * c4;
+          if (row >= ti.m_end || col >= p.N) continue;
+          const float o[4] = {sum.x * alpha, sum.y * alpha, sum.z * alpha, sum.w * alpha};
+          if (p.c_dtype == Q4_BF16) {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.N + col;
+            if (col + 4 <= p.N && (p.N % 4) == 0) {  // 8-byte aligned: one store
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]), hi = __floats2bfloat162_rn(o[2], o[3]);
+              uint2 w;
+              w.x = *reinterpret_cast<const uint32_t*>(&lo);
+              w.y = *reinterpret_cast<const uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(out) = w;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (col + i < p.N) out[i] = __float2bfloat16_rn(o[i]);
+            }
+          } else {
+            float* out = reinterpret_cast<float*>(p.C) + (int64_t)row * p.N + col;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (col + i < p.N) out[i] = o[i];
+          }
         }
       }
     }
