@@ -409,8 +409,8 @@ class Grouped:
     default_steps = 200
     kernel = "grouped step (quantize tokens + routed scales + grouped GEMM)"
     T, E, N, K, top = 4096, 64, 2048, 7168, 8
-    launches_per_step = 5  # amax, quantize, schedule, routed scales, grouped GEMM
-    kernel_launches = 5
+    launches_per_step = 6  # amax, quantize, schedule, routed scales, routed copy, grouped GEMM
+    kernel_launches = 6
 
     def config(self):
         return {"workload": "grouped_moe 64 experts NVFP4 2048x7168, 4096 bf16 tokens, top-8 routing",

@@ -183,7 +183,7 @@ q4_status gemm_w4a4_mxfp4(const q4_operand* A, const q4_operand* B, int64_t M, i
  * before the previous kernel in the stream has finished (A and C wait for
  * it).  Wq and Ws must not be written by a preceding kernel that releases its
  * successor early (griddepcontrol.launch_dependents); kernels that do not do
- * this, copies, and this library's quantize_int4_g128 are safe.
+ * this, copies, and this library's quantizers are safe.
  */
 q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t* Ws, int64_t M,
                           int64_t N, int64_t K, void* C_bf16, void* ws, size_t ws_bytes,

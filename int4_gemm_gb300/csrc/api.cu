@@ -45,7 +45,6 @@ struct Carver {
 };
 
 bool valid_dtype(int d) { return d == Q4_F32 || d == Q4_BF16 || d == Q4_F16; }
-size_t dtype_size(int d) { return d == Q4_F32 ? 4 : 2; }
 }  // namespace
 
 int* device_status_ptr() {

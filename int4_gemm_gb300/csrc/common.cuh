@@ -34,11 +34,14 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 
 // Programmatic dependent launch: wait until the previous kernel in the stream
 // has completed and its writes are visible (a no-op without a programmatic
-// dependency); let the next kernel start launching.
+// dependency).  The quantizers and the W4A4 kernels issue no
+// griddepcontrol.launch_dependents: the next kernel is released only as their
+// blocks exit.  Releasing it at kernel entry let its blocks occupy SM slots
+// while this kernel still ran and made the short MXFP4 step (quantize +
+// split-K GEMM) about 1 us slower, with no gain on the longer steps.  The
+// W4A16 GEMM does release its successor early, so that the next decode GEMM
+// streams its weights under this one's tail.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers

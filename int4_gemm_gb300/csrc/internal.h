@@ -84,10 +84,10 @@ q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_byt
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Launch with programmatic dependent launch allowed: the kernel may start while
-// the previous kernel in the stream finishes; it calls pdl_wait() (common.cuh)
-// before its first global-memory access, so it sees all of that kernel's
-// writes.
+// Launch with programmatic dependent launch allowed: the kernel may start once
+// the previous kernel's blocks have exited, before that grid has completed;
+// it calls pdl_wait() (common.cuh) before its first global-memory access, so
+// it sees all of that kernel's writes.
 template <typename... KArgs, typename... Args>
 q4_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                      cudaStream_t stream, Args... args) {

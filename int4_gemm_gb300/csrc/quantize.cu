@@ -97,7 +97,6 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t n8,
                                                         unsigned* amax_bits, int* status) {
   pdl_wait();  // inputs may come from the previous kernel
-  pdl_trigger();
   float m = 0.f;
   bool bad = false;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -187,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 4)
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4,
                  const unsigned* __restrict__ amax_bits, float* tensor_scale, KernelCtl ctl) {
   pdl_wait();  // inputs may come from the previous kernel
-  pdl_trigger();
   // x and codes start at row um.row0; scales are indexed by the global row
   constexpr uint32_t kTileBytes = kQUnits * 16 * sizeof(T);
   extern __shared__ __align__(128) uint8_t qring[];  // [kQStages][kTileBytes]
@@ -317,7 +315,6 @@ __global__ void __launch_bounds__(kThreads)
     mxfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4) {
   pdl_wait();  // inputs may come from the previous kernel
-  pdl_trigger();
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < um.units;
   float v[16];
@@ -360,8 +357,6 @@ __global__ void __launch_bounds__(kThreads)
     int4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                 uint16_t* __restrict__ scales) {
   pdl_wait();  // inputs may come from the previous kernel
-  // No early release of the next kernel: the W4A16 GEMM reads its weights
-  // and scales before it waits for its predecessor, and these are they.
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < um.units;
   float v[16];
@@ -401,7 +396,6 @@ __global__ void __launch_bounds__(kThreads)
     scales_to_mma_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t nsf, int64_t nsf4,
                          uint8_t* __restrict__ dst, int64_t total) {
   pdl_wait();  // inputs may come from the previous kernel
-  pdl_trigger();
   const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (d >= total) return;
   const int64_t tile = d >> 9, o = d & 511;

@@ -12,7 +12,8 @@
 //    requested before the kernel waits for the previous kernel in the stream
 //    (activations and the output come after the wait).  The weights must
 //    therefore not be written by a kernel that releases its successor early;
-//    this library's INT4 quantizer does not.
+//    this library's quantizers do not.  This kernel itself releases the next
+//    one as soon as its own weight loads are issued.
 //  * Nibbles become exact bf16 integers with one LOP3 (mask, flip the sign
 //    bit, OR the exponent of 128) and one bf16x2 subtraction of 136.
 //  * The products q * a are exact in the MMA and are summed in FP32; the FP16

@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
   constexpr int kStages = C_::kStages;
   extern __shared__ uint8_t smem_raw[];
   pdl_wait();  // operands, scales and the schedule may come from the previous kernel
-  pdl_trigger();
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -554,7 +553,6 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
 __global__ void grouped_sched_kernel(const int32_t* __restrict__ offsets, int E,
                                      int32_t* __restrict__ sched) {
   pdl_wait();
-  pdl_trigger();
   if (threadIdx.x == 0 && blockIdx.x == 0) {
     int acc = 0;
     sched[0] = 0;
@@ -575,7 +573,6 @@ __global__ void __launch_bounds__(128)
                       const uint8_t* __restrict__ tok_sf, int64_t nsf,
                       uint8_t* __restrict__ out) {
   pdl_wait();
-  pdl_trigger();
   const int tr = blockIdx.x;
   if (tr >= __ldg(sched + E)) return;
   int e = 0;
@@ -603,7 +600,6 @@ __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint8_t* __restrict__ codes, const int32_t* __restrict__ row_token,
                        int64_t R, int64_t row_bytes, uint8_t* __restrict__ out) {
   pdl_wait();
-  pdl_trigger();
   const int64_t vpr = row_bytes / 16, total = R * vpr;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
        v += (int64_t)gridDim.x * blockDim.x) {
