@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   // Weight loads go out before the wait on the previous kernel in the stream
   // (see the note at the top); activations and the output wait for it.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // 16-byte scale loads need 8 groups per row and a 16-byte aligned Ws (the
+  // interface only asks for 2-byte alignment)
+  const bool s16 = (ngroups & 7) == 0 && (reinterpret_cast<uintptr_t>(Ws) & 15) == 0;
 
   float acc[2][TS][4];  // [tile][token set][fragment]
 #pragma unroll
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint16_t* src = Ws + (int64_t)(wok[i] ? wrow[i] : 0) * ngroups + c0;
-      if (gc == kChunk && (ngroups & 7) == 0) {
+      if (gc == kChunk && s16) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
         spk[i][0] = v.x; spk[i][1] = v.y; spk[i][2] = v.z; spk[i][3] = v.w;
       } else {
@@ -292,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   cp_async_wait<0>();  // no copy may still target this CTA's shared memory at exit
+  if (ng == 0) asm volatile("griddepcontrol.wait;" ::: "memory");  // C is written below
 
   // ---- push the partial sums of each owned row slice to its owner rank:
   // recv[src rank][row - owner * per][token] in the owner's shared memory

@@ -306,10 +306,8 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         }
         tc_fence_after();
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
-            alive = false;
-            break;
-          }
+          // sf_full implies full in both CTAs: every scale-writer warp waits
+          // for its own CTA's copies of the stage before it arrives
           if (!mbar_wait(smem_u32(&sm->sf_full[stage]), phase, p.ctl, abort_flag)) {
             alive = false;
             break;
@@ -421,13 +419,9 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const int row = ti.m_row0 + q * 32 + lane;
       const bool row_ok = row < ti.m_end;
       const bool vec_ok = (p.N % 8) == 0;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
-        tmem_ld_wait();
+      auto store_chunk = [&](int c, const uint32_t (&r)[32]) {
         const int col0 = ti.n0 + c * 32;
-        if (!row_ok || col0 >= p.N) continue;
+        if (!row_ok || col0 >= p.N) return;
         const bool full_chunk = col0 + 32 <= p.N;
         if (p.c_dtype == Q4_BF16) {
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.N + col0;
@@ -463,10 +457,25 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
               if (col0 + i < p.N) out[i] = __uint_as_float(r[i]) * alpha;
           }
         }
+      };
+      // Four 32-column TMEM loads per wait; the accumulator goes back to the
+      // MMA as soon as its last columns are in registers, before they are
+      // scaled and stored.
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN / 32; c0 += 4) {
+        uint32_t r[4][32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tmem_ld_32x32b_x32(t_row + (c0 + g) * 32, r[g]);
+        tmem_ld_wait();
+        if (c0 + 4 >= BN / 32) {  // every accumulator column is in registers
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_leader(&sm->acc_empty);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) store_chunk(c0 + g, r[g]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_leader(&sm->acc_empty);
       ++tcount;
     }
   }

@@ -178,6 +178,55 @@ def test_w4a16_right_after_quantizing_its_weights(lib):
     assert lib.sync_status() == 0
 
 
+def test_w4a16_scales_off_16_byte_boundary(lib):
+    """Ws only needs 2-byte alignment: scales that start 2 bytes past a 16-byte
+    boundary give the same result as an aligned copy."""
+    M, N, K = 4, 512, 1024  # 8 groups per row: the aligned path would take 16-byte loads
+    A, W = workloads.decode(M, seed=21, N=N, K=K)
+    A = A.cuda()
+    wq, ws = lib.quantize_int4_g128(torch.from_numpy(W).cuda())
+    want = lib.gemm_w4a16_int4(A, wq, ws)
+    shifted = torch.zeros(N * K // 128 + 8, dtype=torch.int16, device="cuda")
+    shifted[1:1 + N * K // 128].copy_(ws.view(torch.int16).reshape(-1))
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.lib().gemm_w4a16_int4(A.data_ptr(), wq.data_ptr(), shifted.data_ptr() + 2, M, N, K,
+                                     C.data_ptr(), None, 0, stream) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(C, want)
+    assert lib.sync_status() == 0
+
+
+def test_w4a16_chain_of_launches(lib):
+    """Each launch reads the previous launch's output as its activations, with
+    no host synchronization: the next kernel starts early and prefetches its
+    weights, but reads its activations only after its predecessor is done."""
+    N = K = 2048
+    Ws = []
+    for i in range(6):
+        _, W = workloads.decode(1, seed=40 + i, N=N, K=K)
+        Ws.append(lib.quantize_int4_g128(torch.from_numpy(W).cuda()))
+    for M in (1, 4, 16):
+        a0 = (torch.randn(M, K, generator=torch.Generator().manual_seed(M)) * 0.05).to(torch.bfloat16).cuda()
+        want, x = [], a0
+        for wq, ws in Ws:  # one launch at a time
+            x = lib.gemm_w4a16_int4(x, wq, ws)
+            torch.cuda.synchronize()
+            want.append(x)
+        outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in Ws]
+        stream = torch.cuda.current_stream().cuda_stream
+        torch.cuda.synchronize()
+        x = a0
+        for (wq, ws), out in zip(Ws, outs):
+            assert lib.lib().gemm_w4a16_int4(x.data_ptr(), wq.data_ptr(), ws.data_ptr(), M, N, K,
+                                             out.data_ptr(), None, 0, stream) == 0
+            x = out
+        torch.cuda.synchronize()
+        for got, w in zip(outs, want):
+            assert torch.equal(got, w)
+    assert lib.sync_status() == 0
+
+
 def test_w4a16_repeatable(lib):
     A, W = workloads.decode(16, seed=9, N=1024, K=4096)
     wq, ws = lib.quantize_int4_g128(torch.from_numpy(W).cuda())
