@@ -46,9 +46,15 @@ FP4_OVER_BF16 = 6.0
 # ncu-measured DRAM traffic per launch of the dominant kernel (bytes), keyed by
 # workload; None until a capture of the current kernel exists.
 NCU_TRAFFIC = {
-    # ncu dram__bytes_read.sum + dram__bytes_write.sum, mean over the M = 1, 4, 16
-    # launches of the current w4a16_kernel at N = K = 8192
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+    # kernel of the current code, at the bench's own sizes:
+    # w4a16_kernel, mean over the M = 1, 4, 16 launches at N = K = 8192
     "decode": 34.76e6,
+    # fp4_gemm_kernel (CTA pairs) at 8192 x 28672 x 8192, mean of 3 launches
+    # (568 MB read: A and B tiles re-read from DRAM ~3.3x; 433 MB written)
+    "prefill": 1001.2e6,
+    # split-K fp4_gemm_kernel at 256 x 2048 x 7168 (C stays in L2)
+    "moe": 8.81e6,
 }
 
 
