@@ -51,5 +51,6 @@ from .quantize import (  # noqa: F401
     pack_nibbles, unpack_nibbles,
 )
 from .gemm import (  # noqa: F401
-    gemm_fp64, gemm_w4a4_nvfp4, gemm_w4a4_mxfp4, gemm_w4a16_int4, grouped_gemm_moe,
+    gemm_fp64, gemm_w4a4_nvfp4, gemm_w4a4_mxfp4, gemm_w4a16_int4, gemm_w4a16_nvfp4,
+    gemm_w4a16_mxfp4, grouped_gemm_moe,
 )

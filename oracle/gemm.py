@@ -7,7 +7,9 @@ matrix product is numpy's float64 matmul, used as a library step.
 * W4A4 ("Low-bit inference for very large MoE", "Kernels on different
   hardware": activations quantized to FP4 too, both operands enter the FP4
   tensor cores): C = dequant(A) . dequant(B)^T.
-* W4A16 (same section, W4A16 row): C = A_bf16 . dequant(W)^T.
+* W4A16 (same section, W4A16 row, which lists INT4 and FP4 weights with
+  16-bit activations): C = A_bf16 . dequant(W)^T, W in INT4 g128, NVFP4 or
+  MXFP4.
 * Grouped MoE (same section, "MoE's grouped GEMM must support low bits too":
   one low-bit weight matrix per expert, grouped by routing): for every expert
   e, C[rows of e] = A_hat[tokens routed to e] . W_hat_e^T, where the tokens are
@@ -40,6 +42,16 @@ def gemm_w4a4_mxfp4(a_codes, a_scales, b_codes, b_scales) -> np.ndarray:
 def gemm_w4a16_int4(a, w_codes, w_scales) -> np.ndarray:
     """C = a . dequant(W)^T with ``a`` the (bf16-valued) activations."""
     return gemm_fp64(np.asarray(a, np.float64), dequantize_int4_g128(w_codes, w_scales))
+
+
+def gemm_w4a16_nvfp4(a, w_codes, w_scales, w_g) -> np.ndarray:
+    """C = a . dequant(W)^T, W NVFP4 (row-major E4M3 scales, tensor scale w_g)."""
+    return gemm_fp64(np.asarray(a, np.float64), dequantize_nvfp4(w_codes, w_scales, w_g))
+
+
+def gemm_w4a16_mxfp4(a, w_codes, w_scales) -> np.ndarray:
+    """C = a . dequant(W)^T, W MXFP4 (row-major E8M0 scales)."""
+    return gemm_fp64(np.asarray(a, np.float64), dequantize_mxfp4(w_codes, w_scales))
 
 
 def grouped_gemm_moe(tokens, expert_offsets, row_token, experts_q):

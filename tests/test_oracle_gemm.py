@@ -99,6 +99,41 @@ def test_w4a16_group_form_and_brute_force():
     assert np.allclose(C, ref, rtol=1e-12, atol=1e-12)
 
 
+def _mxfp4_value(codes, scales, i, k):
+    c = unpack_nibbles(codes)[i, k]
+    return float(F.e2m1_decode(c)) * float(F.e8m0_decode(scales[i, k // 32]))
+
+
+def test_w4a16_fp4_weights_brute_force():
+    """W4A16 with FP4 weights, element by element from the codes: bf16-valued
+    activations times e2m1(code) * block scale (* tensor scale for NVFP4)."""
+    M, N, K = 3, 5, 64
+    a = workloads.to_bf16(workloads.normal(workloads.rng_for(26, 1), (M, K), 1.0)).float().numpy()
+    w = workloads.normal(workloads.rng_for(26, 2), (N, K), 0.02)
+    w[1, 7] = 1.5  # an outlier: other blocks of row 1 get small scales
+    qn = oracle.quantize_nvfp4(w)
+    qm = oracle.quantize_mxfp4(w)
+    Cn = oracle.gemm_w4a16_nvfp4(a, *qn)
+    Cm = oracle.gemm_w4a16_mxfp4(a, *qm)
+    assert Cn.shape == (M, N) and Cm.shape == (M, N)
+    for i in range(M):
+        for j in range(N):
+            rn = sum(float(a[i, k]) * _nvfp4_value(*qn, j, k) for k in range(K))
+            rm = sum(float(a[i, k]) * _mxfp4_value(*qm, j, k) for k in range(K))
+            assert abs(Cn[i, j] - rn) <= 1e-12 * max(1.0, abs(rn))
+            assert abs(Cm[i, j] - rm) <= 1e-12 * max(1.0, abs(rm))
+
+
+def test_w4a16_fp4_identity_activations_give_the_weights():
+    """A = I: C^T is the dequantized weight matrix itself."""
+    K = 64
+    w = workloads.normal(workloads.rng_for(27, 2), (8, K), 0.02)
+    qn, qm = oracle.quantize_nvfp4(w), oracle.quantize_mxfp4(w)
+    eye = np.eye(K)
+    assert np.array_equal(oracle.gemm_w4a16_nvfp4(eye, *qn).T, oracle.dequantize_nvfp4(*qn))
+    assert np.array_equal(oracle.gemm_w4a16_mxfp4(eye, *qm).T, oracle.dequantize_mxfp4(*qm))
+
+
 def test_grouped_moe_matches_per_row_brute_force():
     T, E, N, K, top = 12, 4, 8, 32, 2
     tok = workloads.to_bf16(workloads.normal(workloads.rng_for(25, 1), (T, K), 1.0)).float().numpy()
