@@ -8,7 +8,8 @@ over the timed steps, with all inputs resident in HBM; ``e2e`` is the same
 metric through the public Python API with the activations copied in from
 pinned host memory and the outputs copied back every step.
 
-Other workloads (``--workload``): ``prefill`` (NVFP4 W4A4, 8192 x 28672 x
+Other workloads (``--workload``): ``decode_nvfp4`` (the decode step with
+NVFP4 weights), ``prefill`` (NVFP4 W4A4, 8192 x 28672 x
 8192, A quantized on the fly), ``moe`` (MXFP4 W4A4, 256 x 2048 x 7168, A
 quantized on the fly), ``grouped`` (64-expert routed NVFP4 MoE), ``tiny``.
 
@@ -268,6 +269,54 @@ class Decode:
     oracle_grain = 64
 
 
+class DecodeNvfp4(Decode):
+    """W4A16 decode with NVFP4 weights: N = K = 8192, bf16 activations M = 1, 4, 16."""
+    name = "w4a16_decode_nvfp4"
+    kernel = "w4a16_kernel<NVFP4>"
+
+    def config(self):
+        return {"workload": "w4a16_decode_nvfp4 N=K=8192 NVFP4 weights (row-major E4M3 scales), "
+                            "bf16 A, M=1,4,16 per step",
+                "M": list(self.Ms), "N": self.N, "K": self.K,
+                "l2": f"rotating {self.copies} weight copies ({self.copies * self.weight_bytes() / 1e6:.0f} MB > L2)"}
+
+    def weight_bytes(self):
+        return self.N * self.K // 2 + self.N * (self.K // 16)
+
+    def bytes_per_gemm(self, M, N=None):
+        N = self.N if N is None else N
+        return N * self.K // 2 + N * (self.K // 16) + M * self.K * 2 + M * N * 2
+
+    def setup(self, q4, dev, seed, shape=None):
+        super().setup(q4, dev, seed, shape)
+        del self.wq, self.ws
+        wd = torch.from_numpy(self.w_host).to(dev)
+        c, s, g = q4.quantize_nvfp4(wd)
+        del wd
+        self.wq = [c] + [c.clone() for _ in range(self.copies - 1)]
+        self.ws = [s] + [s.clone() for _ in range(self.copies - 1)]
+        self.wg = [g] + [g.clone() for _ in range(self.copies - 1)]
+
+    def step(self, i):
+        for j, M in enumerate(self.Ms):
+            c = (3 * i + j) % self.copies
+            self.q4.gemm_w4a16_nvfp4(self.A[M], self.wq[c], self.ws[c], self.wg[c], out=self.C[M])
+
+    def kernel_only(self, i):
+        self.step(i)
+
+    def oracle_prepare(self, rows):
+        import oracle
+        self.o_rows = rows
+        self.o_w = oracle.quantize_nvfp4(self.w_host, rows=np.arange(rows))
+        self.o_a = {M: self.A_host[M].float().numpy() for M in self.Ms}
+
+    def oracle_step(self):
+        import oracle
+        for M in self.Ms:
+            oracle.gemm_w4a16_nvfp4(self.o_a[M], *self.o_w)
+
+
 class W4A4:
     """W4A4 GEMM with A quantized on the fly; B pre-quantized (MMA scale layout)."""
     nvfp4 = True
@@ -494,8 +543,11 @@ class Grouped:
     oracle_grain = 128
 
 
-WORKLOADS = {"decode": Decode, "prefill": Prefill, "moe": Moe, "grouped": Grouped}
-DTYPES = {"decode": "bf16 (exact int4 values) x bf16 -> fp32", "prefill": "e2m1 x e2m1 -> fp32",
+WORKLOADS = {"decode": Decode, "decode_nvfp4": DecodeNvfp4, "prefill": Prefill, "moe": Moe,
+             "grouped": Grouped}
+DTYPES = {"decode": "bf16 (exact int4 values) x bf16 -> fp32",
+          "decode_nvfp4": "bf16 (exact e2m1 x e4m3 values) x bf16 -> fp32",
+          "prefill": "e2m1 x e2m1 -> fp32",
           "moe": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32"}
 
 
@@ -576,7 +628,8 @@ def wl_setup_host(wl, seed):
         wl.N = b.shape[0]
 
 
-SEEDS = {"decode": workloads.SEED_BASE + 2, "moe": workloads.SEED_BASE + 3,
+SEEDS = {"decode": workloads.SEED_BASE + 2, "decode_nvfp4": workloads.SEED_BASE + 2,
+         "moe": workloads.SEED_BASE + 3,
          "prefill": workloads.SEED_BASE + 4, "grouped": workloads.SEED_BASE + 5}
 
 

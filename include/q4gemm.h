@@ -190,6 +190,30 @@ q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t*
                           q4_stream_t stream);
 
 /*
+ * W4A16 with FP4 weights ("Low-bit inference for very large MoE", "Kernels on
+ * different hardware": the W4A16 row lists INT4 or FP4 weights with 16-bit
+ * activations): C[m, n] = sum_k a[m, k] * w[n, k] with
+ *   NVFP4: w = e2m1(code) * e4m3(Ws[n, k / 16]) * g,   g = *w_tensor_scale
+ *   MXFP4: w = e2m1(code) * 2^(Ws[n, k / 32] - 127)
+ * A_bf16 [M, K]; Wq [N, K/2] E2M1 codes; Ws row-major scale bytes
+ * (Q4_SCALES_ROWMAJOR, as quantize_nvfp4 / quantize_mxfp4 write them);
+ * C_bf16 [M, N].  The block scale is folded into each weight in bf16, which
+ * is exact (e2m1 x E4M3 has at most 6 significant bits; e2m1 x 2^e for
+ * scale bytes up to 252, all that a quantizer of finite data writes), so
+ * every product with an activation is exact; the sums are FP32, g is applied
+ * once in FP32, and the only rounding to bf16 is the final store.
+ * K % 128 == 0; any M >= 0 (tuned for M <= 16).  Alignment: A, Wq 16 bytes;
+ * NVFP4 Ws 2 bytes, w_tensor_scale 4 bytes.  Launched like gemm_w4a16_int4
+ * (programmatic dependent launch; Wq and Ws are read before the previous
+ * kernel in the stream has finished, under the same rule as there).
+ */
+q4_status gemm_w4a16_nvfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws,
+                           const float* w_tensor_scale, int64_t M, int64_t N, int64_t K,
+                           void* C_bf16, q4_stream_t stream);
+q4_status gemm_w4a16_mxfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws, int64_t M,
+                           int64_t N, int64_t K, void* C_bf16, q4_stream_t stream);
+
+/*
  * Grouped routed-MoE NVFP4 GEMM ("Low-bit inference for very large MoE",
  * "Kernels on different hardware": one low-bit weight matrix per expert,
  * grouped by routing).  The T tokens [T, K] bf16 are NVFP4-quantized once as

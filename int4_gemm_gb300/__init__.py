@@ -70,6 +70,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "gemm_w4a4_nvfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "gemm_w4a4_mxfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "gemm_w4a16_int4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
+    _sig(lib, "gemm_w4a16_nvfp4", I, P, P, P, P, I64, I64, I64, P, P)
+    _sig(lib, "gemm_w4a16_mxfp4", I, P, P, P, I64, I64, I64, P, P)
     _sig(lib, "grouped_gemm_moe", I, P, I64, I64, P, P, I64, I, P, P, P, I64, P, P, SZ, P)
     _sig(lib, "q4_sync_status", I, P)
     _sig(lib, "q4_status_string", ctypes.c_char_p, I)
@@ -247,6 +249,33 @@ def gemm_w4a16_int4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=Non
     C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
     _check("gemm_w4a16_int4", lib().gemm_w4a16_int4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(), M,
                                                      N, K, C.data_ptr(), None, 0, _stream(stream)))
+    return C
+
+
+def gemm_w4a16_nvfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, Wg: torch.Tensor,
+                     out=None, stream=None) -> torch.Tensor:
+    """C [M, N] bf16 = A [M, K] bf16 . dequant(W)^T, W NVFP4: codes [N, K/2],
+    row-major E4M3 scales [N, K/16], tensor scale Wg (one float32)."""
+    _cuda2d(A, "A")
+    M, K = A.shape
+    N = Wq.shape[0]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    _check("gemm_w4a16_nvfp4", lib().gemm_w4a16_nvfp4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(),
+                                                       Wg.data_ptr(), M, N, K, C.data_ptr(),
+                                                       _stream(stream)))
+    return C
+
+
+def gemm_w4a16_mxfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=None,
+                     stream=None) -> torch.Tensor:
+    """C [M, N] bf16 = A [M, K] bf16 . dequant(W)^T, W MXFP4: codes [N, K/2],
+    row-major E8M0 scales [N, K/32]."""
+    _cuda2d(A, "A")
+    M, K = A.shape
+    N = Wq.shape[0]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    _check("gemm_w4a16_mxfp4", lib().gemm_w4a16_mxfp4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(),
+                                                       M, N, K, C.data_ptr(), _stream(stream)))
     return C
 
 

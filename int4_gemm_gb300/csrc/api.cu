@@ -347,6 +347,32 @@ q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t*
   return launch_w4a16(A_bf16, Wq, Ws, M, N, K, C_bf16, reinterpret_cast<cudaStream_t>(stream));
 }
 
+static q4_status w4a16_fp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws,
+                           const float* w_g, bool nvfp4, int64_t M, int64_t N, int64_t K,
+                           void* C_bf16, q4_stream_t stream) {
+  if (M < 0 || N < 0 || K <= 0) return Q4_ERR_INVALID_ARG;
+  if (K % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (ceil_div(N, 128) > 65535 || ceil_div(M, 16) > 65535) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return Q4_OK;
+  if (!A_bf16 || !Wq || !Ws || !C_bf16 || !aligned(A_bf16, 16) || !aligned(Wq, 16) ||
+      !aligned(C_bf16, 2) || (nvfp4 && (!w_g || !aligned(w_g, 4) || !aligned(Ws, 2))))
+    return Q4_ERR_INVALID_ARG;
+  return launch_w4a16_fp4(A_bf16, Wq, Ws, w_g, nvfp4, M, N, K, C_bf16,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status gemm_w4a16_nvfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws,
+                           const float* w_tensor_scale, int64_t M, int64_t N, int64_t K,
+                           void* C_bf16, q4_stream_t stream) {
+  return w4a16_fp4(A_bf16, Wq, Ws, w_tensor_scale, true, M, N, K, C_bf16, stream);
+}
+
+q4_status gemm_w4a16_mxfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws, int64_t M,
+                           int64_t N, int64_t K, void* C_bf16, q4_stream_t stream) {
+  return w4a16_fp4(A_bf16, Wq, Ws, nullptr, false, M, N, K, C_bf16, stream);
+}
+
 q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            const int32_t* expert_offsets, const int32_t* row_token, int64_t R,
                            int E, const uint8_t* W_codes, const uint8_t* W_scales,

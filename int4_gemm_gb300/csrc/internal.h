@@ -76,6 +76,10 @@ q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream);
 
 q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int64_t M, int64_t N,
                        int64_t K, void* C, cudaStream_t stream);
+// FP4 weights: Wsf row-major E4M3 (nvfp4, tensor scale *wg) or E8M0 bytes
+q4_status launch_w4a16_fp4(const void* A, const uint8_t* Wq, const uint8_t* Wsf, const float* wg,
+                           bool nvfp4, int64_t M, int64_t N, int64_t K, void* C,
+                           cudaStream_t stream);
 
 // TMA descriptor creation through the driver entry point.
 q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,

@@ -68,6 +68,45 @@ __device__ __forceinline__ uint32_t nib_pair_to_bf16x2(uint32_t w) {
   return t;
 }
 
+// Weight formats of the W4A16 kernel.
+constexpr int kInt4 = 0, kNvfp4 = 1, kMxfp4 = 2;
+
+// E2M1 codes at nibbles i and i + 4 of w -> bf16x2 holding code * 2^-126,
+// exactly: the three magnitude bits go to bf16 bits 6..8 (the two low bits of
+// the exponent field and the top mantissa bit) and the sign bit to bit 15.
+// Exponent field 0 is the subnormal range, so code 1 (0.5) becomes
+// 0.5 * 2^-126 like every other code.  sgn = w & 0x88888888.
+template <int i>
+__device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t w, uint32_t sgn) {
+  constexpr int sm = 6 - 4 * i;
+  uint32_t m;
+  if constexpr (sm >= 0) m = w << sm;
+  else m = w >> -sm;
+  return (m & 0x01C001C0u) | ((sgn << (12 - 4 * i)) & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Scale bytes -> float (exact; finite encodings only).  E4M3: bias 7, three
+// mantissa bits, subnormals m * 2^-9.  E8M0: 2^(b - 127), byte 0 = 2^-127.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+  return (b & 0x80u) ? -mag : mag;
+}
+__device__ __forceinline__ float e8m0_value(uint32_t b) {
+  return __uint_as_float(b ? (b << 23) : 0x00400000u);
+}
+// the bf16x2 with both halves equal to v (exact for the scale values above)
+__device__ __forceinline__ uint32_t bf16x2_splat(float v) {
+  const __nv_bfloat162 h = __float2bfloat162_rn(v);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint32_t mapa_u32(uint32_t a, uint32_t rank) {
   uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
@@ -99,12 +138,16 @@ __device__ __forceinline__ void cluster_sync() {
 
 
 // grid = (CS, ceil(N / 256), ceil(M / 16)), cluster = (CS, 1, 1).  TS = token
-// sets of 8 (1 when at most 8 tokens per block, else 2).
-template <int TS>
+// sets of 8 (1 when at most 8 tokens per block, else 2).  FMT: kInt4 (Wsc =
+// FP16 scales [N, K/128]), kNvfp4 (E4M3 bytes [N, K/16], tensor scale *wg) or
+// kMxfp4 (E8M0 bytes [N, K/32]).
+template <int TS, int FMT>
 __global__ void __launch_bounds__(kThreads, 2)
     w4a16_kernel(const __nv_bfloat16* __restrict__ A, const uint8_t* __restrict__ Wq,
-                 const uint16_t* __restrict__ Ws, __nv_bfloat16* __restrict__ C, int M, int N,
-                 int K, int groups_per_cta) {
+                 const void* __restrict__ Wsc, const float* __restrict__ wg,
+                 __nv_bfloat16* __restrict__ C, int M, int N, int K, int groups_per_cta) {
+  const uint16_t* Ws = static_cast<const uint16_t*>(Wsc);
+  const uint8_t* Wf = static_cast<const uint8_t*>(Wsc);
   constexpr int kTp = 8 * TS;  // tokens staged per CTA
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* ring = smem;                                              // [slot][chunk][thread] x 16 B
@@ -165,11 +208,37 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int gi0 = 0; gi0 < ng; gi0 += kChunk) {
     const int gc = min(kChunk, ng - gi0);
     const int c0 = g_begin + gi0;
-    // ---- FP16 scales of this thread's rows for the chunk (eight per row)
+    // ---- scales of this thread's rows for the chunk.  INT4: the FP16 scale of
+    // each of the eight groups.  FP4: per group, the block scales of this
+    // thread's 32 columns (NVFP4: the 2 bytes of blocks 2 quad, 2 quad + 1;
+    // MXFP4: the byte of block quad), packed in order of the group.
     uint32_t spk[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint16_t* src = Ws + (int64_t)(wok[i] ? wrow[i] : 0) * ngroups + c0;
+      const int64_t row = wok[i] ? wrow[i] : 0;
+      if constexpr (FMT == kNvfp4) {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(Wf + row * (K / 16) + (int64_t)c0 * 8) + quad;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = 2 * e < gc ? __ldg(src + 8 * e) : 0u;
+          const uint32_t hi = 2 * e + 1 < gc ? __ldg(src + 8 * e + 4) : 0u;
+          spk[i][e] = lo | (hi << 16);
+        }
+        continue;
+      } else if constexpr (FMT == kMxfp4) {
+        const uint8_t* src = Wf + row * (K / 32) + (int64_t)c0 * 4 + quad;
+        spk[i][2] = spk[i][3] = 0u;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          uint32_t v = 0u;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (4 * e + b < gc) v |= (uint32_t)__ldg(src + 4 * (4 * e + b)) << (8 * b);
+          spk[i][e] = v;
+        }
+        continue;
+      }
+      const uint16_t* src = Ws + row * ngroups + c0;
       if (gc == kChunk && s16) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
         spk[i][0] = v.x; spk[i][1] = v.y; spk[i][2] = v.z; spk[i][3] = v.w;
@@ -213,15 +282,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           v.z = __byte_perm(x[u].y, x[u].w, 0x5410);
           v.w = __byte_perm(x[u].y, x[u].w, 0x7632);
           act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
-          const uint32_t e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+          if constexpr (FMT == kInt4) {
+            const uint32_t e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            sum += __uint_as_float(e[i] << 16) + __uint_as_float(e[i] & 0xFFFF0000u);
+            for (int i = 0; i < 4; ++i)
+              sum += __uint_as_float(e[i] << 16) + __uint_as_float(e[i] & 0xFFFF0000u);
+          }
         }
       }
+      if constexpr (FMT == kInt4) {  // FP4 weights have no offset to remove
 #pragma unroll
-      for (int o = 1; o < kSplit; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (part == 0 && gi < gc && tok < mt) csum[gi * kTok + tok] = 136.0f * sum;
+        for (int o = 1; o < kSplit; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (part == 0 && gi < gc && tok < mt) csum[gi * kTok + tok] = 136.0f * sum;
+      }
     }
     __syncthreads();
 
@@ -235,6 +308,54 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           wv[i] = *reinterpret_cast<const uint4*>(ring + ((slot * 4 + i) * kThreads + tid) * 16);
+        if constexpr (FMT != kInt4) {
+          // FP4: the block scale is folded into each weight, exactly in bf16
+          // (e2m1 x E4M3 has at most 6 significant bits; e2m1 x 2^e is exact
+          // for the E8M0 bytes a quantizer of finite data writes), so the
+          // products with the activations are exact and the MMA accumulates
+          // straight into the FP32 sums: no per-group promotion.
+          uint32_t s2[4][2];  // [row][half of this thread's 32 columns]
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            if constexpr (FMT == kNvfp4) {
+              const uint32_t b2 = (spk[r][gl >> 1] >> ((gl & 1) * 16)) & 0xFFFFu;
+              s2[r][0] = bf16x2_splat(e4m3_value(b2 & 0xFFu));
+              s2[r][1] = bf16x2_splat(e4m3_value(b2 >> 8));
+            } else {
+              s2[r][0] = s2[r][1] = bf16x2_splat(e8m0_value((spk[r][gl >> 2] >> ((gl & 3) * 8)) & 0xFFu));
+            }
+          }
+          constexpr uint32_t kTwo126 = 0x7E807E80u;  // bf16x2 of 2^126
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 bf[TS];
+#pragma unroll
+            for (int s = 0; s < TS; ++s) bf[s] = act[((gl * 4 + w) * kTp + lrow + 8 * s) * 4 + quad];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const uint32_t lo = word(wv[2 * t], w), hi = word(wv[2 * t + 1], w);
+              const uint32_t ls = lo & 0x88888888u, hs = hi & 0x88888888u;
+              const uint32_t sl = s2[2 * t][w >> 1], sh = s2[2 * t + 1][w >> 1];
+              uint32_t pl[4], ph[4];
+              pl[0] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<0>(lo, ls), kTwo126), sl);
+              pl[1] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<1>(lo, ls), kTwo126), sl);
+              pl[2] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<2>(lo, ls), kTwo126), sl);
+              pl[3] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<3>(lo, ls), kTwo126), sl);
+              ph[0] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<0>(hi, hs), kTwo126), sh);
+              ph[1] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<1>(hi, hs), kTwo126), sh);
+              ph[2] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<2>(hi, hs), kTwo126), sh);
+              ph[3] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<3>(hi, hs), kTwo126), sh);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int s = 0; s < TS; ++s)
+                  mma_bf16_16816(acc[t][s], pl[2 * h], ph[2 * h], pl[2 * h + 1], ph[2 * h + 1],
+                                 h ? bf[s].z : bf[s].x, h ? bf[s].w : bf[s].y);
+            }
+          }
+          issue(gi + kRing);  // refill the slot just read
+          continue;
+        }
         float part[2][TS][4];
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -317,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   cluster_sync();  // every push has landed; nothing remote is touched afterwards
 
   // ---- rank q adds rows [q * per, (q + 1) * per) over the source ranks in order
+  // and applies the NVFP4 tensor scale (read after the dependency wait)
+  const float gsc = FMT == kNvfp4 ? __ldg(wg) : 1.f;
   const int r_lo = rank * per, r_hi = min(kRows, r_lo + per);
   const int tq = (mt + 3) / 4;  // groups of four tokens
   for (int e = tid; e < (r_hi - r_lo) * tq; e += kThreads) {
@@ -331,15 +454,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float vv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (4 * t4 + i < mt) C[(int64_t)(m0 + 4 * t4 + i) * N + n] = __float2bfloat16_rn(vv[i]);
+        if (4 * t4 + i < mt) C[(int64_t)(m0 + 4 * t4 + i) * N + n] = __float2bfloat16_rn(vv[i] * gsc);
     }
   }
 }
 
 }  // namespace
 
-q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int64_t M, int64_t N,
-                       int64_t K, void* C, cudaStream_t stream) {
+namespace {
+template <int FMT>
+q4_status launch_w4a16_fmt(const void* A, const uint8_t* Wq, const void* Wsc, const float* wg,
+                           int64_t M, int64_t N, int64_t K, void* C, cudaStream_t stream) {
   if (M == 0 || N == 0) return Q4_OK;
   const int ngroups = (int)(K / 128);
   // split K over a cluster of up to 8 CTAs, at least one group each
@@ -354,10 +479,10 @@ q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!attr_done[dev]) {
-    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem1));
-    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem2));
+    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<1, FMT>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1));
+    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a16_kernel<2, FMT>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2));
     attr_done[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
@@ -378,12 +503,25 @@ q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int
   cfg.numAttrs = 2;
   // one token set of 8 when every token block has at most 8 tokens
   if (M <= 8)
-    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel<1>, (const __nv_bfloat16*)A, Wq, Ws,
+    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel<1, FMT>, (const __nv_bfloat16*)A, Wq, Wsc, wg,
                                    (__nv_bfloat16*)C, (int)M, (int)N, (int)K, gpc));
   else
-    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel<2>, (const __nv_bfloat16*)A, Wq, Ws,
+    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a16_kernel<2, FMT>, (const __nv_bfloat16*)A, Wq, Wsc, wg,
                                    (__nv_bfloat16*)C, (int)M, (int)N, (int)K, gpc));
   return Q4_OK;
+}
+}  // namespace
+
+q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int64_t M, int64_t N,
+                       int64_t K, void* C, cudaStream_t stream) {
+  return launch_w4a16_fmt<kInt4>(A, Wq, Ws, nullptr, M, N, K, C, stream);
+}
+
+q4_status launch_w4a16_fp4(const void* A, const uint8_t* Wq, const uint8_t* Wsf, const float* wg,
+                           bool nvfp4, int64_t M, int64_t N, int64_t K, void* C,
+                           cudaStream_t stream) {
+  return nvfp4 ? launch_w4a16_fmt<kNvfp4>(A, Wq, Wsf, wg, M, N, K, C, stream)
+               : launch_w4a16_fmt<kMxfp4>(A, Wq, Wsf, nullptr, M, N, K, C, stream);
 }
 
 }  // namespace q4

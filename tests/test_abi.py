@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["quantize_nvfp4", "quantize_mxfp4", "quantize_int4_g128", "gemm_w4a4_nvfp4",
-                 "gemm_w4a4_mxfp4", "gemm_w4a16_int4", "grouped_gemm_moe", "q4_sync_status",
+                 "gemm_w4a4_mxfp4", "gemm_w4a16_int4", "gemm_w4a16_nvfp4", "gemm_w4a16_mxfp4",
+                 "grouped_gemm_moe", "q4_sync_status",
                  "q4_workspace_size", "q4_scales_to_mma"]:
         assert want in names
 
@@ -53,9 +54,16 @@ def test_host_argument_checks(clib):
     assert clib.gemm_w4a16_int4(fake + 2, fake, fake, 4, 4, 128, fake, None, 0, None) == -1
     # NVFP4 quantize needs its workspace
     assert clib.quantize_nvfp4(fake, 1, 4, 64, fake, fake, 0, fake, None, 0, None) == -6
+    # FP4-weight W4A16: K % 128, a missing tensor scale, misaligned NVFP4 scales
+    assert clib.gemm_w4a16_nvfp4(fake, fake, fake, fake, 4, 4, 100, fake, None) == -2
+    assert clib.gemm_w4a16_mxfp4(fake, fake, fake, 4, 4, 64, fake, None) == -2
+    assert clib.gemm_w4a16_nvfp4(fake, fake, fake, None, 4, 4, 128, fake, None) == -1
+    assert clib.gemm_w4a16_nvfp4(fake, fake, fake + 1, fake, 4, 4, 128, fake, None) == -1
+    assert clib.gemm_w4a16_mxfp4(None, fake, fake, 4, 4, 128, fake, None) == -1
     # empty problems are no-ops
     assert clib.quantize_int4_g128(None, 1, 0, 128, None, None, None) == 0
     assert clib.gemm_w4a16_int4(None, None, None, 0, 4, 128, None, None, 0, None) == 0
+    assert clib.gemm_w4a16_mxfp4(None, None, None, 0, 4, 128, None, None) == 0
 
 
 def test_workspace_sizes(clib):

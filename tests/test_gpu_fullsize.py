@@ -30,6 +30,37 @@ def test_decode_full(lib):
     assert lib.sync_status() == 0
 
 
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_decode_fp4_weights_full_sampled(lib, fmt):
+    """Decode with FP4 weights at N = K = 8192, M = 1, 4, 16: codes and scales
+    of 512 sampled weight rows bit for bit, and the outputs of those rows (all
+    tokens) against the oracle."""
+    N = K = 8192
+    seed = workloads.SEED_BASE + 2
+    w = workloads.int4_weights(N, K, seed)
+    rows = np.sort(np.random.default_rng(7).choice(N, 512, replace=False))
+    wt = torch.from_numpy(w).cuda()
+    if fmt == "nvfp4":
+        c, sc, g = lib.quantize_nvfp4(wt)
+        oq = oracle.quantize_nvfp4(w, rows=rows)
+        assert g.cpu().numpy()[0] == oq[2]
+    else:
+        c, sc = lib.quantize_mxfp4(wt)
+        oq = oracle.quantize_mxfp4(w, rows=rows)
+    assert np.array_equal(c.cpu().numpy()[rows], oq[0])
+    assert np.array_equal(sc.cpu().numpy()[rows], oq[1])
+    for M in (1, 4, 16):
+        A = workloads.to_bf16(workloads.normal(workloads.rng_for(seed, 1), (M, K), 1.0))
+        if fmt == "nvfp4":
+            C = lib.gemm_w4a16_nvfp4(A.cuda(), c, sc, g)
+            R = oracle.gemm_w4a16_nvfp4(A.float().numpy(), *oq)
+        else:
+            C = lib.gemm_w4a16_mxfp4(A.cuda(), c, sc)
+            R = oracle.gemm_w4a16_mxfp4(A.float().numpy(), *oq)
+        assert_gemm_close(C.float().cpu().numpy()[:, rows], R)
+    assert lib.sync_status() == 0
+
+
 def test_moe_mxfp4_full(lib):
     a, b = workloads.moe()
     ad, bd = a.cuda(), torch.from_numpy(b).cuda()

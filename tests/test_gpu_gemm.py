@@ -154,6 +154,67 @@ def test_w4a16_int4(lib, shape):
     assert lib.sync_status() == 0
 
 
+W4A16_FP4_SHAPES = [(1, 256, 1024), (4, 520, 2048), (16, 1000, 1152), (5, 128, 128),
+                    (17, 300, 8192), (33, 256, 512)]
+
+
+def _fp4_weights(lib, w, fmt):
+    """GPU-quantized FP4 weights (row-major scales), checked bit for bit
+    against the oracle's, and the oracle's copy."""
+    wt = torch.from_numpy(w).cuda()
+    if fmt == "nvfp4":
+        c, s, g = lib.quantize_nvfp4(wt)
+        oq = oracle.quantize_nvfp4(w)
+        assert np.array_equal(c.cpu().numpy(), oq[0]) and np.array_equal(s.cpu().numpy(), oq[1])
+        assert g.cpu().numpy()[0] == oq[2]
+        return (c, s, g), oq
+    c, s = lib.quantize_mxfp4(wt)
+    oq = oracle.quantize_mxfp4(w)
+    assert np.array_equal(c.cpu().numpy(), oq[0]) and np.array_equal(s.cpu().numpy(), oq[1])
+    return (c, s), oq
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("shape", W4A16_FP4_SHAPES)
+def test_w4a16_fp4_weights(lib, shape, fmt):
+    M, N, K = shape
+    A, w = workloads.decode(M, seed=sum(shape) + 3, N=N, K=K)
+    q, oq = _fp4_weights(lib, w, fmt)
+    if fmt == "nvfp4":
+        C = lib.gemm_w4a16_nvfp4(A.cuda(), *q)
+        R = oracle.gemm_w4a16_nvfp4(A.float().numpy(), *oq)
+    else:
+        C = lib.gemm_w4a16_mxfp4(A.cuda(), *q)
+        R = oracle.gemm_w4a16_mxfp4(A.float().numpy(), *oq)
+    assert_gemm_close(C.float().cpu().numpy(), R)
+    assert lib.sync_status() == 0
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_w4a16_fp4_identity_activations_give_the_weights(lib, fmt):
+    """A = I (and a tensor scale of 1): every output is one dequantized weight,
+    e2m1 x block scale, which bf16 holds exactly -- so the output must equal
+    the oracle's dequantization bit for bit, for every code (the subnormal
+    0.5 included) and scale met."""
+    K, N = 256, 384
+    w = workloads.normal(workloads.rng_for(31, 2), (N, K), 0.02)
+    w[5, 3:40] *= 300.0  # large blocks next to small ones in the same rows
+    w[9, 100:140] *= 1e-3
+    q, oq = _fp4_weights(lib, w, fmt)
+    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    for m0 in range(0, K, 128):
+        A = eye[m0:m0 + 128].contiguous()
+        if fmt == "nvfp4":
+            one = torch.ones(1, dtype=torch.float32, device="cuda")
+            C = lib.gemm_w4a16_nvfp4(A, q[0], q[1], one)
+            want = oracle.dequantize_nvfp4(oq[0], oq[1], np.float32(1.0))[:, m0:m0 + 128].T
+        else:
+            C = lib.gemm_w4a16_mxfp4(A, *q)
+            want = oracle.dequantize_mxfp4(*oq)[:, m0:m0 + 128].T
+        assert np.array_equal(C.float().cpu().numpy(), want.astype(np.float32))
+    assert lib.sync_status() == 0
+
+
 def test_w4a16_right_after_quantizing_its_weights(lib):
     """Weights quantized into poisoned buffers and read by the very next launch
     on the same stream, with no host synchronization in between: the GEMM
