@@ -400,16 +400,20 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         float* part = reinterpret_cast<float*>(smem) + (q * 32 + lane) * kPartStride;
         const bool has_k = kb_end > kb_begin;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
+        for (int c0 = 0; c0 < BN / 32; c0 += 4) {  // four 32-column loads per TMEM wait
+          uint32_t r[4][32];
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (c0 + g) * 32, r[g]);
           tmem_ld_wait();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            reinterpret_cast<float4*>(part + c * 32)[v] =
-                has_k ? make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<float4*>(part + (c0 + g) * 32)[v] =
+                  has_k ? make_float4(__uint_as_float(r[g][4 * v]), __uint_as_float(r[g][4 * v + 1]),
+                                      __uint_as_float(r[g][4 * v + 2]), __uint_as_float(r[g][4 * v + 3]))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         tc_fence_before();
         ++tcount;
