@@ -31,17 +31,29 @@ def e2m1_decode(code) -> np.ndarray:
     return np.where((c & 8) != 0, -mag, mag)
 
 
-def e2m1_nearest(mag) -> np.ndarray:
+def e2m1_nearest(mag, ties: str = "smaller") -> np.ndarray:
     """Index (0..7) of the E2M1 magnitude nearest to each ``mag`` in [0, 6].
 
     "Quantization in deployment", "Fake quantization", ``fp4``: the value is
     the one at the smallest absolute distance, and when two are equally near
     the first one in the table (the smaller magnitude) is taken.  The distances
     are formed in float64, where they are exact for float32 inputs.
+
+    ``ties="even"`` is the IEEE alternative (round half to even, the rounding
+    of the hardware E2M1 convert): of two equally near values the one with the
+    even code, i.e. mantissa bit 0, is taken.
     """
     m = np.asarray(mag, dtype=np.float64)
     dist = np.abs(m[..., None] - E2M1_MAGNITUDES)
-    return np.argmin(dist, axis=-1).astype(np.uint8)
+    first = np.argmin(dist, axis=-1)
+    if ties == "smaller":
+        return first.astype(np.uint8)
+    if ties != "even":
+        raise ValueError(ties)
+    nxt = np.minimum(first + 1, 7)
+    tie = np.take_along_axis(dist, nxt[..., None], -1)[..., 0] == np.take_along_axis(
+        dist, first[..., None], -1)[..., 0]
+    return np.where(tie & (first % 2 == 1), nxt, first).astype(np.uint8)
 
 
 def e4m3_decode(byte) -> np.ndarray:

@@ -47,12 +47,23 @@ def unpack_nibbles(packed: np.ndarray) -> np.ndarray:
     return out
 
 
-def _e2m1_codes(x: np.ndarray, S: np.ndarray) -> np.ndarray:
+def _ties(rounding: str) -> str:
+    """The E2M1 tie rule of a rounding mode: the pages' (ties to the smaller
+    magnitude) or IEEE round half to even."""
+    if rounding == "pages":
+        return "smaller"
+    if rounding == "rne":
+        return "even"
+    raise ValueError(rounding)
+
+
+def _e2m1_codes(x: np.ndarray, S: np.ndarray, ties: str = "smaller") -> np.ndarray:
     """E2M1 codes of x / S ("Quantization in deployment", "Fake quantization",
     ``fp4``): y = clamp(x / S, -6, 6) in float32, the nearest E2M1 magnitude
-    (ties to the smaller one), and the sign of x in bit 3."""
+    (ties to the smaller one, or to the even code with ``ties="even"``), and
+    the sign of x in bit 3."""
     y = np.clip(x / S, F32(-E2M1_MAX), F32(E2M1_MAX))
-    idx = e2m1_nearest(np.abs(y))
+    idx = e2m1_nearest(np.abs(y), ties)
     return idx | ((x < 0).astype(np.uint8) << 3)
 
 
@@ -69,7 +80,7 @@ def nvfp4_tensor_scale(x) -> np.float32:
     return F32(max(amax, F32_1E_12) / F32(E4M3_MAX * E2M1_MAX))
 
 
-def quantize_nvfp4(x, g=None, rows=None):
+def quantize_nvfp4(x, g=None, rows=None, rounding="pages"):
     """NVFP4 quantization ("Quantization in deployment", "Fake quantization",
     ``nvfp4`` then ``fp4``), per block of 16 along K:
 
@@ -82,6 +93,8 @@ def quantize_nvfp4(x, g=None, rows=None):
     A block whose scale byte is 0 stores all-zero codes (reading 4).
     ``g`` defaults to :func:`nvfp4_tensor_scale` of the whole ``x``; ``rows``
     optionally selects the rows to quantize (g still covers the whole x).
+    ``rounding="rne"`` rounds step 5 half to even instead of to the smaller
+    magnitude (everything else is unchanged).
     Returns (codes [r, K/2] u8, scales [r, K/16] u8, g float32).
     """
     a = _as_f32_2d(x)
@@ -99,7 +112,7 @@ def quantize_nvfp4(x, g=None, rows=None):
         t = (amax_b / F32(6.0)) / g
         bs = e4m3_encode(t)
         S = (np.maximum(e4m3_decode(bs).astype(np.float32), F32_1E_12) * g).astype(np.float32)
-        c = _e2m1_codes(blk, S[..., None])
+        c = _e2m1_codes(blk, S[..., None], _ties(rounding))
         c = np.where((bs == 0)[..., None], np.uint8(0), c)
         codes[r0:r1] = pack_nibbles(c.reshape(r1 - r0, K))
         scales[r0:r1] = bs
@@ -119,7 +132,7 @@ def dequantize_nvfp4(codes, scales, g) -> np.ndarray:
 # MXFP4: E2M1 codes, one E8M0 (power of two) scale per 32
 # ---------------------------------------------------------------------------
 
-def quantize_mxfp4(x, rows=None):
+def quantize_mxfp4(x, rows=None, rounding="pages"):
     """MXFP4 quantization ("Quantization in deployment", "Fake quantization",
     ``mxfp4``), per block of 32 along K:
 
@@ -129,7 +142,8 @@ def quantize_mxfp4(x, rows=None):
        lands in [4, 8) times the scale ("Quantization chains", "MXFP4 against
        NVFP4 scales");
     3. scale S = 2^e, stored as the E8M0 byte e + 127;
-    4. each element is rounded to E2M1 at x / S, clamped to +-6.
+    4. each element is rounded to E2M1 at x / S, clamped to +-6 (ties to the
+       smaller magnitude, or half to even with ``rounding="rne"``).
 
     Returns (codes [r, K/2] u8, scales [r, K/32] u8).
     """
@@ -146,7 +160,7 @@ def quantize_mxfp4(x, rows=None):
         amax_b = np.maximum(np.max(np.abs(blk), axis=-1), F32_1E_12)
         e = floor_log2(amax_b) - 2
         S = np.ldexp(F32(1.0), e.astype(np.int32)).astype(np.float32)
-        c = _e2m1_codes(blk, S[..., None])
+        c = _e2m1_codes(blk, S[..., None], _ties(rounding))
         codes[r0:r1] = pack_nibbles(c.reshape(r1 - r0, K))
         scales[r0:r1] = (e + 127).astype(np.uint8)
     return codes, scales

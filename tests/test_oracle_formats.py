@@ -52,6 +52,41 @@ def test_e2m1_nearest_brute_force_and_ties_to_smaller():
     assert F.e2m1_nearest(np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])).tolist() == [0, 1, 2, 3, 4, 5, 6]
 
 
+def test_e2m1_nearest_ties_to_even_is_ieee_half_even():
+    """ties="even" agrees with rounding to one mantissa bit with numpy's round
+    half to even, binade by binade (0.5 steps below 2, 1 in [2, 4), 2 in
+    [4, 6]), on a dense grid that includes every midpoint; and it differs from
+    the pages' rule exactly at the midpoints of an odd lower neighbour."""
+    mags = np.concatenate([np.arange(0, 6.0001, 1 / 64), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]])
+    step = np.where(mags < 2, 0.5, np.where(mags < 4, 1.0, 2.0))
+    want = np.minimum(np.round(mags / step) * step, 6.0)
+    got = F.E2M1_MAGNITUDES[F.e2m1_nearest(mags, ties="even")]
+    assert np.array_equal(got, want)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    assert list(F.e2m1_nearest(mids, ties="even")) == [0, 2, 2, 4, 4, 6, 6]
+    assert list(F.e2m1_nearest(mids)) == [0, 1, 2, 3, 4, 5, 6]
+    off = ~np.isin(mags, mids)
+    assert np.array_equal(F.e2m1_nearest(mags[off], ties="even"), F.e2m1_nearest(mags[off]))
+
+
+def test_quantizers_round_half_even_on_request():
+    """MXFP4 with scale 1 (block max 6): the seven midpoints and their
+    negatives quantize to the even codes with rounding="rne" and to the
+    smaller ones by default; NVFP4 with S = 1 likewise."""
+    import oracle
+    from oracle.quantize import unpack_nibbles
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    row = np.array([6.0] + mids + [-m for m in mids] + [0.0] * 17, np.float32)[None, :]
+    pages = unpack_nibbles(oracle.quantize_mxfp4(row)[0])[0, 1:15]
+    rne = unpack_nibbles(oracle.quantize_mxfp4(row, rounding="rne")[0])[0, 1:15]
+    assert list(pages) == [0, 1, 2, 3, 4, 5, 6] + [8, 9, 10, 11, 12, 13, 14]
+    assert list(rne) == [0, 2, 2, 4, 4, 6, 6] + [8, 10, 10, 12, 12, 14, 14]
+    nv = np.array([2688.0] + [0.0] * 15 + [6.0] + mids + [0.0] * 8, np.float32)[None, :]  # g = 1, S = 1
+    c_p = unpack_nibbles(oracle.quantize_nvfp4(nv)[0])[0, 17:24]
+    c_r = unpack_nibbles(oracle.quantize_nvfp4(nv, rounding="rne")[0])[0, 17:24]
+    assert list(c_p) == [0, 1, 2, 3, 4, 5, 6] and list(c_r) == [0, 2, 2, 4, 4, 6, 6]
+
+
 def test_e4m3_limits_from_pages():
     g = GOLD["e4m3_limits"]
     pos = F.e4m3_decode(np.arange(0x7F))
