@@ -69,6 +69,10 @@ typedef int q4_status;
 
 typedef enum { Q4_F32 = 0, Q4_BF16 = 1, Q4_F16 = 2 } q4_dtype;
 typedef enum { Q4_SCALES_ROWMAJOR = 0, Q4_SCALES_MMA = 1 } q4_scale_layout;
+/* Tie rule of the E2M1 rounding step: the pages' (a value halfway between two
+ * E2M1 magnitudes takes the smaller one) or IEEE round half to even (the even
+ * code, mantissa bit 0).  Everything else is identical in both modes. */
+typedef enum { Q4_ROUND_PAGES = 0, Q4_ROUND_RNE = 1 } q4_rounding;
 
 /* Operation codes for q4_workspace_size(). */
 typedef enum {
@@ -131,6 +135,21 @@ q4_status quantize_nvfp4(const void* x, int x_dtype, int64_t rows, int64_t K, ui
  */
 q4_status quantize_mxfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
                          uint8_t* scales, int scale_layout, q4_stream_t stream);
+
+/*
+ * The two FP4 quantizers with a choice of E2M1 tie rule (q4_rounding).
+ * quantize_nvfp4 / quantize_mxfp4 are these with Q4_ROUND_PAGES.  With
+ * Q4_ROUND_RNE an element whose quotient x / S (float32) lies exactly halfway
+ * between two E2M1 magnitudes gets the even code (0.25 -> 0, 0.75 -> 1,
+ * 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4); scales, tensor scale,
+ * signs, layouts, workspace and errors are as in the calls above (an unknown
+ * rounding value is Q4_ERR_INVALID_ARG).
+ */
+q4_status quantize_nvfp4_ex(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                            uint8_t* scales, int scale_layout, int rounding, float* tensor_scale,
+                            void* ws, size_t ws_bytes, q4_stream_t stream);
+q4_status quantize_mxfp4_ex(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                            uint8_t* scales, int scale_layout, int rounding, q4_stream_t stream);
 
 /*
  * Symmetric INT4 quantization with one FP16 scale per 128 (K % 128 == 0),

@@ -26,6 +26,7 @@ OP_QUANTIZE_NVFP4, OP_GEMM_W4A4_NVFP4, OP_GEMM_W4A4_MXFP4, OP_GEMM_W4A16_INT4 = 
 
 _DTYPE = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
 _LAYOUT = {"rowmajor": ROWMAJOR, "mma": MMA}
+_ROUNDING = {"pages": 0, "rne": 1}  # q4_rounding: E2M1 ties to the smaller magnitude / to even
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -64,6 +65,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "q4_mma_scales_bytes", SZ, I64, I64)
     _sig(lib, "quantize_nvfp4", I, P, I, I64, I64, P, P, I, P, P, SZ, P)
     _sig(lib, "quantize_mxfp4", I, P, I, I64, I64, P, P, I, P)
+    _sig(lib, "quantize_nvfp4_ex", I, P, I, I64, I64, P, P, I, I, P, P, SZ, P)
+    _sig(lib, "quantize_mxfp4_ex", I, P, I, I64, I64, P, P, I, I, P)
     _sig(lib, "quantize_int4_g128", I, P, I, I64, I64, P, P, P)
     _sig(lib, "q4_scales_to_mma", I, P, I64, I64, P, P)
     op = ctypes.POINTER(_Operand)
@@ -122,8 +125,10 @@ def mma_scales_bytes(rows: int, nsf: int) -> int:
 
 # --------------------------------------------------------------------------- quantizers
 
-def quantize_nvfp4(x: torch.Tensor, scale_layout: str = "rowmajor", stream=None):
-    """-> (codes u8 [rows, K/2], scales u8, tensor_scale f32 [1])."""
+def quantize_nvfp4(x: torch.Tensor, scale_layout: str = "rowmajor", rounding: str = "pages",
+                   stream=None):
+    """-> (codes u8 [rows, K/2], scales u8, tensor_scale f32 [1]).
+    rounding: "pages" (E2M1 ties to the smaller magnitude) or "rne"."""
     _cuda2d(x, "x")
     rows, K = x.shape
     dev = x.device
@@ -135,14 +140,16 @@ def quantize_nvfp4(x: torch.Tensor, scale_layout: str = "rowmajor", stream=None)
         scales = _empty(mma_scales_bytes(rows, K // 16), dev)
     ts = torch.empty(1, dtype=torch.float32, device=dev)
     ws = workspace(OP_QUANTIZE_NVFP4, rows, 0, K, dev)
-    _check("quantize_nvfp4", lib().quantize_nvfp4(
+    _check("quantize_nvfp4", lib().quantize_nvfp4_ex(
         x.data_ptr(), _DTYPE[x.dtype], rows, K, codes.data_ptr(), scales.data_ptr(), lay,
-        ts.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+        _ROUNDING[rounding], ts.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return codes, scales, ts
 
 
-def quantize_mxfp4(x: torch.Tensor, scale_layout: str = "rowmajor", stream=None):
-    """-> (codes u8 [rows, K/2], scales u8)."""
+def quantize_mxfp4(x: torch.Tensor, scale_layout: str = "rowmajor", rounding: str = "pages",
+                   stream=None):
+    """-> (codes u8 [rows, K/2], scales u8).
+    rounding: "pages" (E2M1 ties to the smaller magnitude) or "rne"."""
     _cuda2d(x, "x")
     rows, K = x.shape
     dev = x.device
@@ -152,9 +159,9 @@ def quantize_mxfp4(x: torch.Tensor, scale_layout: str = "rowmajor", stream=None)
         scales = torch.empty((rows, K // 32), dtype=torch.uint8, device=dev)
     else:
         scales = _empty(mma_scales_bytes(rows, K // 32), dev)
-    _check("quantize_mxfp4", lib().quantize_mxfp4(
+    _check("quantize_mxfp4", lib().quantize_mxfp4_ex(
         x.data_ptr(), _DTYPE[x.dtype], rows, K, codes.data_ptr(), scales.data_ptr(), lay,
-        _stream(stream)))
+        _ROUNDING[rounding], _stream(stream)))
     return codes, scales
 
 

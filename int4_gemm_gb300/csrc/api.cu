@@ -264,11 +264,12 @@ size_t q4_workspace_size_moe(int64_t T, int64_t N, int64_t K, int E, int64_t R) 
   return c.used;
 }
 
-q4_status quantize_nvfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
-                         uint8_t* scales, int scale_layout, float* tensor_scale, void* ws,
-                         size_t ws_bytes, q4_stream_t stream) {
+q4_status quantize_nvfp4_ex(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                            uint8_t* scales, int scale_layout, int rounding, float* tensor_scale,
+                            void* ws, size_t ws_bytes, q4_stream_t stream) {
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (rows < 0 || K <= 0 || !valid_dtype(x_dtype)) return Q4_ERR_INVALID_ARG;
+  if (rounding != Q4_ROUND_PAGES && rounding != Q4_ROUND_RNE) return Q4_ERR_INVALID_ARG;
   if (K % 16) return Q4_ERR_UNSUPPORTED_SHAPE;
   if (scale_layout != Q4_SCALES_ROWMAJOR && scale_layout != Q4_SCALES_MMA) return Q4_ERR_INVALID_ARG;
   if (!tensor_scale) return Q4_ERR_INVALID_ARG;
@@ -286,18 +287,33 @@ q4_status quantize_nvfp4(const void* x, int x_dtype, int64_t rows, int64_t K, ui
     return Q4_OK;
   }
   if ((st = launch_amax(x, x_dtype, rows * K, amax, s)) != Q4_OK) return st;
-  return launch_quant_nvfp4(x, x_dtype, rows, K, codes, scales, scale_layout, amax, tensor_scale, s);
+  return launch_quant_nvfp4(x, x_dtype, rows, K, codes, scales, scale_layout, amax, tensor_scale, s,
+                            rounding == Q4_ROUND_RNE);
 }
 
-q4_status quantize_mxfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
-                         uint8_t* scales, int scale_layout, q4_stream_t stream) {
+q4_status quantize_nvfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                         uint8_t* scales, int scale_layout, float* tensor_scale, void* ws,
+                         size_t ws_bytes, q4_stream_t stream) {
+  return quantize_nvfp4_ex(x, x_dtype, rows, K, codes, scales, scale_layout, Q4_ROUND_PAGES,
+                           tensor_scale, ws, ws_bytes, stream);
+}
+
+q4_status quantize_mxfp4_ex(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                            uint8_t* scales, int scale_layout, int rounding, q4_stream_t stream) {
   if (rows < 0 || K <= 0 || !valid_dtype(x_dtype)) return Q4_ERR_INVALID_ARG;
+  if (rounding != Q4_ROUND_PAGES && rounding != Q4_ROUND_RNE) return Q4_ERR_INVALID_ARG;
   if (K % 32) return Q4_ERR_UNSUPPORTED_SHAPE;
   if (scale_layout != Q4_SCALES_ROWMAJOR && scale_layout != Q4_SCALES_MMA) return Q4_ERR_INVALID_ARG;
   if (rows == 0) return Q4_OK;
   if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16)) return Q4_ERR_INVALID_ARG;
   return launch_quant_mxfp4(x, x_dtype, rows, K, codes, scales, scale_layout,
-                            reinterpret_cast<cudaStream_t>(stream));
+                            reinterpret_cast<cudaStream_t>(stream), rounding == Q4_ROUND_RNE);
+}
+
+q4_status quantize_mxfp4(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                         uint8_t* scales, int scale_layout, q4_stream_t stream) {
+  return quantize_mxfp4_ex(x, x_dtype, rows, K, codes, scales, scale_layout, Q4_ROUND_PAGES,
+                           stream);
 }
 
 q4_status quantize_int4_g128(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes,

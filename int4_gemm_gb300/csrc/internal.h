@@ -27,11 +27,12 @@ int num_sms();                        // SM count of the current device
 // ---------------------------------------------------------------- quantizers
 q4_status launch_amax(const void* x, int dtype, int64_t n, unsigned* amax_bits,
                       cudaStream_t stream);
+// rne: E2M1 ties to the even code instead of the pages' smaller magnitude
 q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                              uint8_t* scales, int layout, const unsigned* amax_bits,
-                             float* tensor_scale, cudaStream_t stream);
+                             float* tensor_scale, cudaStream_t stream, bool rne = false);
 q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
-                             uint8_t* scales, int layout, cudaStream_t stream);
+                             uint8_t* scales, int layout, cudaStream_t stream, bool rne = false);
 q4_status launch_quant_int4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                             uint16_t* scales, cudaStream_t stream);
 q4_status launch_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, uint8_t* dst,

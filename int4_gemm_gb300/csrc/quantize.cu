@@ -138,11 +138,13 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
 }
 
 // E2M1 magnitude code of |x| from its seven decision bounds: the number of
-// bounds it reaches.
-__device__ __forceinline__ uint32_t code_from_bounds(float a, const float (&B)[7], bool strict) {
+// bounds it passes.  Bound k lies between codes k and k + 1; at equality the
+// pages' rule keeps the smaller code, round-half-to-even (rne) the even one,
+// i.e. it passes the odd bounds.
+__device__ __forceinline__ uint32_t code_from_bounds(float a, const float (&B)[7], bool rne) {
   uint32_t c = 0;
 #pragma unroll
-  for (int k = 0; k < 7; ++k) c += strict ? (a > B[k]) : (a >= B[k]);
+  for (int k = 0; k < 7; ++k) c += (a > B[k]) | ((k & 1) & rne & (a == B[k]));
   return c;
 }
 
@@ -172,6 +174,8 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 //    division.  If y itself has three significant bits it may be a tie; its
 //    predecessor lies in the cell that ties-to-smaller selects, and any other
 //    three-bit y lies inside its cell, so the predecessor converts correctly.
+//    With rne (round half to even on request) y itself is converted: the
+//    hardware convert breaks the tie to the even code.
 // The sign goes in bit 3 when x < 0, also for codes of magnitude 0; the
 // hardware convert keeps the sign of a negative zero.
 // Persistent: each CTA walks tiles of 256 units (one per thread), a 4-slot
@@ -184,7 +188,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 4)
     nvfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, int layout, int64_t nsf4,
-                 const unsigned* __restrict__ amax_bits, float* tensor_scale, KernelCtl ctl) {
+                 const unsigned* __restrict__ amax_bits, float* tensor_scale, KernelCtl ctl,
+                 bool rne) {
   pdl_wait();  // inputs may come from the previous kernel
   // x and codes start at row um.row0; scales are indexed by the global row
   constexpr uint32_t kTileBytes = kQUnits * 16 * sizeof(T);
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 4)
           const uint32_t d = (__float_as_uint(y[j]) & 0x7FFFFFFFu) - 0x3E000000u + 8u;
           if (((d & 0x1FFFF0u) == 0u) & (d < 0x02B00008u)) {
             uint32_t b = __float_as_uint(__fdiv_rn(fabsf(v[j]), S));
-            if ((b & 0x1FFFFFu) == 0u) b -= 1u;  // |y| >= 0.12 here, so b > 0
+            if (!rne && (b & 0x1FFFFFu) == 0u) b -= 1u;  // |y| >= 0.12 here, so b > 0
             y[j] = __uint_as_float(b | (__float_as_uint(y[j]) & 0x80000000u));
           }
         }
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     mxfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
-                 uint8_t* __restrict__ scales, int layout, int64_t nsf4) {
+                 uint8_t* __restrict__ scales, int layout, int64_t nsf4, bool rne) {
   pdl_wait();  // inputs may come from the previous kernel
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = u < um.units;
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(kThreads)
   uint2 packed = make_uint2(0u, 0u);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const uint32_t c = code_from_bounds(fabsf(v[j]), B, true) | (v[j] < 0.f ? 8u : 0u);
+    const uint32_t c = code_from_bounds(fabsf(v[j]), B, rne) | (v[j] < 0.f ? 8u : 0u);
     if (j < 8) packed.x |= c << (4 * j);
     else packed.y |= c << (4 * (j - 8));
   }
@@ -443,7 +448,7 @@ const T* rows_from(const void* x, int64_t r0, int64_t K) {
 
 q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
                              uint8_t* scales, int layout, const unsigned* amax_bits,
-                             float* tensor_scale, cudaStream_t stream) {
+                             float* tensor_scale, cudaStream_t stream, bool rne) {
   const int64_t nblk = K / 16;
   const int64_t nsf4 = ceil_div(nblk, 4);
   // every byte of an unpadded MMA layout is written by the kernel
@@ -466,16 +471,16 @@ q4_status launch_quant_nvfp4(const void* x, int dtype, int64_t rows, int64_t K, 
     uint8_t* c = codes + r0 * (K / 2);
     const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(um.units, kQUnits), max_ctas);
     if (dtype == Q4_F32)
-      return launch_pdl(nvfp4_kernel<float>, grid, kThreads, ring, stream, rows_from<float>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+      return launch_pdl(nvfp4_kernel<float>, grid, kThreads, ring, stream, rows_from<float>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl, rne);
     else if (dtype == Q4_BF16)
-      return launch_pdl(nvfp4_kernel<__nv_bfloat16>, grid, kThreads, ring, stream, rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+      return launch_pdl(nvfp4_kernel<__nv_bfloat16>, grid, kThreads, ring, stream, rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl, rne);
     else
-      return launch_pdl(nvfp4_kernel<__half>, grid, kThreads, ring, stream, rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl);
+      return launch_pdl(nvfp4_kernel<__half>, grid, kThreads, ring, stream, rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4, amax_bits, tensor_scale, ctl, rne);
   });
 }
 
 q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, uint8_t* codes,
-                             uint8_t* scales, int layout, cudaStream_t stream) {
+                             uint8_t* scales, int layout, cudaStream_t stream, bool rne) {
   const int64_t nblk = K / 16;
   const int64_t nsf4 = ceil_div(K / 32, 4);
   if (layout == Q4_SCALES_MMA && (rows % 128 || (K / 32) % 4))
@@ -485,11 +490,11 @@ q4_status launch_quant_mxfp4(const void* x, int dtype, int64_t rows, int64_t K, 
   return for_row_chunks(rows, nblk, [&](const UnitMap& um, unsigned grid, int64_t r0) {
     uint8_t* c = codes + r0 * (K / 2);
     if (dtype == Q4_F32)
-      return launch_pdl(mxfp4_kernel<float>, grid, kThreads, 0, stream, rows_from<float>(x, r0, K), um, c, scales, layout, nsf4);
+      return launch_pdl(mxfp4_kernel<float>, grid, kThreads, 0, stream, rows_from<float>(x, r0, K), um, c, scales, layout, nsf4, rne);
     else if (dtype == Q4_BF16)
-      return launch_pdl(mxfp4_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4);
+      return launch_pdl(mxfp4_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, rows_from<__nv_bfloat16>(x, r0, K), um, c, scales, layout, nsf4, rne);
     else
-      return launch_pdl(mxfp4_kernel<__half>, grid, kThreads, 0, stream, rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4);
+      return launch_pdl(mxfp4_kernel<__half>, grid, kThreads, 0, stream, rows_from<__half>(x, r0, K), um, c, scales, layout, nsf4, rne);
   });
 }
 

@@ -60,6 +60,9 @@ def test_host_argument_checks(clib):
     assert clib.gemm_w4a16_nvfp4(fake, fake, fake, None, 4, 4, 128, fake, None) == -1
     assert clib.gemm_w4a16_nvfp4(fake, fake, fake + 1, fake, 4, 4, 128, fake, None) == -1
     assert clib.gemm_w4a16_mxfp4(None, fake, fake, 4, 4, 128, fake, None) == -1
+    # an unknown rounding mode
+    assert clib.quantize_mxfp4_ex(fake, 1, 4, 64, fake, fake, 0, 2, None) == -1
+    assert clib.quantize_nvfp4_ex(fake, 1, 4, 64, fake, fake, 0, -1, fake, fake, 256, None) == -1
     # empty problems are no-ops
     assert clib.quantize_int4_g128(None, 1, 0, 128, None, None, None) == 0
     assert clib.gemm_w4a16_int4(None, None, None, 0, 4, 128, None, None, 0, None) == 0

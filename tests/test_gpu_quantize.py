@@ -162,11 +162,12 @@ def _neighbours(c, n=2):
     return out
 
 
-def test_nvfp4_decisions_next_to_midpoints(lib):
+@pytest.mark.parametrize("rounding", ["pages", "rne"])
+def test_nvfp4_decisions_next_to_midpoints(lib, rounding):
     """Values within two ulps of m_k * S, the real numbers whose float32
     quotients by S sit on the E2M1 midpoints, for block scales that are not
     powers of two.  The tensor scale is 1 (tensor amax 2688), so S is the E4M3
-    block scale itself."""
+    block scale itself.  Both tie rules."""
     mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
     s0s = [1.125, 1.375, 2.75, 0.8125, 13.0, 208.0, 0.0390625, 0.001953125 * 5]
     rows = [[2688.0] + [0.0] * 15]
@@ -179,14 +180,15 @@ def test_nvfp4_decisions_next_to_midpoints(lib):
             rows.append(vals + [0.0] * (16 - len(vals)))
     x = np.array(rows, np.float32).reshape(1, -1)
     xd, xh = _dev(x, torch.float32)
-    c, s, g = lib.quantize_nvfp4(xd)
-    oc, os_, og = oracle.quantize_nvfp4(xh)
+    c, s, g = lib.quantize_nvfp4(xd, rounding=rounding)
+    oc, os_, og = oracle.quantize_nvfp4(xh, rounding=rounding)
     assert g.item() == 1.0 == float(og)
     assert np.array_equal(s.cpu().numpy(), os_)
     assert np.array_equal(c.cpu().numpy(), oc)
 
 
-def test_mxfp4_decisions_next_to_midpoints(lib):
+@pytest.mark.parametrize("rounding", ["pages", "rne"])
+def test_mxfp4_decisions_next_to_midpoints(lib, rounding):
     mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
     rows = []
     for e in (-40, -7, 0, 3, 60, 120):
@@ -196,7 +198,39 @@ def test_mxfp4_decisions_next_to_midpoints(lib):
             rows.append(vals + [0.0] * (32 - len(vals)))
     x = np.array(rows, np.float32).reshape(1, -1)
     xd, xh = _dev(x, torch.float32)
-    c, s = lib.quantize_mxfp4(xd)
-    oc, os_ = oracle.quantize_mxfp4(xh)
+    c, s = lib.quantize_mxfp4(xd, rounding=rounding)
+    oc, os_ = oracle.quantize_mxfp4(xh, rounding=rounding)
     assert np.array_equal(s.cpu().numpy(), os_)
     assert np.array_equal(c.cpu().numpy(), oc)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_round_half_even_matches_oracle_on_random_data(lib, fmt, dtype):
+    """rounding="rne" on ordinary data with injected midpoint values (exact
+    ties under MXFP4's power-of-two scales; NVFP4 ties are covered by the
+    midpoint test) and ragged rows, both scale layouts: bit-exact against the
+    oracle."""
+    rows, K = 300, 1024
+    x = workloads.normal(workloads.rng_for(41, 1), (rows, K), 1.0)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    r = np.random.default_rng(42)
+    pick = r.random((rows, K)) < 0.2
+    x[pick] = (mids[r.integers(0, 7, pick.sum())] * np.float32(2.0) ** r.integers(-3, 3, pick.sum())
+               * np.where(r.random(pick.sum()) < 0.5, -1, 1)).astype(np.float32)
+    xd, xh = _dev(x, dtype)
+    for layout in ("rowmajor", "mma"):
+        if fmt == "nvfp4":
+            c, s, _ = lib.quantize_nvfp4(xd, scale_layout=layout, rounding="rne")
+            oc, os_, _ = oracle.quantize_nvfp4(xh, rounding="rne")
+            op = oracle.quantize_nvfp4(xh)[0]
+        else:
+            c, s = lib.quantize_mxfp4(xd, scale_layout=layout, rounding="rne")
+            oc, os_ = oracle.quantize_mxfp4(xh, rounding="rne")
+            op = oracle.quantize_mxfp4(xh)[0]
+        assert np.array_equal(c.cpu().numpy(), oc)
+        if layout == "rowmajor":
+            assert np.array_equal(s.cpu().numpy(), os_)
+    if fmt == "mxfp4":  # power-of-two scales: the injected midpoints are exact ties
+        assert not np.array_equal(oc, op)
+    assert lib.sync_status() == 0
