@@ -11,7 +11,9 @@ pinned host memory and the outputs copied back every step.
 Other workloads (``--workload``): ``decode_nvfp4`` (the decode step with
 NVFP4 weights), ``prefill`` (NVFP4 W4A4, 8192 x 28672 x
 8192, A quantized on the fly), ``moe`` (MXFP4 W4A4, 256 x 2048 x 7168, A
-quantized on the fly), ``grouped`` (64-expert routed NVFP4 MoE), ``tiny``.
+quantized on the fly), ``grouped`` (64-expert routed NVFP4 MoE),
+``quantize`` / ``quantize_rne`` (NVFP4 quantization of the prefill
+activations alone, E2M1 ties to the smaller magnitude / to even), ``tiny``.
 
 ``--impl reference`` times the CPU oracle (the reference arm: a plain, slow
 numpy/FP64 restatement of the method) on a bounded sample of the same
@@ -317,6 +319,90 @@ class DecodeNvfp4(Decode):
             oracle.gemm_w4a16_nvfp4(self.o_a[M], *self.o_w)
 
 
+class QuantizeNvfp4:
+    """NVFP4 quantization of the prefill activations, A bf16 8192 x 8192 into the
+    tensor-core scale layout: the amax pass and the encode pass."""
+    name = "nvfp4_quantize"
+    unit = "GB/s"
+    bound = "hbm"
+    default_steps = 2000
+    kernel = "amax_kernel + nvfp4_kernel"
+    rounding = "pages"
+    M = K = 8192
+    launches_per_step = 2
+    kernel_launches = 2
+
+    def config(self):
+        return {"workload": f"nvfp4_quantize A bf16 {self.M}x{self.K} (the prefill activations) -> codes + "
+                            f"MMA-layout E4M3 scales + tensor scale, E2M1 ties: {self.rounding}",
+                "M": self.M, "K": self.K, "l2": "input larger than L2 (134 MB)"}
+
+    def setup(self, q4, dev, seed, shape=None):
+        self.q4 = q4
+        if shape:
+            self.M, self.K = shape[0], shape[-1]
+        a = workloads.prefill_activations(seed, self.M, self.K)
+        self.x_host = a.float().numpy()
+        self.x = a.to(dev)
+        self.codes = torch.empty((self.M, self.K // 2), dtype=torch.uint8, device=dev)
+        self.sf = torch.empty(q4.mma_scales_bytes(self.M, self.K // 16), dtype=torch.uint8, device=dev)
+        self.g = torch.empty(1, dtype=torch.float32, device=dev)
+        self.ws = q4.workspace(q4.OP_QUANTIZE_NVFP4, self.M, 0, self.K, dev)
+        self.x_pin = a.pin_memory()
+        self.c_host = torch.empty_like(self.codes, device="cpu").pin_memory()
+        self.sf_host = torch.empty_like(self.sf, device="cpu").pin_memory()
+        self.h2d = self.M * self.K * 2
+        self.d2h = self.codes.numel() + self.sf.numel()
+
+    def step(self, i):
+        rc = self.q4.lib().quantize_nvfp4_ex(
+            self.x.data_ptr(), 1, self.M, self.K, self.codes.data_ptr(), self.sf.data_ptr(), 1,
+            1 if self.rounding == "rne" else 0, self.g.data_ptr(), self.ws.data_ptr(),
+            self.ws.numel(), torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+
+    kernel_only = step
+
+    def units_per_step(self):
+        # x read twice (the tensor scale needs the whole tensor's amax before any
+        # element is encoded, and x is larger than L2), codes and scales written
+        return 2 * self.M * self.K * 2 + self.M * self.K // 2 + self.M * self.K // 16
+
+    kernel_units = units_per_step
+
+    def flops_per_step(self):
+        return 0.0
+
+    def e2e_step(self, i):
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.step(i)
+        self.c_host.copy_(self.codes, non_blocking=True)
+        self.sf_host.copy_(self.sf, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def oracle_prepare(self, rows):
+        self.o_rows = rows
+        self.o_x = np.ascontiguousarray(self.x_host[:rows])
+
+    def oracle_step(self):
+        import oracle
+        oracle.quantize_nvfp4(self.o_x, rounding=self.rounding)
+
+    def oracle_units(self):
+        return 2 * self.o_rows * self.K * 2 + self.o_rows * self.K // 2 + self.o_rows * self.K // 16
+
+    def oracle_sample_text(self):
+        return (f"the first {self.o_rows} rows as their own tensor (amax, E4M3 block scales, "
+                f"E2M1 codes, ties: {self.rounding})")
+
+    oracle_grain = 64
+
+
+class QuantizeNvfp4Rne(QuantizeNvfp4):
+    name = "nvfp4_quantize_rne"
+    rounding = "rne"
+
+
 class W4A4:
     """W4A4 GEMM with A quantized on the fly; B pre-quantized (MMA scale layout)."""
     nvfp4 = True
@@ -544,9 +630,10 @@ class Grouped:
 
 
 WORKLOADS = {"decode": Decode, "decode_nvfp4": DecodeNvfp4, "prefill": Prefill, "moe": Moe,
-             "grouped": Grouped}
+             "grouped": Grouped, "quantize": QuantizeNvfp4, "quantize_rne": QuantizeNvfp4Rne}
 DTYPES = {"decode": "bf16 (exact int4 values) x bf16 -> fp32",
           "decode_nvfp4": "bf16 (exact e2m1 x e4m3 values) x bf16 -> fp32",
+          "quantize": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)", "quantize_rne": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)",
           "prefill": "e2m1 x e2m1 -> fp32",
           "moe": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32"}
 
@@ -617,6 +704,8 @@ def wl_setup_host(wl, seed):
         wl.w_host = workloads.int4_weights(wl.N, wl.K, seed)
         wl.A_host = {M: workloads.to_bf16(workloads.normal(workloads.rng_for(seed, 1), (M, wl.K), 1.0))
                      for M in wl.Ms}
+    elif isinstance(wl, QuantizeNvfp4):
+        wl.x_host = workloads.prefill_activations(seed, wl.M, wl.K).float().numpy()
     elif isinstance(wl, Grouped):
         tok, _, offs, rt = workloads.grouped(seed, T=wl.T, E=wl.E, N=wl.N, K=wl.K, top_k=wl.top,
                                              experts=False)
@@ -630,7 +719,8 @@ def wl_setup_host(wl, seed):
 
 SEEDS = {"decode": workloads.SEED_BASE + 2, "decode_nvfp4": workloads.SEED_BASE + 2,
          "moe": workloads.SEED_BASE + 3,
-         "prefill": workloads.SEED_BASE + 4, "grouped": workloads.SEED_BASE + 5}
+         "prefill": workloads.SEED_BASE + 4, "grouped": workloads.SEED_BASE + 5,
+         "quantize": workloads.SEED_BASE + 4, "quantize_rne": workloads.SEED_BASE + 4}
 
 
 def main():

@@ -164,7 +164,7 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 // The pages' rule is y = x / S in float32 (rounded to nearest), clamped to
 // [-6, 6], then rounded to the nearest E2M1 value with ties to the smaller
 // magnitude.  Here:
-//  * y0 = |x| * RN(1/S) is within 1.5 ulp of |x| / S.  The E2M1 decision
+//  * y0 = |x| * R, with R within 1 ulp of 1/S, is within 2.5 ulp of |x| / S.  The E2M1 decision
 //    points t_k in {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5} have three
 //    significant bits, so when y0 is more than 8 ulp away from every float
 //    with three significant bits, RN(|x| / S) and y0 lie strictly inside the
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   constexpr uint32_t kTileBytes = kQUnits * 16 * sizeof(T);
   extern __shared__ __align__(128) uint8_t qring[];  // [kQStages][kTileBytes]
   __shared__ __align__(8) uint64_t full[kQStages];
-  __shared__ float s_g;
+  __shared__ float s_g, s_c6g;
   __shared__ int s_abort;
   const uint32_t ntiles = (um.units + kQUnits - 1) / kQUnits;
   const uint32_t tid = threadIdx.x;
@@ -214,11 +214,12 @@ __global__ void __launch_bounds__(kThreads, 4)
     fence_mbar_init();
     // per-tensor scale g = max(amax_t, 1e-12) / (448 * 6), once per CTA
     s_g = __fdiv_rn(fmaxf(__uint_as_float(*amax_bits), 1e-12f), 2688.0f);
+    s_c6g = __frcp_rn(__fmul_rn(6.0f, s_g));  // 1 / (6 g) within 1 ulp
     s_abort = 0;
     for (uint32_t i = 0; i + 1 < kQStages; ++i) issue(i);
   }
   __syncthreads();
-  const float g = s_g;
+  const float g = s_g, c6g = s_c6g;
 
   uint32_t i = 0;
   for (; tile_of(i) < ntiles; ++i) {
@@ -255,14 +256,21 @@ __global__ void __launch_bounds__(kThreads, 4)
     for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
 
     // block scale: E4M3 of (amax_b / 6) / g, round to nearest even
-    const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+    // t = RN(RN(amax / 6) / g) matters only through its E4M3 rounding.  ta =
+    // amax * RN(1 / RN(6 g)) is within 5 ulp of t, and the E4M3 rounding cells
+    // (normal, subnormal and the saturation edge) are bounded by floats with at
+    // most 5 significant bits; unless ta is within 8 ulp of such a float, t and
+    // ta round to the same E4M3 value.  Otherwise t is computed as defined.
+    float t = __fmul_rn(amax, c6g);
+    if (((__float_as_uint(t) + 8u) & 0x7FFF0u) == 0u) t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
     const __nv_fp8_storage_t bs = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
     const float bsf = __half2float(__half(__nv_cvt_fp8_to_halfraw(bs, __NV_E4M3)));
     const float S = __fmul_rn(fmaxf(bsf, 1e-12f), g);
 
     uint2 packed = make_uint2(0u, 0u);
     if (bs != 0) {
-      const float R = __frcp_rn(S);
+      float R;  // 1 / S within 1 ulp (S is a normal float: e4m3 >= 2^-9, g > 3e-16)
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(R) : "f"(S));
       // y = x * R + 0 rounds once like x * R, keeps the sign of a negative x
       // (so its code carries the sign bit even when its magnitude rounds to 0)
       // and turns x = -0 into +0, whose code is 0.

@@ -187,6 +187,28 @@ def test_nvfp4_decisions_next_to_midpoints(lib, rounding):
     assert np.array_equal(c.cpu().numpy(), oc)
 
 
+def test_nvfp4_block_scales_next_to_e4m3_midpoints(lib):
+    """Blocks whose t = (amax / 6) / g lies within a few ulp of an E4M3
+    rounding boundary -- every midpoint between consecutive E4M3 values,
+    subnormal ones included -- with g = 1 (tensor amax 2688): scale bytes and
+    codes match the oracle bit for bit.  (t cannot pass 448: a block's amax is
+    at most the tensor's, 2688 g.)"""
+    from oracle import formats as F
+    vals = np.unique(F.e4m3_decode(np.arange(0, 127)))
+    mids = (vals[1:] + vals[:-1]) / 2
+    rows = [[2688.0] + [0.0] * 15]
+    for m in mids:
+        for a in _neighbours(6.0 * m, 4):
+            rows.append([float(a), -0.5 * float(a)] + [0.0] * 14)
+    x = np.array(rows, np.float32).reshape(1, -1)
+    xd, xh = _dev(x, torch.float32)
+    c, s, g = lib.quantize_nvfp4(xd)
+    oc, os_, og = oracle.quantize_nvfp4(xh)
+    assert g.item() == 1.0 == float(og)
+    assert np.array_equal(s.cpu().numpy(), os_)
+    assert np.array_equal(c.cpu().numpy(), oc)
+
+
 @pytest.mark.parametrize("rounding", ["pages", "rne"])
 def test_mxfp4_decisions_next_to_midpoints(lib, rounding):
     mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]

@@ -28,7 +28,8 @@ import numpy as np
 
 __all__ = [
     "WORKED_ROW", "SEED_BASE", "rng_for", "normal", "add_entry_outliers",
-    "scale_channels", "to_bf16", "tiny", "decode", "moe", "prefill", "grouped",
+    "scale_channels", "to_bf16", "tiny", "decode", "moe", "prefill", "prefill_activations",
+    "grouped",
     "route_top_k", "nvfp4_pair", "mxfp4_pair", "int4_weights",
 ]
 
@@ -139,12 +140,19 @@ def moe(seed: int = SEED_BASE + 3, M: int = 256, N: int = 2048, K: int = 7168):
     return to_bf16(a), b
 
 
-def prefill(seed: int = SEED_BASE + 4, M: int = 8192, N: int = 28672, K: int = 8192):
-    """bf16 A [M, K] (torch) and float32 B [N, K] (numpy)."""
+def prefill_activations(seed: int = SEED_BASE + 4, M: int = 8192, K: int = 8192):
+    """The prefill activations alone: bf16 [M, K] (torch), N(0, 1) with 0.5% of
+    the channels scaled by 20."""
     a = normal(rng_for(seed, 1), (M, K), 1.0)
     scale_channels(rng_for(seed, 5), a)
+    return to_bf16(a)
+
+
+def prefill(seed: int = SEED_BASE + 4, M: int = 8192, N: int = 28672, K: int = 8192):
+    """bf16 A [M, K] (torch) and float32 B [N, K] (numpy)."""
+    a = prefill_activations(seed, M, K)
     b = normal(rng_for(seed, 2), (N, K), 0.02)
-    return to_bf16(a), b
+    return a, b
 
 
 def route_top_k(T: int, E: int, top_k: int, seed: int, bias_std: float = 0.2,
