@@ -58,6 +58,8 @@ NCU_TRAFFIC = {
     "prefill": 1001.2e6,
     # split-K fp4_gemm_kernel at 256 x 2048 x 7168 (C stays in L2)
     "moe": 8.81e6,
+    # w4a16_kernel<NVFP4>, mean over the M = 1, 4, 16 launches at N = K = 8192
+    "decode_nvfp4": 37.94e6,
 }
 
 
