@@ -36,7 +36,7 @@
 namespace q4 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of codes)
+constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of codes); BN: widest N tile
 constexpr int kMaxStages = 5;
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
 constexpr int kWriterThreads = 128;    // 4 scale-writer warps
@@ -44,12 +44,9 @@ constexpr int kWriterWarp0 = (kThreads + kWriterThreads) / 32 - 4;  // warps 6-9
 template <bool GROUPED>
 constexpr int block_threads() { return kThreads + kWriterThreads; }
 constexpr uint32_t kABytes = BM * BK / 2;     // 16 KiB
-constexpr uint32_t kBBytes = BN * BK / 2;     // 32 KiB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = BN;             // 256 FP32 columns
-constexpr uint32_t kSfColsPerStage = 48;      // 16 (A) + 32 (B)
+constexpr uint32_t kSfColsPerStage = 48;      // 16 (A) + 32 (B: two 128-row chunks)
 constexpr int kMaxExperts = 1024;
-constexpr int kPartStride = BN + 4;  // FP32 partial tile row stride (split-K), padded against bank conflicts
 
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank) {
   uint32_t ra;
@@ -64,9 +61,13 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank
 
 // Stage: [A codes | B codes (all BN rows, or this CTA's half in pairs) |
 // A scales (128 rows) | B scales (256 rows)]
-template <bool NV, bool P2 = false>
+// BNT: N tile width (256; 128 for split-K on few output tiles).
+template <bool NV, bool P2 = false, int BNT = BN>
 struct Cfg {
-  static constexpr int kStages = P2 ? 5 : 4;
+  static constexpr uint32_t kBBytes = BNT * BK / 2;
+  static constexpr uint32_t kAccCols = BNT;   // FP32 accumulator columns
+  static constexpr int kPartStride = BNT + 4;  // FP32 partial tile row stride (split-K), padded against bank conflicts
+  static constexpr int kStages = P2 ? 5 : (BNT == 128 ? 5 : 4);
   static constexpr uint32_t kSfaBytes = NV ? 2048u : 1024u;  // 128 rows x (16 | 8) scales
   static constexpr uint32_t kSfbBytes = 2 * kSfaBytes;        // 256 rows
   static constexpr uint32_t kBLoad = P2 ? kBBytes / 2 : kBBytes;
@@ -79,7 +80,8 @@ struct Cfg {
 static_assert(Cfg<true>::kStageBytes % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0, "");
 static_assert(Cfg<true, true>::kStageBytes % 1024 == 0 && Cfg<false, true>::kStageBytes % 1024 == 0, "");
 static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<true, true>::kSmemBytes <= 232448, "shared memory");
-static_assert(kAccCols + kMaxStages * kSfColsPerStage <= kTmemCols, "TMEM columns");
+static_assert(BN + kMaxStages * kSfColsPerStage <= kTmemCols, "TMEM columns");
+static_assert(Cfg<true, false, 128>::kSmemBytes <= 232448 && Cfg<false, false, 128>::kStageBytes % 1024 == 0, "");
 
 struct Smem {
   uint64_t full[kMaxStages];
@@ -111,6 +113,7 @@ struct Params {
   void* C;
   int c_dtype;
   int num_m, num_n;       // dense tile counts
+  int bn;                 // N tile width (the kernel's BNT)
   // grouped
   const int32_t* offsets;
   const int32_t* sched;
@@ -135,7 +138,7 @@ __device__ __forceinline__ TileInfo dense_tile(const Params& p, int t, int crank
   const int m = mg * CM + crank;
   ti.m_row0 = m * BM;
   ti.m_end = (int)p.M;
-  ti.n0 = n * BN;
+  ti.n0 = n * p.bn;
   ti.sf_block = m;
   ti.e = 0;
   ti.ok = true;
@@ -153,7 +156,7 @@ __device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sch
   ti.e = e;
   ti.m_row0 = __ldg(p.offsets + e) + (tr - sched[e]) * BM;
   ti.m_end = __ldg(p.offsets + e + 1);
-  ti.n0 = n * BN;
+  ti.n0 = n * p.bn;
   ti.sf_block = tr;
   ti.ok = ti.m_row0 < ti.m_end;
   return ti;
@@ -163,11 +166,14 @@ __device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sch
 // KS > 1: split-K -- a cluster of KS CTAs owns one output tile, each CTA a
 // slice of the K blocks; the FP32 partial tiles are reduced through
 // distributed shared memory in rank order (deterministic).
-template <bool NV, bool GROUPED, int KS = 1, bool P2 = false>
+template <bool NV, bool GROUPED, int KS = 1, bool P2 = false, int BNT = BN>
 __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-  using C_ = Cfg<NV, P2>;
+  using C_ = Cfg<NV, P2, BNT>;
+  static_assert(BNT == BN || (BNT == 128 && !P2), "N tile: 256, or 128 without pairs");
+  constexpr uint32_t kAccCols = C_::kAccCols;
+  constexpr int kPartStride = C_::kPartStride;
   constexpr int kStages = C_::kStages;
   extern __shared__ uint8_t smem_raw[];
   pdl_wait();  // operands, scales and the schedule may come from the previous kernel
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const uint8_t* sfa = p.a_sf + (int64_t)ti.sf_block * nsf4_a * 512;
       const uint8_t* sfb = p.b_sf + (int64_t)ti.e * p.b_sf_expert_bytes;
       const int nb0 = ti.n0 / 128;
-      const bool b_hi = nb0 + 1 < nblk_b;
+      const bool b_hi = BNT > 128 && nb0 + 1 < nblk_b;  // the tile's second 128 B rows exist
       const uint32_t bytes = kABytes + C_::kBLoad + (a_sf_ok ? C_::kSfaBytes : 0u) +
                              C_::kSfaBytes * (b_hi ? 2 : 1);
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
           const uint32_t sfb_s = smem_u32(st + C_::kSfbOff);
           // B codes: the whole tile, or this CTA's 128-row half of the pair's tile
           tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2),
-                      b_row + (P2 ? crank * (BN / 2) : 0), full);
+                      b_row + (P2 ? crank * (BNT / 2) : 0), full);
           bulk_load(sfb_s, sfb0, C_::kSfaBytes, full);
           if (b_hi) bulk_load(sfb_s + C_::kSfaBytes, sfb0 + nsf4_a * 512, C_::kSfaBytes, full);
         }
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
             const uint64_t bd = smem_desc(st + kABytes + 32 * k, 16, 1024, 2);
             const uint32_t j = NV ? k : k >> 1;
             const uint32_t sf_id = NV ? 0u : (k & 1) * 2;
-            const uint32_t idesc = fp4_idesc(BM * TM, BN, !NV, sf_id, sf_id);
+            const uint32_t idesc = fp4_idesc(BM * TM, BNT, !NV, sf_id, sf_id);
             const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
             if constexpr (P2)
               tc_mma_fp4_pair<NV ? 4 : 2>(tmem, ad, bd, idesc, sf_t + 4 * j, sf_t + 16 + 8 * j, acc);
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         float* part = reinterpret_cast<float*>(smem) + (q * 32 + lane) * kPartStride;
         const bool has_k = kb_end > kb_begin;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN / 32; c0 += 4) {  // four 32-column loads per TMEM wait
+        for (int c0 = 0; c0 < BNT / 32; c0 += 4) {  // four 32-column loads per TMEM wait
           uint32_t r[4][32];
 #pragma unroll
           for (int g = 0; g < 4; ++g)
@@ -468,12 +474,12 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       // scaled and stored.
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN / 32; c0 += 4) {
+      for (int c0 = 0; c0 < BNT / 32; c0 += 4) {
         uint32_t r[4][32];
 #pragma unroll
         for (int g = 0; g < 4; ++g) tmem_ld_32x32b_x32(t_row + (c0 + g) * 32, r[g]);
         tmem_ld_wait();
-        if (c0 + 4 >= BN / 32) {  // every accumulator column is in registers
+        if (c0 + 4 >= BNT / 32) {  // every accumulator column is in registers
           tc_fence_before();
           __syncwarp();
           if (lane == 0) arrive_leader(&sm->acc_empty);
@@ -505,7 +511,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const int rows = (BM + KS - 1) / KS;
       const int r_lo = krank * rows, r_hi = min(BM, r_lo + rows);
       const uint32_t base = smem_u32(smem);
-      const int items = (r_hi - r_lo) * (BN / 4);
+      const int items = (r_hi - r_lo) * (BNT / 4);
       // kBatch items per thread per round: all their remote loads are in flight
       // together, so a round costs one distributed-shared-memory round trip
       constexpr int kBatch = 4;
@@ -514,7 +520,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
           const int e = e0 + b * blockDim.x;
-          const int r = r_lo + (e < items ? e : 0) / (BN / 4), c4 = (e < items ? e : 0) % (BN / 4);
+          const int r = r_lo + (e < items ? e : 0) / (BNT / 4), c4 = (e < items ? e : 0) % (BNT / 4);
           const uint32_t off = (uint32_t)(r * kPartStride + 4 * c4) * 4u;
 #pragma unroll
           for (int qq = 0; qq < KS; ++qq)  // this CTA's own partial by a plain shared load
@@ -525,7 +531,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         for (int b = 0; b < kBatch; ++b) {
           const int e = e0 + b * blockDim.x;
           if (e >= items) break;
-          const int r = r_lo + e / (BN / 4), c4 = e % (BN / 4);
+          const int r = r_lo + e / (BNT / 4), c4 = e % (BNT / 4);
           float4 sum = v[b][0];
 #pragma unroll
           for (int qq = 1; qq < KS; ++qq) {
@@ -644,15 +650,15 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <bool NV, bool GROUPED, int KS = 1, bool P2 = false>
+template <bool NV, bool GROUPED, int KS = 1, bool P2 = false, int BNT = BN>
 q4_status set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!done[dev]) {
-    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, KS, P2>,
+    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, KS, P2, BNT>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)Cfg<NV, P2>::kSmemBytes));
+                                     (int)Cfg<NV, P2, BNT>::kSmemBytes));
     done[dev] = 1;
   }
   return Q4_OK;
@@ -701,17 +707,18 @@ q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Param
 
 // Split-K for problems with few output tiles: KS CTAs (one cluster) per tile,
 // launched as exactly tiles x KS CTAs (one tile per cluster).
-template <bool NV, int KS>
+template <bool NV, int KS, int BNT>
 q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                         cudaStream_t stream) {
-  static_assert(KS * 0 + (BM * (BN + 4) * 4) <= Cfg<NV>::kStages * Cfg<NV>::kStageBytes, "partial tile fits");
+  using C_ = Cfg<NV, false, BNT>;
+  static_assert(KS * 0 + (BM * C_::kPartStride * 4) <= C_::kStages * C_::kStageBytes, "partial tile fits");
   q4_status st;
-  if ((st = set_smem_attr<NV, false, KS>()) != Q4_OK) return st;
+  if ((st = set_smem_attr<NV, false, KS, false, BNT>()) != Q4_OK) return st;
   const int tiles = p.num_m * p.num_n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * KS), 1, 1);
   cfg.blockDim = dim3(block_threads<false>(), 1, 1);
-  cfg.dynamicSmemBytes = Cfg<NV>::kSmemBytes;
+  cfg.dynamicSmemBytes = C_::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -724,21 +731,17 @@ q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Para
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, KS>, ta, tb, p));
+  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, KS, false, BNT>, ta, tb, p));
   return Q4_OK;
 }
 
-template <bool NV>
+template <bool NV, int BNT>
 q4_status dispatch_splitk(int ks, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                           cudaStream_t stream) {
-  switch (ks) {
-    case 2: return launch_splitk<NV, 2>(ta, tb, p, stream);
-    case 3: return launch_splitk<NV, 3>(ta, tb, p, stream);
-    case 4: return launch_splitk<NV, 4>(ta, tb, p, stream);
-    case 5: return launch_splitk<NV, 5>(ta, tb, p, stream);
-    case 6: return launch_splitk<NV, 6>(ta, tb, p, stream);
-    case 7: return launch_splitk<NV, 7>(ta, tb, p, stream);
-    default: return launch_splitk<NV, 8>(ta, tb, p, stream);
+  switch (ks) {  // 2 <= ks <= 4
+    case 2: return launch_splitk<NV, 2, BNT>(ta, tb, p, stream);
+    case 3: return launch_splitk<NV, 3, BNT>(ta, tb, p, stream);
+    default: return launch_splitk<NV, 4, BNT>(ta, tb, p, stream);
   }
 }
 
@@ -756,19 +759,32 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   p.a_sf = a.a_scales; p.b_sf = a.b_scales; p.b_sf_expert_bytes = 0;
   p.a_g = a.a_g; p.b_g = a.b_g;
   p.C = a.C; p.c_dtype = a.c_dtype;
-  p.num_m = (int)ceil_div(a.M, BM); p.num_n = (int)ceil_div(a.N, BN);
+  p.num_m = (int)ceil_div(a.M, BM); p.num_n = (int)ceil_div(a.N, BN); p.bn = BN;
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
-  // few output tiles: split K over a cluster so that the grid fills the GPU.
-  // At most 4 CTAs per cluster: measured on GB300 (256 x 2048 x 7168,
-  // 128 x 4096 x 8192) 4 is fastest and 8 is slower than no split, since
-  // clusters of 8 one-CTA-per-SM blocks are not all resident at once.
-  const int tiles = p.num_m * p.num_n, nkb = (int)(a.K / BK);
+  // few output tiles: split K over a cluster so that the grid fills the GPU,
+  // on 128-wide N tiles when there are few enough of them (twice the tiles,
+  // half the bytes and half the partial tile per CTA).  At most 4 CTAs per
+  // cluster: measured on GB300 (256 x 2048 x 7168, 128 x 4096 x 8192) 4 is
+  // fastest and 8 is slower than no split, since clusters of 8
+  // one-CTA-per-SM blocks are not all resident at once.
+  const int nkb = (int)(a.K / BK);
+  const int tiles128 = p.num_m * (int)ceil_div(a.N, 128), tiles = p.num_m * p.num_n;
+  if (tiles128 * 2 <= num_sms() && nkb >= 2) {
+    const int ks = std::min(4, std::min(num_sms() / tiles128, nkb));
+    CUtensorMap tb128;
+    if ((st = make_tmap_2d_u8(&tb128, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, 128, true)) != Q4_OK) return st;
+    Params p128 = p;
+    p128.num_n = (int)ceil_div(a.N, 128);
+    p128.bn = 128;
+    return a.nvfp4 ? dispatch_splitk<true, 128>(ks, ta, tb128, p128, stream)
+                   : dispatch_splitk<false, 128>(ks, ta, tb128, p128, stream);
+  }
   if (tiles * 2 <= num_sms() && nkb >= 2) {
     const int ks = std::min(4, std::min(num_sms() / tiles, nkb));
     if (ks >= 2)
-      return a.nvfp4 ? dispatch_splitk<true>(ks, ta, tb, p, stream)
-                     : dispatch_splitk<false>(ks, ta, tb, p, stream);
+      return a.nvfp4 ? dispatch_splitk<true, BN>(ks, ta, tb, p, stream)
+                     : dispatch_splitk<false, BN>(ks, ta, tb, p, stream);
   }
   // CTA pairs (2-SM MMA on 256x256 tiles) whenever M spans two tiles: each SM
   // then receives half of each B tile
@@ -816,7 +832,7 @@ q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream) {
   p.b_sf_expert_bytes = (int64_t)mma_scales_bytes(a.N, a.K / 16);
   p.a_g = a.a_g; p.b_g = a.w_g;
   p.C = a.C; p.c_dtype = Q4_BF16;
-  p.num_m = 0; p.num_n = (int)ceil_div(a.N, BN);
+  p.num_m = 0; p.num_n = (int)ceil_div(a.N, BN); p.bn = BN;
   p.offsets = a.offsets; p.sched = a.sched; p.E = a.E;
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();

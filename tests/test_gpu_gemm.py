@@ -14,7 +14,7 @@ from tests._util import assert_gemm_close
 pytestmark = pytest.mark.gpu
 
 W4A4_SHAPES = [(16, 256, 512), (1, 256, 256), (130, 300, 768), (257, 520, 1024),
-               (128, 256, 4096), (2048, 4096, 256), (300, 1000, 512)]
+               (128, 256, 4096), (2048, 4096, 256), (300, 1000, 512), (1000, 2048, 1024)]
 
 
 def _nv_pair(M, N, K, seed):
