@@ -676,12 +676,13 @@ def run_reference(args, dist):
     wl_setup_host(wl, args.seed)
     K = args.steps or wl.default_steps
     W = max(3, args.warmup)
-    # size the per-step sample so that the whole run takes about two minutes
+    # size the per-step sample so that the whole run takes about --reference-seconds
+    # (two minutes by default)
     wl.oracle_prepare(wl.oracle_grain)
     t0 = time.perf_counter()
     wl.oracle_step()
     t1 = time.perf_counter() - t0
-    grains = max(1, int(120.0 / max((K + W) * t1, 1e-9)))
+    grains = max(1, int(args.reference_seconds / max((K + W) * t1, 1e-9)))
     wl.oracle_prepare(wl.oracle_grain * min(grains, 64))
     for _ in range(W):
         wl.oracle_step()
@@ -734,6 +735,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="--impl reference: about how long the whole run takes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default=None,
                     help="M,N,K override (a smaller case of the same code path, e.g. for profiling)")
