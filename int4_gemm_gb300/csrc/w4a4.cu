@@ -8,10 +8,14 @@
 //
 // Structure (one persistent CTA per SM; on large problems the CTAs work in
 // pairs, see P2 below):
-//   warp 0     producer: TMA tiles of packed codes (128-byte swizzle) and bulk
-//              copies of the scale tiles into a 4-stage shared-memory ring.
+//   warp 0     code producer: TMA tiles of packed codes (128-byte swizzle)
+//              into a 4- or 5-stage shared-memory ring.
+//   warp 10    scale producer: bulk copies of the stage's scale tiles into the
+//              same stage (its own arrival on the stage's barrier), so the
+//              two producers issue their copies in parallel (prefill GEMM
+//              656 -> 634 us against one producer issuing all of them).
 //   warp 1     allocates TMEM; one lane issues tcgen05.mma ... block_scale,
-//              128x256x64 per instruction, FP32 accumulation in TMEM.
+//              128xBNTx64 per instruction, FP32 accumulation in TMEM.
 //   warps 2-5  epilogue: tcgen05.ld of the 128x256 FP32 accumulator, times
 //              gA * gB (NVFP4), rounded to bf16 (or kept FP32), stored.
 //   warps 6-9  scale writers: each stage's scale tiles go from shared memory
@@ -38,11 +42,11 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 256;   // BK in elements (128 bytes of codes); BN: widest N tile
 constexpr int kMaxStages = 5;
-constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
+constexpr int kThreads = 192;          // code producer, MMA, 4 epilogue warps
 constexpr int kWriterThreads = 128;    // 4 scale-writer warps
 constexpr int kWriterWarp0 = (kThreads + kWriterThreads) / 32 - 4;  // warps 6-9
 template <bool GROUPED>
-constexpr int block_threads() { return kThreads + kWriterThreads; }
+constexpr int block_threads() { return kThreads + kWriterThreads + 32; }  // + the scale producer warp
 constexpr uint32_t kABytes = BM * BK / 2;     // 16 KiB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfColsPerStage = 48;      // 16 (A) + 32 (B: two 128-row chunks)
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->full[s]), 2);  // code producer + scale producer
       mbar_init(smem_u32(&sm->empty[s]), 1);
       mbar_init(smem_u32(&sm->sf_full[s]), P2 ? 8 : 4);  // one arrival per scale-writer warp
     }
@@ -252,18 +256,10 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     uint32_t issued_phase[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
     bool alive = true;
-    const int nsf4_a = (int)((p.K / (NV ? 16 : 32) + 3) / 4);
-    const int nblk_b = (int)((p.N + 127) / 128);
     for (int t = cid; t < total_tiles && alive; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
-      const bool a_sf_ok = ti.sf_block < (GROUPED ? (1 << 30) : p.num_m);  // a CTA past M loads no scales
-      const uint8_t* sfa = p.a_sf + (int64_t)ti.sf_block * nsf4_a * 512;
-      const uint8_t* sfb = p.b_sf + (int64_t)ti.e * p.b_sf_expert_bytes;
-      const int nb0 = ti.n0 / 128;
-      const bool b_hi = BNT > 128 && nb0 + 1 < nblk_b;  // the tile's second 128 B rows exist
-      const uint32_t bytes = kABytes + C_::kBLoad + (a_sf_ok ? C_::kSfaBytes : 0u) +
-                             C_::kSfaBytes * (b_hi ? 2 : 1);
+      const uint32_t bytes = kABytes + C_::kBLoad;
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
         if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
@@ -276,15 +272,9 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
           mbar_arrive_expect_tx(full, bytes);
           // A rows: the tile's rows (grouped: rows of the routed copy of the codes)
           tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
-          const int64_t jsf = (int64_t)kb * C_::kSfChunks * 512;
-          if (a_sf_ok) bulk_load(smem_u32(st + C_::kSfaOff), sfa + jsf, C_::kSfaBytes, full);
-          const uint8_t* sfb0 = sfb + (int64_t)nb0 * nsf4_a * 512 + jsf;
-          const uint32_t sfb_s = smem_u32(st + C_::kSfbOff);
           // B codes: the whole tile, or this CTA's 128-row half of the pair's tile
           tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2),
                       b_row + (P2 ? crank * (BNT / 2) : 0), full);
-          bulk_load(sfb_s, sfb0, C_::kSfaBytes, full);
-          if (b_hi) bulk_load(sfb_s + C_::kSfaBytes, sfb0 + nsf4_a * 512, C_::kSfaBytes, full);
         }
         issued[stage] = 1;
         issued_phase[stage] = phase;
@@ -391,6 +381,52 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         if (++stage == kStages) stage = 0, phase ^= 1;
       }
     }
+  } else if (warp == kWriterWarp0 + 4) {
+    // ------------------------------------------------------------ scale producer
+    // (the same walk over tiles and stages as the code producer)
+    uint32_t stage = 0, phase = 0;
+    int issued[kStages];
+    uint32_t issued_phase[kStages];
+    for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
+    bool alive = true;
+    const int nsf4_a = (int)((p.K / (NV ? 16 : 32) + 3) / 4);
+    const int nblk_b = (int)((p.N + 127) / 128);
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
+      const TileInfo ti = tile_at(t);
+      if (!ti.ok) continue;
+      const bool a_sf_ok = ti.sf_block < (GROUPED ? (1 << 30) : p.num_m);  // a CTA past M loads no scales
+      const uint8_t* sfa = p.a_sf + (int64_t)ti.sf_block * nsf4_a * 512;
+      const uint8_t* sfb = p.b_sf + (int64_t)ti.e * p.b_sf_expert_bytes;
+      const int nb0 = ti.n0 / 128;
+      const bool b_hi = BNT > 128 && nb0 + 1 < nblk_b;  // the tile's second 128 B rows exist
+      const uint32_t bytes = (a_sf_ok ? C_::kSfaBytes : 0u) + C_::kSfaBytes * (b_hi ? 2 : 1);
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint8_t* st = smem + stage * C_::kStageBytes;
+        const uint32_t full = smem_u32(&sm->full[stage]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, bytes);
+          const int64_t jsf = (int64_t)kb * C_::kSfChunks * 512;
+          if (a_sf_ok) bulk_load(smem_u32(st + C_::kSfaOff), sfa + jsf, C_::kSfaBytes, full);
+          const uint8_t* sfb0 = sfb + (int64_t)nb0 * nsf4_a * 512 + jsf;
+          const uint32_t sfb_s = smem_u32(st + C_::kSfbOff);
+          bulk_load(sfb_s, sfb0, C_::kSfaBytes, full);
+          if (b_hi) bulk_load(sfb_s + C_::kSfaBytes, sfb0 + nsf4_a * 512, C_::kSfaBytes, full);
+        }
+        issued[stage] = 1;
+        issued_phase[stage] = phase;
+        if (++stage == kStages) stage = 0, phase ^= 1;
+      }
+    }
+    if (lane == 0) {
+      KernelCtl drain = p.ctl;
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
