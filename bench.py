@@ -54,10 +54,10 @@ NCU_TRAFFIC = {
     # w4a16_kernel, mean over the M = 1, 4, 16 launches at N = K = 8192
     "decode": 34.76e6,
     # fp4_gemm_kernel (CTA pairs) at 8192 x 28672 x 8192, mean of 3 launches
-    # (568 MB read: A and B tiles re-read from DRAM ~3.3x; 433 MB written)
-    "prefill": 1001.2e6,
-    # split-K fp4_gemm_kernel at 256 x 2048 x 7168 (C stays in L2)
-    "moe": 8.81e6,
+    # (235 MB read: A and B once each, scales; 435 MB of C written)
+    "prefill": 670.0e6,
+    # split-K fp4_gemm_kernel (128-wide tiles) at 256 x 2048 x 7168 (C stays in L2)
+    "moe": 8.82e6,
     # w4a16_kernel<NVFP4>, mean over the M = 1, 4, 16 launches at N = K = 8192
     "decode_nvfp4": 37.94e6,
 }
