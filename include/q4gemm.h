@@ -298,6 +298,13 @@ const char* q4_status_string(q4_status s);
  * launch. */
 int q4_set_wait_timeout_ms(int ms);
 
+/* Diagnostic: launch one warp that waits, through the kernels' own bounded
+ * wait, on a barrier that nothing completes.  After the timeout set above it
+ * gives up and latches Q4_ERR_TIMEOUT, which q4_sync_status() then returns;
+ * the context stays usable.  Exercises the failure path of the pipelines
+ * without faulting or hanging the GPU. */
+q4_status q4_selftest_wait_timeout(q4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "q4_sync_status", I, P)
     _sig(lib, "q4_status_string", ctypes.c_char_p, I)
     _sig(lib, "q4_set_wait_timeout_ms", I, I)
+    _sig(lib, "q4_selftest_wait_timeout", I, P)
     _sig(lib, "gemm_w4a4_nvfp4_noalloc", I, P, I, op, I64, I64, I64, P, I, P)
     _sig(lib, "q4_noalloc_scratch_bytes", SZ)
     _sig(lib, "q4_noalloc_required_bytes", SZ, I64, I64)

@@ -235,6 +235,27 @@ q4_status gemm_fp4_common(bool nv, const q4_operand* A, const q4_operand* B, int
 }  // namespace
 }  // namespace q4
 
+namespace q4 {
+namespace {
+// One warp waits, through the same bounded wait as every pipeline barrier, on
+// an mbarrier that nothing arrives on: the wait gives up after ctl.wait_ns,
+// latches Q4_ERR_TIMEOUT and the kernel returns (no trap, nothing left
+// pending), so the failure path can be exercised without harming the context.
+__global__ void wait_probe_kernel(KernelCtl ctl) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, ctl, &abort_flag);
+  __syncwarp();
+}
+}  // namespace
+}  // namespace q4
+
 using namespace q4;
 
 extern "C" {
@@ -460,6 +481,13 @@ const char* q4_status_string(q4_status s) {
 int q4_set_wait_timeout_ms(int ms) {
   if (ms <= 0) return g_wait_ms.load();
   return g_wait_ms.exchange(ms);
+}
+
+q4_status q4_selftest_wait_timeout(q4_stream_t stream) {
+  const KernelCtl ctl{device_status_ptr(), wait_budget_ns()};
+  if (!ctl.status) return Q4_ERR_CUDA;
+  wait_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ctl);
+  return cudaGetLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
 }  // extern "C"
