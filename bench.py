@@ -224,11 +224,20 @@ class Decode:
         self.wq = [wq] + [wq.clone() for _ in range(self.copies - 1)]
         self.ws = [ws] + [ws.clone() for _ in range(self.copies - 1)]
         self.w_host = w
-        self.A = {M: workloads.to_bf16(workloads.normal(workloads.rng_for(seed, 1), (M, self.K), 1.0)).to(dev)
-                  for M in self.Ms}
-        self.C = {M: torch.empty((M, self.N), dtype=torch.bfloat16, device=dev) for M in self.Ms}
-        self.A_host = {M: self.A[M].cpu().pin_memory() for M in self.Ms}
-        self.C_host = {M: torch.empty((M, self.N), dtype=torch.bfloat16).pin_memory() for M in self.Ms}
+        # the step's three activation matrices (and outputs) are row slices of
+        # one buffer each, so that the end-to-end step moves them with one
+        # host-to-device and one device-to-host copy
+        rows = sum(self.Ms)
+        a_all = torch.cat([workloads.to_bf16(workloads.normal(workloads.rng_for(seed, 1), (M, self.K), 1.0))
+                           for M in self.Ms])
+        self.A_all = a_all.to(dev)
+        self.C_all = torch.empty((rows, self.N), dtype=torch.bfloat16, device=dev)
+        self.A_pin = a_all.pin_memory()
+        self.C_pin = torch.empty((rows, self.N), dtype=torch.bfloat16).pin_memory()
+        offs = np.cumsum((0,) + tuple(self.Ms))
+        self.A = {M: self.A_all[offs[j]:offs[j + 1]] for j, M in enumerate(self.Ms)}
+        self.C = {M: self.C_all[offs[j]:offs[j + 1]] for j, M in enumerate(self.Ms)}
+        self.A_host = {M: self.A_pin[offs[j]:offs[j + 1]] for j, M in enumerate(self.Ms)}
         self.h2d = sum(M * self.K * 2 for M in self.Ms)
         self.d2h = sum(M * self.N * 2 for M in self.Ms)
 
@@ -244,11 +253,9 @@ class Decode:
     kernel_launches = 3
 
     def e2e_step(self, i):
-        for M in self.Ms:
-            self.A[M].copy_(self.A_host[M], non_blocking=True)
+        self.A_all.copy_(self.A_pin, non_blocking=True)
         self.step(i)
-        for M in self.Ms:
-            self.C_host[M].copy_(self.C[M], non_blocking=True)
+        self.C_pin.copy_(self.C_all, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     # ---- oracle sample: the first `rows` weight rows, all three M
@@ -346,13 +353,16 @@ class QuantizeNvfp4:
         a = workloads.prefill_activations(seed, self.M, self.K)
         self.x_host = a.float().numpy()
         self.x = a.to(dev)
-        self.codes = torch.empty((self.M, self.K // 2), dtype=torch.uint8, device=dev)
-        self.sf = torch.empty(q4.mma_scales_bytes(self.M, self.K // 16), dtype=torch.uint8, device=dev)
+        # codes and scales are slices of one buffer: one device-to-host copy
+        # returns both in the end-to-end step
+        nc, ns = self.M * self.K // 2, q4.mma_scales_bytes(self.M, self.K // 16)
+        self.out = torch.empty(nc + ns, dtype=torch.uint8, device=dev)
+        self.codes = self.out[:nc].view(self.M, self.K // 2)
+        self.sf = self.out[nc:]
         self.g = torch.empty(1, dtype=torch.float32, device=dev)
         self.ws = q4.workspace(q4.OP_QUANTIZE_NVFP4, self.M, 0, self.K, dev)
         self.x_pin = a.pin_memory()
-        self.c_host = torch.empty_like(self.codes, device="cpu").pin_memory()
-        self.sf_host = torch.empty_like(self.sf, device="cpu").pin_memory()
+        self.out_host = torch.empty_like(self.out, device="cpu").pin_memory()
         self.h2d = self.M * self.K * 2
         self.d2h = self.codes.numel() + self.sf.numel()
 
@@ -378,8 +388,7 @@ class QuantizeNvfp4:
     def e2e_step(self, i):
         self.x.copy_(self.x_pin, non_blocking=True)
         self.step(i)
-        self.c_host.copy_(self.codes, non_blocking=True)
-        self.sf_host.copy_(self.sf, non_blocking=True)
+        self.out_host.copy_(self.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     def oracle_prepare(self, rows):
