@@ -137,17 +137,6 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
   }
 }
 
-// E2M1 magnitude code of |x| from its seven decision bounds: the number of
-// bounds it passes.  Bound k lies between codes k and k + 1; at equality the
-// pages' rule keeps the smaller code, round-half-to-even (rne) the even one,
-// i.e. it passes the odd bounds.
-__device__ __forceinline__ uint32_t code_from_bounds(float a, const float (&B)[7], bool rne) {
-  uint32_t c = 0;
-#pragma unroll
-  for (int k = 0; k < 7; ++k) c += (a > B[k]) | ((k & 1) & rne & (a == B[k]));
-  return c;
-}
-
 // Magnitude-and-sign E2M1 codes of two floats, RNE, saturating at 6: the
 // code of lo in bits 0..3, of hi in bits 4..7.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
@@ -320,9 +309,15 @@ __global__ void __launch_bounds__(kThreads, 4)
 // ------------------------------------------------------------------ MXFP4
 // One thread per 16 elements; a thread pair shares one 32-element block.
 //
-// y = x / 2^e is exact whenever it is a normal float, and a subnormal y lies
-// far below the smallest midpoint, so RN(|x| / 2^e) > t_k <=> |x| > t_k * 2^e,
-// and t_k * 2^e is itself an exact float (e is in [-42, 125]).
+// y = x * 2^-e is exactly x / 2^e whenever it is a normal float (e is in
+// [-42, 125], so 2^-e is a normal float and |y| < 8), and a subnormal y lies
+// far below the smallest midpoint 0.25.  The hardware RNE convert of y is then
+// the E2M1 code with ties to even; for the pages' ties to the smaller
+// magnitude, a y with at most three significant bits (every midpoint has
+// three) is replaced by its predecessor, which lies in the cell that rule
+// selects (any other such y -- an E2M1 value, 7, or 0.125 -- stays in its
+// cell).  y = x * 2^-e + 0 turns x = -0 into +0 (code 0) and keeps the sign of
+// every negative x, as the pages' sign rule asks.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     mxfp4_kernel(const T* __restrict__ x, const UnitMap um, uint8_t* __restrict__ codes,
@@ -342,15 +337,19 @@ __global__ void __launch_bounds__(kThreads)
 
   amax = fmaxf(amax, 1e-12f);  // normal, so floor(log2) is its exponent field
   const int e = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 2;
-  const float p2 = __uint_as_float((uint32_t)(127 + e) << 23);  // 2^e
-  const float B[7] = {0.25f * p2, 0.75f * p2, 1.25f * p2, 1.75f * p2,
-                      2.5f * p2,  3.5f * p2,  5.0f * p2};
-  uint2 packed = make_uint2(0u, 0u);
+  const float rp2 = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+  float y[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const uint32_t c = code_from_bounds(fabsf(v[j]), B, rne) | (v[j] < 0.f ? 8u : 0u);
-    if (j < 8) packed.x |= c << (4 * j);
-    else packed.y |= c << (4 * (j - 8));
+    uint32_t b = __float_as_uint(__fmaf_rn(v[j], rp2, 0.0f));
+    if (!rne && (b & 0x1FFFFFu) == 0u && (b & 0x7FFFFFFFu) != 0u) b -= 1u;  // magnitude predecessor
+    y[j] = __uint_as_float(b);
+  }
+  uint2 packed = make_uint2(0u, 0u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    packed.x |= cvt_e2m1x2(y[2 * j], y[2 * j + 1]) << (8 * j);
+    packed.y |= cvt_e2m1x2(y[8 + 2 * j], y[8 + 2 * j + 1]) << (8 * j);
   }
   reinterpret_cast<uint2*>(codes)[u] = packed;
 
