@@ -21,6 +21,9 @@ Sources (web pages, cited by title and section):
   NVFP4 example, the per-tensor vs per-block E4M3 example.
 * "LLM quantization" (drpranayjha.com, part 18): the eight-weight worked
   example and the outlier example.
+* "Quantization in deployment", "Fake quantization" (``fp8``,
+  ``fp8_blockwise``) and exercise 2 (block FP8's per-block promotion in the
+  GEMM): FP8 blockwise quantization and GEMM (``oracle.fp8``).
 
 Readings taken where the pages are silent or disagree (each one is also listed
 with its reason in the design notes of this repository):
@@ -36,6 +39,8 @@ with its reason in the design notes of this repository):
 6. Element 2j of a row goes to the low nibble of byte j, element 2j+1 to the
    high nibble; INT4 codes are 4-bit two's complement.
 7. The NVFP4 per-tensor scale covers the whole operand passed in.
+8. FP8 blockwise: an E4M3 byte keeps the sign of x / s, also when it rounds to
+   zero (an IEEE cast; x = -0 gives 0x80).
 
 Parity pins: every quantizer and the E2M1 / E4M3 / E8M0 / FP16 encoders are
 pinned by tests against values printed on the pages, closed forms and brute
@@ -44,7 +49,7 @@ by special cases (identity operand, equal blocks); no page prints a GEMM
 output, so beyond that their parity rests on the FP64 definition.
 """
 
-from . import formats, quantize, gemm  # noqa: F401
+from . import formats, quantize, gemm, fp8  # noqa: F401
 from .quantize import (  # noqa: F401
     nvfp4_tensor_scale, quantize_nvfp4, quantize_mxfp4, quantize_int4_g128,
     dequantize_nvfp4, dequantize_mxfp4, dequantize_int4_g128,
@@ -53,4 +58,7 @@ from .quantize import (  # noqa: F401
 from .gemm import (  # noqa: F401
     gemm_fp64, gemm_w4a4_nvfp4, gemm_w4a4_mxfp4, gemm_w4a16_int4, gemm_w4a16_nvfp4,
     gemm_w4a16_mxfp4, grouped_gemm_moe,
+)
+from .fp8 import (  # noqa: F401
+    e4m3_encode_signed, quantize_fp8_blockwise, dequantize_fp8_blockwise, gemm_fp8_blockwise,
 )
