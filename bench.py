@@ -553,6 +553,84 @@ class Moe(W4A4):
         return m * self.K * 2 + self.o_rows * self.K // 2 + self.o_rows * self.K // 32 + m * self.o_rows * 2
 
 
+class Fp8Blockwise:
+    """FP8 blockwise GEMM: A quantized on the fly into (1, 128) blocks, B
+    pre-quantized into 128 x 128 blocks, block-promoted tcgen05 GEMM."""
+    name = "fp8_blockwise"
+    unit = "TFLOP/s"
+    bound = "tensor"
+    tensor_over_bf16 = 2.0  # nominal dense FP8 : BF16 on GB300 (4.5 vs 2.25 PFLOP/s)
+    default_steps = 200
+    kernel = "fp8_gemm_kernel"
+    launches_per_step = 2  # activation quantizer + GEMM
+    kernel_launches = 1
+    oracle_grain = 128
+
+    def config(self):
+        return {"workload": f"fp8_blockwise A bf16 {self.M}x{self.K} (quantized on the fly, 1x128 blocks), "
+                            f"B E4M3 {self.N}x{self.K} (128x128 blocks)",
+                "M": self.M, "N": self.N, "K": self.K,
+                "l2": "inputs larger than L2 (A 134 MB bf16, B 235 MB)"}
+
+    def setup(self, q4, dev, seed, shape=None):
+        self.q4 = q4
+        a, b = workloads.prefill(seed, *(shape or ()))
+        self.M, self.K = a.shape
+        self.N = b.shape[0]
+        self.a_host, self.b_host = a, b
+        bd = torch.from_numpy(b).to(dev)
+        self.qb, self.sb = q4.quantize_fp8_blockwise(bd, 128)
+        del bd
+        self.A = a.to(dev)
+        self.qa = torch.empty((self.M, self.K), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((self.M, self.K // 128), dtype=torch.float32, device=dev)
+        q4.quantize_fp8_blockwise(self.A, 1, codes=self.qa, scales=self.sa)
+        self.C = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        self.A_pin = a.pin_memory()
+        self.C_host = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.M * self.K * 2
+        self.d2h = self.M * self.N * 2
+
+    def step(self, i):
+        self.q4.quantize_fp8_blockwise(self.A, 1, codes=self.qa, scales=self.sa)
+        self.q4.gemm_fp8_blockwise(self.qa, self.sa, self.qb, self.sb, out=self.C)
+
+    def kernel_only(self, i):
+        self.q4.gemm_fp8_blockwise(self.qa, self.sa, self.qb, self.sb, out=self.C)
+
+    def e2e_step(self, i):
+        self.A.copy_(self.A_pin, non_blocking=True)
+        self.step(i)
+        self.C_host.copy_(self.C, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def flops_per_step(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def units_per_step(self):
+        return self.flops_per_step()
+
+    def kernel_units(self):
+        return self.flops_per_step()
+
+    def oracle_prepare(self, rows):
+        self.o_rows = rows
+        self.o_a = self.a_host.float().numpy()
+
+    def oracle_step(self):
+        import oracle
+        qa = oracle.quantize_fp8_blockwise(self.o_a[:min(self.M, 64)], (1, 128))
+        qb = oracle.quantize_fp8_blockwise(self.b_host[:self.o_rows], (128, 128))
+        oracle.gemm_fp8_blockwise(*qa, *qb)
+
+    def oracle_units(self):
+        return 2.0 * min(self.M, 64) * self.o_rows * self.K
+
+    def oracle_sample_text(self):
+        return (f"A rows 0..{min(self.M, 64) - 1} x B rows 0..{self.o_rows - 1}: FP8 blockwise quantize "
+                f"both + FP64 block-promoted GEMM")
+
+
 class Grouped:
     """64-expert routed NVFP4 MoE: tokens quantized once, grouped tcgen05 GEMM."""
     name = "grouped_moe"
@@ -641,12 +719,14 @@ class Grouped:
 
 
 WORKLOADS = {"decode": Decode, "decode_nvfp4": DecodeNvfp4, "prefill": Prefill, "moe": Moe,
-             "grouped": Grouped, "quantize": QuantizeNvfp4, "quantize_rne": QuantizeNvfp4Rne}
+             "grouped": Grouped, "quantize": QuantizeNvfp4, "quantize_rne": QuantizeNvfp4Rne,
+             "fp8_blockwise": Fp8Blockwise}
 DTYPES = {"decode": "bf16 (exact int4 values) x bf16 -> fp32",
           "decode_nvfp4": "bf16 (exact e2m1 x e4m3 values) x bf16 -> fp32",
           "quantize": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)", "quantize_rne": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)",
           "prefill": "e2m1 x e2m1 -> fp32",
-          "moe": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32"}
+          "moe": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32",
+          "fp8_blockwise": "e4m3 x e4m3 -> fp32 (block-promoted)"}
 
 
 def scale_units(x, unit):
@@ -710,6 +790,11 @@ def run_reference(args, dist):
     print(json.dumps(line), flush=True)
 
 
+def peak_text(wl):
+    r = getattr(wl, "tensor_over_bf16", FP4_OVER_BF16)
+    return f"bf16_tflops x {r:g} (nominal {'FP8' if r == 2.0 else 'FP4'}:BF16)"
+
+
 def wl_setup_host(wl, seed):
     """Host-only inputs for the oracle arm (no GPU needed)."""
     if isinstance(wl, Decode):
@@ -718,6 +803,10 @@ def wl_setup_host(wl, seed):
                      for M in wl.Ms}
     elif isinstance(wl, QuantizeNvfp4):
         wl.x_host = workloads.prefill_activations(seed, wl.M, wl.K).float().numpy()
+    elif isinstance(wl, Fp8Blockwise):
+        wl.a_host, wl.b_host = workloads.prefill(seed)
+        wl.M, wl.K = wl.a_host.shape
+        wl.N = wl.b_host.shape[0]
     elif isinstance(wl, Grouped):
         tok, _, offs, rt = workloads.grouped(seed, T=wl.T, E=wl.E, N=wl.N, K=wl.K, top_k=wl.top,
                                              experts=False)
@@ -732,7 +821,8 @@ def wl_setup_host(wl, seed):
 SEEDS = {"decode": workloads.SEED_BASE + 2, "decode_nvfp4": workloads.SEED_BASE + 2,
          "moe": workloads.SEED_BASE + 3,
          "prefill": workloads.SEED_BASE + 4, "grouped": workloads.SEED_BASE + 5,
-         "quantize": workloads.SEED_BASE + 4, "quantize_rne": workloads.SEED_BASE + 4}
+         "quantize": workloads.SEED_BASE + 4, "quantize_rne": workloads.SEED_BASE + 4,
+         "fp8_blockwise": workloads.SEED_BASE + 4}
 
 
 def main():
@@ -808,7 +898,8 @@ def main():
     if wl.bound == "hbm":
         peak, punit = pk["hbm_gbs"], "GB/s"
     else:
-        peak, punit = pk["bf16_tflops"] * FP4_OVER_BF16, "TFLOP/s"
+        ratio = getattr(wl, "tensor_over_bf16", FP4_OVER_BF16)
+        peak, punit = pk["bf16_tflops"] * ratio, "TFLOP/s"
     kg = torch.cuda.CUDAGraph()
     with torch.cuda.graph(kg):
         for i in range(G):
@@ -828,7 +919,7 @@ def main():
     roofline = {"bound": wl.bound, "achieved": achieved, "peak": peak, "unit": punit,
                 "frac": achieved / peak, "traffic": NCU_TRAFFIC.get(args.workload),
                 "kernel": wl.kernel, "avg_launch_us": avg_s * 1e6,
-                "peak_source": f"{src} ({'hbm_gbs' if punit == 'GB/s' else 'bf16_tflops x 6 (nominal FP4:BF16)'})"}
+                "peak_source": f"{src} ({'hbm_gbs' if punit == 'GB/s' else peak_text(wl)})"}
 
     # end to end through the public API: host buffers, copies inside the timed region
     n_e2e = min(K, 2000 if wl.unit == "GB/s" else 50)

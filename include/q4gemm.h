@@ -255,6 +255,40 @@ q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            size_t ws_bytes, q4_stream_t stream);
 
 /*
+ * FP8 blockwise quantization ("Quantization in deployment", "Fake
+ * quantization", fp8 and fp8_blockwise): E4M3 codes, one FP32 scale per
+ * block of block_rows x 128 elements, block_rows = 128 for weights
+ * (128 x 128 blocks) or 1 for activations (one scale per row and 128
+ * columns).  For every block, in float32 with IEEE rounding:
+ *   s = max(amax_block, 1e-12) / 448;  code = e4m3_rne(clamp(x / s, -448, 448))
+ * where an E4M3 byte keeps the sign of x / s, also when it rounds to zero.
+ * codes: [rows, K] bytes (one per element, 16-byte aligned); scales: float
+ * [rows / block_rows, K / 128] row-major.  K % 128 == 0; rows % 128 == 0
+ * when block_rows == 128.  x: [rows, K] of x_dtype, 16-byte aligned.  A
+ * non-finite input latches Q4_ERR_NONFINITE (see q4_sync_status()).
+ */
+q4_status quantize_fp8_blockwise(const void* x, int x_dtype, int64_t rows, int64_t K,
+                                 int block_rows, uint8_t* codes, float* scales,
+                                 q4_stream_t stream);
+
+/*
+ * Block-promoted FP8 GEMM ("Quantization in deployment", exercise 2, the cost
+ * of block FP8): the tensor cores sum the FP8 products of each 128-wide K
+ * block in FP32, and each block's sum is multiplied by its activation and
+ * weight scales and added into the FP32 result:
+ *   C[m, n] = sum_kb sa[m, kb] * sb[n / 128, kb] * sum_{k in kb} qa[m, k] * qb[n, k]
+ * qa: E4M3 [M, K] with sa float [M, K / 128] (quantize_fp8_blockwise with
+ * block_rows 1); qb: E4M3 [N, K] with sb float [N / 128, K / 128] (block_rows
+ * 128).  C: [M, N] in c_dtype (Q4_F32, or Q4_BF16 rounded to nearest even),
+ * 16-byte aligned.  K % 128 == 0, N % 128 == 0; any M.  qa and qb 16-byte
+ * aligned.  Asynchronous; operands may come from the previous kernel in the
+ * stream (programmatic dependent launch, read only after it has finished).
+ */
+q4_status gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qb,
+                             const float* sb, int64_t M, int64_t N, int64_t K, void* C,
+                             int c_dtype, q4_stream_t stream);
+
+/*
  * gemm_w4a4_nvfp4 without a workspace, for callers that cannot give the
  * library any device memory beyond inputs and outputs: a plugin or custom-op
  * interface that passes only input and output buffers, an engine whose memory

@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "gemm_w4a16_nvfp4", I, P, P, P, P, I64, I64, I64, P, P)
     _sig(lib, "gemm_w4a16_mxfp4", I, P, P, P, I64, I64, I64, P, P)
     _sig(lib, "grouped_gemm_moe", I, P, I64, I64, P, P, I64, I, P, P, P, I64, P, P, SZ, P)
+    _sig(lib, "quantize_fp8_blockwise", I, P, I, I64, I64, I, P, P, P)
+    _sig(lib, "gemm_fp8_blockwise", I, P, P, P, P, I64, I64, I64, P, I, P)
     _sig(lib, "q4_sync_status", I, P)
     _sig(lib, "q4_status_string", ctypes.c_char_p, I)
     _sig(lib, "q4_set_wait_timeout_ms", I, I)
@@ -284,6 +286,38 @@ def gemm_w4a16_mxfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=No
     C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
     _check("gemm_w4a16_mxfp4", lib().gemm_w4a16_mxfp4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(),
                                                        M, N, K, C.data_ptr(), _stream(stream)))
+    return C
+
+
+def quantize_fp8_blockwise(x: torch.Tensor, block_rows: int, codes=None, scales=None,
+                           stream=None):
+    """FP8 (E4M3) blockwise quantization of x [rows, K] (f32 / bf16 / f16):
+    block_rows 128 for weights (128 x 128 blocks), 1 for activations (1 x 128).
+    -> (codes u8 [rows, K], scales float32 [rows / block_rows, K / 128])."""
+    _cuda2d(x, "x")
+    rows, K = x.shape
+    if codes is None:
+        codes = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((rows // max(block_rows, 1), K // 128), dtype=torch.float32,
+                             device=x.device)
+    _check("quantize_fp8_blockwise", lib().quantize_fp8_blockwise(
+        x.data_ptr(), _DTYPE[x.dtype], rows, K, block_rows, codes.data_ptr(), scales.data_ptr(),
+        _stream(stream)))
+    return codes, scales
+
+
+def gemm_fp8_blockwise(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
+                       out_dtype=torch.bfloat16, out=None, stream=None) -> torch.Tensor:
+    """C [M, N] = sum over 128-wide K blocks of sa * sb * (qa . qb^T): qa E4M3
+    [M, K] with sa [M, K/128], qb E4M3 [N, K] with sb [N/128, K/128]."""
+    _cuda2d(qa, "qa")
+    M, K = qa.shape
+    N = qb.shape[0]
+    C = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
+    _check("gemm_fp8_blockwise", lib().gemm_fp8_blockwise(
+        qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), M, N, K, C.data_ptr(),
+        _DTYPE[C.dtype], _stream(stream)))
     return C
 
 

@@ -410,6 +410,36 @@ q4_status gemm_w4a16_mxfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t*
   return w4a16_fp4(A_bf16, Wq, Ws, nullptr, false, M, N, K, C_bf16, stream);
 }
 
+q4_status quantize_fp8_blockwise(const void* x, int x_dtype, int64_t rows, int64_t K,
+                                 int block_rows, uint8_t* codes, float* scales,
+                                 q4_stream_t stream) {
+  if (rows < 0 || K <= 0 || !valid_dtype(x_dtype) || (block_rows != 1 && block_rows != 128))
+    return Q4_ERR_INVALID_ARG;
+  if (K % 128 || rows % block_rows) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if ((rows / block_rows) * (K / 128) > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return Q4_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4))
+    return Q4_ERR_INVALID_ARG;
+  return launch_quant_fp8(x, x_dtype, rows, K, block_rows, codes, scales,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qb,
+                             const float* sb, int64_t M, int64_t N, int64_t K, void* C,
+                             int c_dtype, q4_stream_t stream) {
+  if (M < 0 || N < 0 || K <= 0 || (c_dtype != Q4_F32 && c_dtype != Q4_BF16))
+    return Q4_ERR_INVALID_ARG;
+  if (K % 128 || N % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 ||
+      ceil_div(M, 128) * (N / 128) > INT32_MAX / 2)
+    return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return Q4_OK;
+  if (!qa || !sa || !qb || !sb || !C || !aligned(qa, 16) || !aligned(qb, 16) || !aligned(C, 16) ||
+      !aligned(sa, 4) || !aligned(sb, 4))
+    return Q4_ERR_INVALID_ARG;
+  return launch_fp8_gemm(qa, sa, qb, sb, M, N, K, C, c_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
 q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            const int32_t* expert_offsets, const int32_t* row_token, int64_t R,
                            int E, const uint8_t* W_codes, const uint8_t* W_scales,

@@ -82,6 +82,15 @@ q4_status launch_w4a16_fp4(const void* A, const uint8_t* Wq, const uint8_t* Wsf,
                            bool nvfp4, int64_t M, int64_t N, int64_t K, void* C,
                            cudaStream_t stream);
 
+// FP8 blockwise: block_rows 1 (activations, blocks (1, 128)) or 128 (weights,
+// 128 x 128); codes [rows, K] E4M3 bytes, scales FP32 row-major per block.
+q4_status launch_quant_fp8(const void* x, int dtype, int64_t rows, int64_t K, int block_rows,
+                           uint8_t* codes, float* scales, cudaStream_t stream);
+// Block-promoted FP8 GEMM: C [M, N] = sum over K blocks of sa * sb * (qa . qb^T).
+q4_status launch_fp8_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                          int64_t M, int64_t N, int64_t K, void* C, int c_dtype,
+                          cudaStream_t stream);
+
 // TMA descriptor creation through the driver entry point.
 q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["quantize_nvfp4", "quantize_mxfp4", "quantize_int4_g128", "gemm_w4a4_nvfp4",
                  "gemm_w4a4_mxfp4", "gemm_w4a16_int4", "gemm_w4a16_nvfp4", "gemm_w4a16_mxfp4",
-                 "grouped_gemm_moe", "q4_sync_status",
+                 "grouped_gemm_moe", "q4_sync_status", "quantize_fp8_blockwise", "gemm_fp8_blockwise",
                  "q4_workspace_size", "q4_scales_to_mma"]:
         assert want in names
 
@@ -58,6 +58,17 @@ def test_host_argument_checks(clib):
     assert clib.gemm_w4a16_nvfp4(fake, fake, fake, fake, 4, 4, 100, fake, None) == -2
     assert clib.gemm_w4a16_mxfp4(fake, fake, fake, 4, 4, 64, fake, None) == -2
     assert clib.gemm_w4a16_nvfp4(fake, fake, fake, None, 4, 4, 128, fake, None) == -1
+    # FP8 blockwise: K % 128, N % 128, rows % 128 for weight blocks, bad block height,
+    # bad output dtype, misaligned operands
+    assert clib.quantize_fp8_blockwise(fake, 1, 4, 100, 1, fake, fake, None) == -2
+    assert clib.quantize_fp8_blockwise(fake, 1, 100, 128, 128, fake, fake, None) == -2
+    assert clib.quantize_fp8_blockwise(fake, 1, 4, 128, 2, fake, fake, None) == -1
+    assert clib.quantize_fp8_blockwise(fake + 8, 1, 4, 128, 1, fake, fake, None) == -1
+    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 128, 100, fake, 1, None) == -2
+    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 100, 128, fake, 1, None) == -2
+    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 128, 128, fake, 2, None) == -1
+    assert clib.gemm_fp8_blockwise(fake + 4, fake, fake, fake, 4, 128, 128, fake, 1, None) == -1
+    assert clib.gemm_fp8_blockwise(None, fake, fake, fake, 0, 128, 128, fake, 1, None) == 0
     assert clib.gemm_w4a16_nvfp4(fake, fake, fake + 1, fake, 4, 4, 128, fake, None) == -1
     assert clib.gemm_w4a16_mxfp4(None, fake, fake, 4, 4, 128, fake, None) == -1
     # an unknown rounding mode
