@@ -147,6 +147,7 @@ constexpr int kSlots = 4;                         // TMEM accumulator slots, 128
 constexpr uint32_t kGTileBytes = GBM * GBK;       // one operand tile of one K block (bytes)
 constexpr uint32_t kGStageBytes = 2 * kGTileBytes;
 constexpr int kPromoWarp0 = 2, kPromoWarps = 8;
+constexpr int kBandM = 32;                       // M tiles per band of the tile order
 constexpr int kGThreads = (kPromoWarp0 + kPromoWarps) * 32;
 constexpr uint32_t kGSmemBytes = kGStages * kGStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(kGSmemBytes <= 232448, "shared memory");
@@ -226,9 +227,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort_flag = &sm->abort;
-  // tiles: m fastest, so the CTAs working at one time share B tiles and sweep all of A
-  auto tile_m = [&](int t) { return (t % p.num_m) * GBM; };
-  auto tile_n = [&](int t) { return (t / p.num_m) * GBN; };
+  // Tile order: bands of kBandM M tiles (32 x 128 rows of A, 33.5 MB at K = 8192,
+  // stay in L2), M fastest inside a band, so the CTAs working at one time share
+  // their B tiles and every band reads B from DRAM once.
+  auto tile_mn = [&](int t, int& m0, int& n0) {
+    const int band_tiles = kBandM * p.num_n;
+    const int band = t / band_tiles, r = t - band * band_tiles;
+    const int gm = min(kBandM, p.num_m - band * kBandM);
+    m0 = (band * kBandM + r % gm) * GBM;
+    n0 = (r / gm) * GBN;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -238,7 +246,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     for (int s = 0; s < kGStages; ++s) issued[s] = 0, issued_phase[s] = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
-      const int m0 = tile_m(t), n0 = tile_n(t);
+      int m0, n0;
+      tile_mn(t, m0, n0);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
@@ -305,7 +314,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     uint32_t gk = 0;
     bool alive = true;
     for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
-      const int m0 = tile_m(t), n0 = tile_n(t);
+      int m0, n0;
+      tile_mn(t, m0, n0);
       const int64_t row = m0 + q * 32 + lane;
       const bool row_ok = row < p.M;
       const float* sa_row = p.sa + (row_ok ? row : p.M - 1) * KB;
