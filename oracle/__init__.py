@@ -61,4 +61,5 @@ from .gemm import (  # noqa: F401
 )
 from .fp8 import (  # noqa: F401
     e4m3_encode_signed, quantize_fp8_blockwise, dequantize_fp8_blockwise, gemm_fp8_blockwise,
+    int4_to_e4m3, gemm_w4a8,
 )

@@ -15,6 +15,13 @@ the pages' definitions, never called by the product path.
   block, that block's sum is multiplied by its activation and weight scales,
   and the results of the K blocks are summed:
       C[m, n] = sum_kb  sa[m, kb] * sb[n // 128, kb] * sum_{k in kb} qa[m, k] qb[n, k].
+* W4A8 ("Low-bit inference for very large MoE", "Kernels on different
+  hardware", the W4A8 row: INT4 weights dequantized to FP8, activations
+  quantized to FP8, the product on FP8 tensor cores).  The INT4 values -8..7
+  are exact E4M3 values, so the weight codes enter the FP8 product unchanged
+  and their FP16 group scale (one per 128 along K, aligned with the 128-wide
+  K blocks) joins the activation scale in the per-block promotion:
+      C[m, n] = sum_kb  sa[m, kb] * s16[n, kb] * sum_{k in kb} qa[m, k] q[n, k].
 
 Arithmetic: the quantizer steps are float32 with IEEE rounding, as the page's
 float32 tensors compute them.  The GEMM is float64: the block sums of E4M3
@@ -25,7 +32,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import E4M3_MAX, F32_1E_12, e4m3_decode, e4m3_encode
+from .formats import E4M3_MAX, F32_1E_12, e4m3_decode, e4m3_encode, fp16_decode
+from .quantize import int4_values
 
 F32 = np.float32
 FP8_BLOCK_K = 128
@@ -101,4 +109,30 @@ def gemm_fp8_blockwise(qa, sa, qb, sb) -> np.ndarray:
         P = A[:, ks] @ B[:, ks].T                              # exact block sums
         wscale = np.repeat(sb[:, kb], br)                      # per output column
         C += P * sa[:, kb][:, None] * wscale[None, :]
+    return C
+
+
+def int4_to_e4m3(q) -> np.ndarray:
+    """E4M3 bytes of INT4 values (exact: every integer in -8..7 is an E4M3
+    value), the weight conversion of W4A8."""
+    return e4m3_encode_signed(np.asarray(q, dtype=np.float32))
+
+
+def gemm_w4a8(qa, sa, w_codes, w_scales) -> np.ndarray:
+    """W4A8 product, float64 [M, N]: FP8 activations qa [M, K] with (1, 128)
+    block scales sa float32 [M, K/128]; INT4 g128 weights (packed codes
+    [N, K/2], FP16 scale bits [N, K/128]) converted to E4M3 and promoted per
+    128-wide K block with sa[m, kb] * s16[n, kb]."""
+    A = e4m3_decode(np.asarray(qa))
+    B = e4m3_decode(int4_to_e4m3(int4_values(w_codes)))
+    M, K = A.shape
+    if B.shape[1] != K or K % FP8_BLOCK_K:
+        raise ValueError("K must match and be a multiple of 128")
+    sa = np.asarray(sa, dtype=np.float64)
+    sw = fp16_decode(np.asarray(w_scales))                    # [N, K/128] float64
+    C = np.zeros((M, B.shape[0]), dtype=np.float64)
+    for kb in range(K // FP8_BLOCK_K):
+        ks = slice(kb * FP8_BLOCK_K, (kb + 1) * FP8_BLOCK_K)
+        P = A[:, ks] @ B[:, ks].T                              # exact block sums
+        C += P * sa[:, kb][:, None] * sw[:, kb][None, :]
     return C

@@ -2,7 +2,8 @@
 blockwise quantizer, a brute-force signed E4M3 cast, the per-block scale tied
 to the block amax, block shapes, and the block-promoted GEMM against plain
 loops over dequantized values (two weight block rows and three K blocks, so a
-wrong block index fails)."""
+wrong block index fails), and the W4A8 product (INT4 weights converted
+exactly to E4M3, FP16 group scales in the promotion) against plain loops."""
 import json
 import os
 
@@ -154,3 +155,40 @@ def test_gemm_fp8_blockwise_identity_gives_dequantized_activations():
     C = oracle.gemm_fp8_blockwise(qa, sa, qb, sb)
     assert np.array_equal(C, oracle.dequantize_fp8_blockwise(qa, sa, (1, 128))[:, :128])
     assert F.e4m3_decode(0x38) == 1.0
+
+
+def test_int4_values_convert_exactly_to_e4m3():
+    """W4A8's weight conversion: every INT4 value -8..7 is an E4M3 value, and
+    the bytes are the ones the E4M3 bit fields give (sign, exponent - 7, three
+    mantissa bits): 1 = 0x38, 2 = 0x40, 3 = 0x44, 7 = 0x4E, -8 = 0xD0."""
+    q = np.arange(-8, 8)
+    b = oracle.int4_to_e4m3(q)
+    assert np.array_equal(F.e4m3_decode(b), q.astype(np.float64))
+    by_value = dict(zip(q.tolist(), b.tolist()))
+    assert by_value[0] == 0x00 and by_value[1] == 0x38 and by_value[2] == 0x40
+    assert by_value[3] == 0x44 and by_value[7] == 0x4E and by_value[-8] == 0xD0
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 256), (2, 130, 384)])
+def test_gemm_w4a8_brute_force(M, N, K):
+    """Plain loops over e4m3(qa) * sa and the INT4 integer times its FP16
+    group scale (three K blocks: a wrong block index or a scale taken from the
+    wrong row fails)."""
+    rng = np.random.default_rng(M + N + K)
+    a = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-3, 3, (M, K)))).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[:, 128:256] *= np.float32(10.0)
+    w[1] *= np.float32(0.01)
+    qa, sa = oracle.quantize_fp8_blockwise(a, (1, 128))
+    wc, ws = oracle.quantize_int4_g128(w)
+    C = oracle.gemm_w4a8(qa, sa, wc, ws)
+    q = oracle.quantize.int4_values(wc)
+    s16 = F.fp16_decode(ws)
+    ref = np.zeros((M, N))
+    for i in range(M):
+        for j in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += (float(F.e4m3_decode(qa[i, k])) * float(sa[i, k // 128])) * (int(q[j, k]) * float(s16[j, k // 128]))
+            ref[i, j] = acc
+    assert np.allclose(C, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
