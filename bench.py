@@ -631,6 +631,56 @@ class Fp8Blockwise:
                 f"both + FP64 block-promoted GEMM")
 
 
+class W4a8(Fp8Blockwise):
+    """W4A8: A quantized on the fly into FP8 (1, 128) blocks, INT4 g128 weights
+    converted to E4M3 inside the GEMM (their FP16 group scales in the promotion)."""
+    name = "w4a8"
+    kernel = "w4a8_gemm_kernel"
+
+    def config(self):
+        return {"workload": f"w4a8 A bf16 {self.M}x{self.K} (FP8 1x128 blocks, quantized on the fly), "
+                            f"W INT4 g128 {self.N}x{self.K}",
+                "M": self.M, "N": self.N, "K": self.K,
+                "l2": "inputs larger than L2 (A 134 MB bf16, W 117 MB INT4)"}
+
+    def setup(self, q4, dev, seed, shape=None):
+        self.q4 = q4
+        a, b = workloads.prefill(seed, *(shape or ()))
+        self.M, self.K = a.shape
+        self.N = b.shape[0]
+        self.a_host, self.b_host = a, b
+        bd = torch.from_numpy(b).to(dev)
+        self.wq, ws16 = q4.quantize_int4_g128(bd)
+        del bd
+        self.wsk = q4.w4a8_weight_scales(ws16)
+        self.A = a.to(dev)
+        self.qa = torch.empty((self.M, self.K), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((self.M, self.K // 128), dtype=torch.float32, device=dev)
+        q4.quantize_fp8_blockwise(self.A, 1, codes=self.qa, scales=self.sa)
+        self.C = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=dev)
+        self.A_pin = a.pin_memory()
+        self.C_host = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.M * self.K * 2
+        self.d2h = self.M * self.N * 2
+
+    def step(self, i):
+        self.q4.quantize_fp8_blockwise(self.A, 1, codes=self.qa, scales=self.sa)
+        self.q4.gemm_w4a8(self.qa, self.sa, self.wq, self.wsk, out=self.C)
+
+    def kernel_only(self, i):
+        self.q4.gemm_w4a8(self.qa, self.sa, self.wq, self.wsk, out=self.C)
+
+    def oracle_step(self):
+        import oracle
+        qa = oracle.quantize_fp8_blockwise(self.o_a[:min(self.M, 64)], (1, 128))
+        wc, ws = oracle.quantize_int4_g128(self.b_host[:self.o_rows])
+        oracle.gemm_w4a8(*qa, wc, ws)
+
+    def oracle_sample_text(self):
+        return (f"A rows 0..{min(self.M, 64) - 1} x W rows 0..{self.o_rows - 1}: FP8 blockwise quantize A, "
+                f"INT4 g128 quantize W + FP64 block-promoted GEMM")
+
+
 class Grouped:
     """64-expert routed NVFP4 MoE: tokens quantized once, grouped tcgen05 GEMM."""
     name = "grouped_moe"
@@ -720,13 +770,14 @@ class Grouped:
 
 WORKLOADS = {"decode": Decode, "decode_nvfp4": DecodeNvfp4, "prefill": Prefill, "moe": Moe,
              "grouped": Grouped, "quantize": QuantizeNvfp4, "quantize_rne": QuantizeNvfp4Rne,
-             "fp8_blockwise": Fp8Blockwise}
+             "fp8_blockwise": Fp8Blockwise, "w4a8": W4a8}
 DTYPES = {"decode": "bf16 (exact int4 values) x bf16 -> fp32",
           "decode_nvfp4": "bf16 (exact e2m1 x e4m3 values) x bf16 -> fp32",
           "quantize": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)", "quantize_rne": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)",
           "prefill": "e2m1 x e2m1 -> fp32",
           "moe": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32",
-          "fp8_blockwise": "e4m3 x e4m3 -> fp32 (block-promoted)"}
+          "fp8_blockwise": "e4m3 x e4m3 -> fp32 (block-promoted)",
+          "w4a8": "e4m3 x int4 (exact e4m3) -> fp32 (block-promoted)"}
 
 
 def scale_units(x, unit):
@@ -822,7 +873,7 @@ SEEDS = {"decode": workloads.SEED_BASE + 2, "decode_nvfp4": workloads.SEED_BASE 
          "moe": workloads.SEED_BASE + 3,
          "prefill": workloads.SEED_BASE + 4, "grouped": workloads.SEED_BASE + 5,
          "quantize": workloads.SEED_BASE + 4, "quantize_rne": workloads.SEED_BASE + 4,
-         "fp8_blockwise": workloads.SEED_BASE + 4}
+         "fp8_blockwise": workloads.SEED_BASE + 4, "w4a8": workloads.SEED_BASE + 4}
 
 
 def main():

@@ -16,6 +16,9 @@
  *          scale per 128.  "Low-bit inference for very large MoE", section
  *          "Why quantization-aware training" (fake_int4), with the group of
  *          128 and FP16 scale of "Quantization chains", "Bits per weight".
+ *  FP8     E4M3 bytes (one per element), one FP32 scale per 128 x 128 weight
+ *          block or per (1, 128) activation block.  "Quantization in
+ *          deployment", "Fake quantization" (fp8_blockwise) and exercise 2.
  *
  * The E2M1 code of a value y = clamp(x / S, -6, 6) is the nearest of
  * 0, 0.5, 1, 1.5, 2, 3, 4, 6 with ties going to the smaller magnitude; its
@@ -287,6 +290,25 @@ q4_status quantize_fp8_blockwise(const void* x, int x_dtype, int64_t rows, int64
 q4_status gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qb,
                              const float* sb, int64_t M, int64_t N, int64_t K, void* C,
                              int c_dtype, q4_stream_t stream);
+
+/*
+ * W4A8 ("Low-bit inference for very large MoE", "Kernels on different
+ * hardware", the W4A8 row: INT4 weights turned into FP8, activations quantized
+ * to FP8, the product on FP8 tensor cores).  Every INT4 value -8..7 is an
+ * E4M3 value, so the weight codes convert exactly; the FP16 group scale (one
+ * per 128 along K) joins the activation scale in the per-K-block promotion:
+ *   C[m, n] = sum_kb sa[m, kb] * s16[n, kb] * sum_{k in kb} qa[m, k] * q[n, k]
+ * qa, sa: FP8 activations from quantize_fp8_blockwise with block_rows 1.
+ * w_codes: [N, K/2] INT4 codes as quantize_int4_g128 writes them (16-byte
+ * aligned).  w_scales_kn: float [K/128, N], the weight scales converted once
+ * by w4a8_weight_scales (16-byte aligned).  C: [M, N] in c_dtype (Q4_F32 or
+ * Q4_BF16), 16-byte aligned.  K % 128 == 0, N % 128 == 0; any M.
+ */
+q4_status w4a8_weight_scales(const uint16_t* w_scales, int64_t N, int64_t K, float* w_scales_kn,
+                             q4_stream_t stream);
+q4_status gemm_w4a8(const uint8_t* qa, const float* sa, const uint8_t* w_codes,
+                    const float* w_scales_kn, int64_t M, int64_t N, int64_t K, void* C,
+                    int c_dtype, q4_stream_t stream);
 
 /*
  * gemm_w4a4_nvfp4 without a workspace, for callers that cannot give the

@@ -78,6 +78,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "grouped_gemm_moe", I, P, I64, I64, P, P, I64, I, P, P, P, I64, P, P, SZ, P)
     _sig(lib, "quantize_fp8_blockwise", I, P, I, I64, I64, I, P, P, P)
     _sig(lib, "gemm_fp8_blockwise", I, P, P, P, P, I64, I64, I64, P, I, P)
+    _sig(lib, "w4a8_weight_scales", I, P, I64, I64, P, P)
+    _sig(lib, "gemm_w4a8", I, P, P, P, P, I64, I64, I64, P, I, P)
     _sig(lib, "q4_sync_status", I, P)
     _sig(lib, "q4_status_string", ctypes.c_char_p, I)
     _sig(lib, "q4_set_wait_timeout_ms", I, I)
@@ -318,6 +320,32 @@ def gemm_fp8_blockwise(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb:
     _check("gemm_fp8_blockwise", lib().gemm_fp8_blockwise(
         qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), M, N, K, C.data_ptr(),
         _DTYPE[C.dtype], _stream(stream)))
+    return C
+
+
+def w4a8_weight_scales(w_scales: torch.Tensor, stream=None) -> torch.Tensor:
+    """FP16 INT4 group scales [N, K/128] (as quantize_int4_g128 returns them,
+    int16 bits) -> float32 [K/128, N], the layout gemm_w4a8 reads."""
+    _cuda2d(w_scales, "w_scales")
+    N, KB = w_scales.shape
+    out = torch.empty((KB, N), dtype=torch.float32, device=w_scales.device)
+    _check("w4a8_weight_scales", lib().w4a8_weight_scales(
+        w_scales.data_ptr(), N, KB * 128, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def gemm_w4a8(qa: torch.Tensor, sa: torch.Tensor, w_codes: torch.Tensor, w_scales_kn: torch.Tensor,
+              out_dtype=torch.bfloat16, out=None, stream=None) -> torch.Tensor:
+    """C [M, N] = sum over 128-wide K blocks of sa * s16 * (qa . q^T): qa E4M3
+    [M, K] with sa [M, K/128]; INT4 codes [N, K/2] with w4a8_weight_scales'
+    float32 [K/128, N]."""
+    _cuda2d(qa, "qa")
+    M, K = qa.shape
+    N = w_codes.shape[0]
+    C = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
+    _check("gemm_w4a8", lib().gemm_w4a8(
+        qa.data_ptr(), sa.data_ptr(), w_codes.data_ptr(), w_scales_kn.data_ptr(), M, N, K,
+        C.data_ptr(), _DTYPE[C.dtype], _stream(stream)))
     return C
 
 

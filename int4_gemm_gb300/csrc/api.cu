@@ -440,6 +440,33 @@ q4_status gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* 
   return launch_fp8_gemm(qa, sa, qb, sb, M, N, K, C, c_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+q4_status w4a8_weight_scales(const uint16_t* w_scales, int64_t N, int64_t K, float* w_scales_kn,
+                             q4_stream_t stream) {
+  if (N < 0 || K <= 0) return Q4_ERR_INVALID_ARG;
+  if (K % 128 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (N == 0) return Q4_OK;
+  if (!w_scales || !w_scales_kn || !aligned(w_scales, 2) || !aligned(w_scales_kn, 4))
+    return Q4_ERR_INVALID_ARG;
+  return launch_w4a8_scales(w_scales, N, K / 128, w_scales_kn, reinterpret_cast<cudaStream_t>(stream));
+}
+
+q4_status gemm_w4a8(const uint8_t* qa, const float* sa, const uint8_t* w_codes,
+                    const float* w_scales_kn, int64_t M, int64_t N, int64_t K, void* C,
+                    int c_dtype, q4_stream_t stream) {
+  if (M < 0 || N < 0 || K <= 0 || (c_dtype != Q4_F32 && c_dtype != Q4_BF16))
+    return Q4_ERR_INVALID_ARG;
+  if (K % 128 || N % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2 ||
+      ceil_div(M, 128) * (N / 128) > INT32_MAX / 2)
+    return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return Q4_OK;
+  if (!qa || !sa || !w_codes || !w_scales_kn || !C || !aligned(qa, 16) || !aligned(w_codes, 16) ||
+      !aligned(w_scales_kn, 16) || !aligned(C, 16) || !aligned(sa, 4))
+    return Q4_ERR_INVALID_ARG;
+  return launch_w4a8_gemm(qa, sa, w_codes, w_scales_kn, M, N, K, C, c_dtype,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
 q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            const int32_t* expert_offsets, const int32_t* row_token, int64_t R,
                            int E, const uint8_t* W_codes, const uint8_t* W_scales,

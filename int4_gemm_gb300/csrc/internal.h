@@ -91,6 +91,14 @@ q4_status launch_fp8_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb,
                           int64_t M, int64_t N, int64_t K, void* C, int c_dtype,
                           cudaStream_t stream);
 
+// W4A8: FP8 activations x INT4 g128 weights on the FP8 tensor cores; wsc is the
+// FP32 [K/128, N] copy of the FP16 weight scales (launch_w4a8_scales).
+q4_status launch_w4a8_scales(const uint16_t* s16, int64_t N, int64_t KB, float* out,
+                             cudaStream_t stream);
+q4_status launch_w4a8_gemm(const uint8_t* qa, const float* sa, const uint8_t* wq, const float* wsc,
+                           int64_t M, int64_t N, int64_t K, void* C, int c_dtype,
+                           cudaStream_t stream);
+
 // TMA descriptor creation through the driver entry point.
 q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,

@@ -1,0 +1,408 @@
+// W4A8: INT4 g128 weights, FP8 (E4M3) activations, FP8 tensor cores.
+//
+// "Low-bit inference for very large MoE", section "Kernels on different
+// hardware", the W4A8 row: the INT4 weights are turned into FP8, the
+// activations are quantized to FP8 and the product runs on the FP8 tensor
+// cores.  Every INT4 value -8..7 is an E4M3 value, so the conversion is
+// exact, and the FP16 group scale (one per 128 along K) lines up with the
+// 128-wide K blocks of the block-promoted FP8 product:
+//   C[m, n] = sum_kb sa[m, kb] * s16[n, kb] * sum_{k in kb} qa[m, k] * q[n, k]
+// (activations from quantize_fp8_blockwise with (1, 128) blocks).
+//
+// The kernel is the block-promoted FP8 GEMM with the B operand kept 4-bit in
+// HBM (one CTA per SM, persistent over 128 x 128 tiles in bands of 32 M tiles):
+//   warp 0      TMA producer: the A tile (E4M3, 128-byte swizzle) and the INT4
+//               tile (128 rows x 64 bytes, unswizzled) of each K block into a
+//               5-stage ring, and the K block's 128 weight scales (FP32, from
+//               the [K/128, N] copy made by w4a8_weight_scales) into a 16-deep
+//               ring of scale buffers;
+//   warps 2, 3  converters: each thread expands the nibbles of two B rows to
+//               E4M3 bytes (a 16-entry byte-permute table) and writes them in
+//               the 128-byte-swizzled layout the MMA reads;
+//   warp 1      MMA issuer: four tcgen05.mma kind::f8f6f4 per K block into one
+//               of four 128-column TMEM slots;
+//   warps 4..11 promotion: slot * s16[n, kb] * sa[m, kb] into 64 FP32 registers
+//               per thread; the tile's rows are stored after its last K block.
+// A scale buffer is refilled only after the promotion of the K block that last
+// used it has finished: the producer of K block g waits for the MMAs of block
+// g - 5 to complete, which were issued after the promotion warps read the
+// buffers of block g - 9 and released its TMEM slot.
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+
+namespace q4 {
+namespace {
+
+constexpr int WBM = 128, WBN = 128, WBK = 128;
+constexpr int kWStages = 5;
+constexpr int kWSlots = 4;                            // TMEM accumulator slots, 128 columns each
+constexpr int kScaleBufs = 16;                        // weight-scale buffers, one K block each
+constexpr int kBandM = 32;                            // M tiles per band of the tile order
+constexpr uint32_t kATileBytes = WBM * WBK;           // E4M3 A tile
+constexpr uint32_t kBTileBytes = WBN * WBK;           // E4M3 B tile after conversion
+constexpr uint32_t kBCodeBytes = WBN * WBK / 2;       // INT4 B tile as loaded
+constexpr uint32_t kWStageBytes = kATileBytes + kBTileBytes + kBCodeBytes;
+constexpr uint32_t kScaleBufBytes = WBN * sizeof(float);
+constexpr int kConvWarp0 = 2, kConvWarps = 2;
+constexpr int kPromWarp0 = 4, kPromWarps = 8;
+constexpr int kWThreads = (kPromWarp0 + kPromWarps) * 32;
+constexpr uint32_t kWSmemBytes =
+    kWStages * kWStageBytes + kScaleBufs * kScaleBufBytes + 1024 /*align*/ + 512 /*barriers*/;
+static_assert(kWStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+static_assert(kWSmemBytes <= 232448, "shared memory");
+static_assert(kWSlots * WBN <= 512, "TMEM columns");
+static_assert(kConvWarps * 2 * 32 == WBN, "two B rows per converter thread");
+
+struct WSmem {
+  uint64_t full[kWStages];      // A tile and INT4 tile landed
+  uint64_t b_ready[kWStages];   // B tile converted (one arrival per converter warp)
+  uint64_t empty[kWStages];     // the stage's MMAs are done
+  uint64_t slot_full[kWSlots];
+  uint64_t slot_empty[kWSlots];
+  uint64_t sc_full[kScaleBufs];  // a K block's weight scales landed
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(WSmem) <= 512, "barrier block");
+
+struct W4a8Params {
+  int64_t M, N, K;
+  const float* sa;   // [M, K / 128]
+  const float* wsc;  // [K / 128, N]
+  void* C;           // [M, N]
+  int c_dtype;
+  int num_m, num_n;
+  KernelCtl ctl;
+};
+
+// tcgen05.mma kind::f8f6f4 descriptor: FP32 accumulator (bits 4-5 = 1), A and B
+// E4M3 (format 0), both K-major, N / 8 in bits 17-22, M / 16 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(WBN >> 3) << 17) | ((uint32_t)(WBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// E4M3 bytes of the eight two's complement INT4 nibbles of w (nibble j ->
+// byte j of the pair).  The low three bits of a nibble index the byte tables
+// of q = 0..7 and of q = -8..-1; a byte permute in sign-replicate mode turns
+// each nibble's sign bit into a byte mask that picks between them.
+__device__ __forceinline__ uint2 int4x8_to_e4m3(uint32_t w) {
+  constexpr uint32_t kPos0 = 0x44403800u;  // 0, 1, 2, 3  -> 0x00 0x38 0x40 0x44
+  constexpr uint32_t kPos1 = 0x4E4C4A48u;  // 4, 5, 6, 7  -> 0x48 0x4A 0x4C 0x4E
+  constexpr uint32_t kNeg0 = 0xCACCCED0u;  // -8, -7, -6, -5 -> 0xD0 0xCE 0xCC 0xCA
+  constexpr uint32_t kNeg1 = 0xB8C0C4C8u;  // -4, -3, -2, -1 -> 0xC8 0xC4 0xC0 0xB8
+  const uint32_t wl = w << 4;  // the sign bit of nibble 2i at bit 7 of byte i
+  uint2 r;
+  uint32_t sel = w & 0x7777u;
+  uint32_t msk = prmt(wl, w, 0xD9C8u);  // nibbles 0..3: bytes 0, 4, 1, 5, sign-replicated
+  r.x = (prmt(kPos0, kPos1, sel) & ~msk) | (prmt(kNeg0, kNeg1, sel) & msk);
+  sel = (w >> 16) & 0x7777u;
+  msk = prmt(wl, w, 0xFBEAu);  // nibbles 4..7: bytes 2, 6, 3, 7, sign-replicated
+  r.y = (prmt(kPos0, kPos1, sel) & ~msk) | (prmt(kNeg0, kNeg1, sel) & msk);
+  return r;
+}
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    w4a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                     const __grid_constant__ CUtensorMap tmap_w, const W4a8Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  pdl_wait();  // operands and scales may come from the previous kernel
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  float* sbuf = reinterpret_cast<float*>(smem + kWStages * kWStageBytes);
+  WSmem* sm = reinterpret_cast<WSmem*>(smem + kWStages * kWStageBytes + kScaleBufs * kScaleBufBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = (int)(p.K / WBK);
+  const int total_tiles = p.num_m * p.num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->b_ready[s]), kConvWarps);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int s = 0; s < kWSlots; ++s) {
+      mbar_init(smem_u32(&sm->slot_full[s]), 1);
+      mbar_init(smem_u32(&sm->slot_empty[s]), kPromWarps);
+    }
+    for (int b = 0; b < kScaleBufs; ++b) mbar_init(smem_u32(&sm->sc_full[b]), 1);
+    mbar_init(smem_u32(&sm->mma_done), 1);
+    sm->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), kWSlots * WBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort_flag = &sm->abort;
+  // bands of kBandM M tiles (a 33.5 MB slice of A at K = 8192 stays in L2), M
+  // fastest inside a band
+  auto tile_mn = [&](int t, int& m0, int& n0) {
+    const int band_tiles = kBandM * p.num_n;
+    const int band = t / band_tiles, r = t - band * band_tiles;
+    const int gm = min(kBandM, p.num_m - band * kBandM);
+    m0 = (band * kBandM + r % gm) * WBM;
+    n0 = (r / gm) * WBN;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0, gk = 0;
+    int issued[kWStages];
+    uint32_t issued_phase[kWStages];
+    for (int s = 0; s < kWStages; ++s) issued[s] = 0, issued_phase[s] = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      for (int kb = 0; kb < KB; ++kb, ++gk) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint8_t* st = smem + stage * kWStageBytes;
+        if (lane == 0) {
+          const uint32_t full = smem_u32(&sm->full[stage]);
+          mbar_arrive_expect_tx(full, kATileBytes + kBCodeBytes);
+          tma_load_2d(smem_u32(st), &tmap_a, kb * WBK, m0, full);
+          tma_load_2d(smem_u32(st + kATileBytes + kBTileBytes), &tmap_w, kb * (WBK / 2), n0, full);
+          const uint32_t b = gk % kScaleBufs;
+          const uint32_t scb = smem_u32(&sm->sc_full[b]);
+          mbar_arrive_expect_tx(scb, kScaleBufBytes);
+          bulk_load(smem_u32(sbuf + b * WBN), p.wsc + (int64_t)kb * p.N + n0, kScaleBufBytes, scb);
+        }
+        issued[stage] = 1;
+        issued_phase[stage] = phase;
+        if (++stage == kWStages) stage = 0, phase ^= 1;
+      }
+    }
+    // drain: every copy this warp issued has landed before the CTA exits (the
+    // scale copies of the last kScaleBufs K blocks; older ones were waited for
+    // by the promotion warps or by this loop's stage waits)
+    if (lane == 0) {
+      KernelCtl drain = p.ctl;
+      for (int s = 0; s < kWStages; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
+      for (uint32_t g = gk > (uint32_t)kScaleBufs ? gk - kScaleBufs : 0u; g < gk; ++g)
+        mbar_wait(smem_u32(&sm->sc_full[g % kScaleBufs]), (g / kScaleBufs) & 1, drain, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, gk = 0;
+      bool alive = true;
+      for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++gk) {
+          const uint32_t slot = gk % kWSlots, sphase = (gk / kWSlots) & 1;
+          // b_ready implies full: the converters waited for the stage's copies
+          if (!mbar_wait(smem_u32(&sm->slot_empty[slot]), sphase ^ 1, p.ctl, abort_flag) ||
+              !mbar_wait(smem_u32(&sm->b_ready[stage]), phase, p.ctl, abort_flag)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * kWStageBytes);
+          const uint32_t d = tmem + slot * WBN;
+#pragma unroll
+          for (uint32_t k = 0; k < WBK / 32; ++k)
+            mma_e4m3(d, smem_desc(st + 32 * k, 16, 1024, 2),
+                     smem_desc(st + kATileBytes + 32 * k, 16, 1024, 2), k != 0 ? 1u : 0u);
+          tc_commit(smem_u32(&sm->empty[stage]));
+          tc_commit(smem_u32(&sm->slot_full[slot]));
+          if (++stage == kWStages) stage = 0, phase ^= 1;
+        }
+      }
+      tc_commit(smem_u32(&sm->mma_done));
+      KernelCtl drain = p.ctl;
+      mbar_wait(smem_u32(&sm->mma_done), 0, drain, nullptr);
+    }
+    __syncwarp();
+  } else if (warp < kPromWarp0) {
+    // ------------------------------------------------------------ converters
+    // thread (warp c, lane l) converts B rows 64 c + l and 64 c + 32 + l; the
+    // 16-byte chunk j of row r goes to r * 128 + ((j ^ (r % 8)) * 16), the
+    // 128-byte swizzle the MMA's shared-memory descriptors describe
+    const int cw = warp - kConvWarp0;
+    uint32_t stage = 0, phase = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint8_t* st = smem + stage * kWStageBytes;
+        const uint8_t* src = st + kATileBytes + kBTileBytes;
+        uint8_t* dst = st + kATileBytes;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = cw * 64 + rr * 32 + lane;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // 16 code bytes = output chunks 2i and 2i + 1
+            const uint4 w = *reinterpret_cast<const uint4*>(src + r * 64 + i * 16);
+            const uint2 e0 = int4x8_to_e4m3(w.x), e1 = int4x8_to_e4m3(w.y);
+            const uint2 e2 = int4x8_to_e4m3(w.z), e3 = int4x8_to_e4m3(w.w);
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i) ^ (r & 7)) << 4)) =
+                make_uint4(e0.x, e0.y, e1.x, e1.y);
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i + 1) ^ (r & 7)) << 4)) =
+                make_uint4(e2.x, e2.y, e3.x, e3.y);
+          }
+        }
+        fence_proxy_async_smem();  // the tensor cores read what these threads wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->b_ready[stage]));
+        if (++stage == kWStages) stage = 0, phase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ promotion + store
+    const int q = warp & 3;                   // TMEM lane quarter this warp may access
+    const int h = (warp - kPromWarp0) >> 2;   // column half of the slot
+    const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16) + h * 64;
+    uint32_t gk = 0;
+    bool alive = true;
+    for (int t = blockIdx.x; t < total_tiles && alive; t += gridDim.x) {
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      const int64_t row = m0 + q * 32 + lane;
+      const bool row_ok = row < p.M;
+      const float* sa_row = p.sa + (row_ok ? row : p.M - 1) * KB;
+      float acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+      float sa_n = __ldg(sa_row);
+      for (int kb = 0; kb < KB; ++kb, ++gk) {
+        const uint32_t slot = gk % kWSlots, sphase = (gk / kWSlots) & 1;
+        const uint32_t b = gk % kScaleBufs;
+        const float sa_k = sa_n;
+        if (kb + 1 < KB) sa_n = __ldg(sa_row + kb + 1);
+        if (!mbar_wait(smem_u32(&sm->slot_full[slot]), sphase, p.ctl, abort_flag) ||
+            !mbar_wait(smem_u32(&sm->sc_full[b]), (gk / kScaleBufs) & 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(t_lane + slot * WBN, r0);
+        tmem_ld_32x32b_x32(t_lane + slot * WBN + 32, r1);
+        tmem_ld_wait();
+        const float4* sw = reinterpret_cast<const float4*>(sbuf + b * WBN + h * 64);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 s0 = sw[v], s1 = sw[8 + v];
+          acc[4 * v] = fmaf(__uint_as_float(r0[4 * v]) * s0.x, sa_k, acc[4 * v]);
+          acc[4 * v + 1] = fmaf(__uint_as_float(r0[4 * v + 1]) * s0.y, sa_k, acc[4 * v + 1]);
+          acc[4 * v + 2] = fmaf(__uint_as_float(r0[4 * v + 2]) * s0.z, sa_k, acc[4 * v + 2]);
+          acc[4 * v + 3] = fmaf(__uint_as_float(r0[4 * v + 3]) * s0.w, sa_k, acc[4 * v + 3]);
+          acc[32 + 4 * v] = fmaf(__uint_as_float(r1[4 * v]) * s1.x, sa_k, acc[32 + 4 * v]);
+          acc[32 + 4 * v + 1] = fmaf(__uint_as_float(r1[4 * v + 1]) * s1.y, sa_k, acc[32 + 4 * v + 1]);
+          acc[32 + 4 * v + 2] = fmaf(__uint_as_float(r1[4 * v + 2]) * s1.z, sa_k, acc[32 + 4 * v + 2]);
+          acc[32 + 4 * v + 3] = fmaf(__uint_as_float(r1[4 * v + 3]) * s1.w, sa_k, acc[32 + 4 * v + 3]);
+        }
+        // the slot goes back after the scale buffer has been read (its refill
+        // waits, through the MMA, for this arrival)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->slot_empty[slot]));
+      }
+      if (!alive || !row_ok) continue;
+      const int64_t col0 = n0 + h * 64;
+      if (p.c_dtype == Q4_BF16) {
+        uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.C) + row * p.N + col0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * v + 2 * i], acc[8 * v + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          out[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        float4* out = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + row * p.N + col0);
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+          out[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kWSlots * WBN);
+  }
+}
+
+// FP16 scale bits [N, KB] -> FP32 [KB, N] (the layout whose K-block rows the
+// GEMM copies whole).
+__global__ void __launch_bounds__(256)
+    w4a8_scales_kernel(const uint16_t* __restrict__ s16, int64_t N, int64_t KB, float* __restrict__ out) {
+  pdl_wait();
+  const int64_t n_all = N * KB;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_all;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t kb = i / N, n = i - kb * N;
+    out[i] = __half2float(__ushort_as_half(__ldg(s16 + n * KB + kb)));
+  }
+}
+
+}  // namespace
+
+q4_status launch_w4a8_scales(const uint16_t* s16, int64_t N, int64_t KB, float* out,
+                             cudaStream_t stream) {
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(N * KB, 256), (int64_t)num_sms() * 8);
+  return launch_pdl(w4a8_scales_kernel, grid, 256, 0, stream, s16, N, KB, out);
+}
+
+q4_status launch_w4a8_gemm(const uint8_t* qa, const float* sa, const uint8_t* wq, const float* wsc,
+                           int64_t M, int64_t N, int64_t K, void* C, int c_dtype,
+                           cudaStream_t stream) {
+  CUtensorMap ta, tw;
+  q4_status st;
+  if ((st = make_tmap_2d_u8(&ta, qa, K, M, K, WBK, WBM, true)) != Q4_OK) return st;
+  if ((st = make_tmap_2d_u8(&tw, wq, K / 2, N, K / 2, WBK / 2, WBN, false)) != Q4_OK) return st;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
+  if (!attr_done[dev]) {
+    Q4_CUDA_TRY(cudaFuncSetAttribute(w4a8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kWSmemBytes));
+    attr_done[dev] = 1;
+  }
+  W4a8Params p;
+  p.M = M, p.N = N, p.K = K;
+  p.sa = sa, p.wsc = wsc, p.C = C, p.c_dtype = c_dtype;
+  p.num_m = (int)ceil_div(M, WBM), p.num_n = (int)(N / WBN);
+  p.ctl = KernelCtl{device_status_ptr(), wait_budget_ns()};
+  const int tiles = p.num_m * p.num_n;
+  const unsigned grid = (unsigned)std::min(tiles, num_sms());
+  return launch_pdl(w4a8_gemm_kernel, grid, kWThreads, kWSmemBytes, stream, ta, tw, p);
+}
+
+}  // namespace q4

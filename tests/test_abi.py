@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["quantize_nvfp4", "quantize_mxfp4", "quantize_int4_g128", "gemm_w4a4_nvfp4",
                  "gemm_w4a4_mxfp4", "gemm_w4a16_int4", "gemm_w4a16_nvfp4", "gemm_w4a16_mxfp4",
-                 "grouped_gemm_moe", "q4_sync_status", "quantize_fp8_blockwise", "gemm_fp8_blockwise",
+                 "grouped_gemm_moe", "q4_sync_status", "quantize_fp8_blockwise", "gemm_fp8_blockwise", "gemm_w4a8", "w4a8_weight_scales",
                  "q4_workspace_size", "q4_scales_to_mma"]:
         assert want in names
 
@@ -69,6 +69,14 @@ def test_host_argument_checks(clib):
     assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 128, 128, fake, 2, None) == -1
     assert clib.gemm_fp8_blockwise(fake + 4, fake, fake, fake, 4, 128, 128, fake, 1, None) == -1
     assert clib.gemm_fp8_blockwise(None, fake, fake, fake, 0, 128, 128, fake, 1, None) == 0
+    # W4A8: K % 128, N % 128, misaligned weight scales or output, bad output dtype
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 100, fake, 1, None) == -2
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 100, 128, fake, 1, None) == -2
+    assert clib.gemm_w4a8(fake, fake, fake, fake + 4, 4, 128, 128, fake, 1, None) == -1
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 128, fake + 8, 1, None) == -1
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 128, fake, 2, None) == -1
+    assert clib.w4a8_weight_scales(fake, 4, 100, fake, None) == -2
+    assert clib.w4a8_weight_scales(fake + 1, 4, 128, fake, None) == -1
     assert clib.gemm_w4a16_nvfp4(fake, fake, fake + 1, fake, 4, 4, 128, fake, None) == -1
     assert clib.gemm_w4a16_mxfp4(None, fake, fake, 4, 4, 128, fake, None) == -1
     # an unknown rounding mode
