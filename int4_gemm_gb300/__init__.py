@@ -115,6 +115,16 @@ def _cuda2d(x: torch.Tensor, name: str) -> torch.Tensor:
     return x
 
 
+def _out(out: Optional[torch.Tensor], M: int, N: int, dtype: torch.dtype, device) -> torch.Tensor:
+    """A new [M, N] output, or the caller's, checked against the call."""
+    if out is None:
+        return torch.empty((M, N), dtype=dtype, device=device)
+    if (tuple(out.shape) != (M, N) or out.dtype != dtype or out.device != torch.device(device)
+            or not out.is_contiguous()):
+        raise ValueError(f"out must be a contiguous {dtype} tensor of shape ({M}, {N}) on {device}")
+    return out
+
+
 def _empty(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 0), dtype=torch.uint8, device=device)
 
@@ -202,20 +212,25 @@ class Fp4Operand:
     tensor_scale: Optional[torch.Tensor] = None
 
 
-def _operand(x: Union[torch.Tensor, Fp4Operand]) -> tuple[_Operand, int]:
+def _operand(x: Union[torch.Tensor, Fp4Operand], K: int) -> tuple[_Operand, int]:
     if isinstance(x, Fp4Operand):
+        _cuda2d(x.codes, "operand codes")
+        if x.codes.shape[1] * 2 != K:
+            raise ValueError(f"operand codes hold K = {x.codes.shape[1] * 2}, not {K}")
         return _Operand(None, 0, x.codes.data_ptr(), x.scales.data_ptr(), _LAYOUT[x.scale_layout],
                         _ptr(x.tensor_scale)), x.codes.shape[0]
     _cuda2d(x, "operand")
+    if x.shape[1] != K:
+        raise ValueError(f"operand has K = {x.shape[1]}, not {K}")
     return _Operand(x.data_ptr(), _DTYPE[x.dtype], None, None, 0, None), x.shape[0]
 
 
 def _gemm_fp4(fn: str, op: int, A, B, K: int, out_dtype: torch.dtype, stream=None, ws=None,
               out=None) -> torch.Tensor:
-    a, M = _operand(A)
-    b, N = _operand(B)
+    a, M = _operand(A, K)
+    b, N = _operand(B, K)
     dev = (A.codes if isinstance(A, Fp4Operand) else A).device
-    C = torch.empty((M, N), dtype=out_dtype, device=dev) if out is None else out
+    C = _out(out, M, N, out_dtype, dev)
     if ws is None:
         ws = workspace(op, M, N, K, dev)
     _check(fn, getattr(lib(), fn)(ctypes.byref(a), ctypes.byref(b), M, N, K, C.data_ptr(),
@@ -242,10 +257,11 @@ def gemm_w4a4_nvfp4_noalloc(A: torch.Tensor, B: Fp4Operand, K: int, out_dtype=to
     workspace: the quantized activations go to the library's fixed 16 MiB
     per-GPU scratch array (see include/q4gemm.h).  B must carry MMA-layout
     scales.  Calls that overlap on the GPU share that scratch and race."""
-    _cuda2d(A, "A")
-    M = A.shape[0]
-    b, N = _operand(B)
-    C = torch.empty((M, N), dtype=out_dtype, device=A.device) if out is None else out
+    if not isinstance(A, torch.Tensor):
+        raise ValueError("A must be the raw activation tensor")
+    _, M = _operand(A, K)
+    b, N = _operand(B, K)
+    C = _out(out, M, N, out_dtype, A.device)
     _check("gemm_w4a4_nvfp4_noalloc", lib().gemm_w4a4_nvfp4_noalloc(
         A.data_ptr(), _DTYPE[A.dtype], ctypes.byref(b), M, N, K, C.data_ptr(), _DTYPE[out_dtype],
         _stream(stream)))
@@ -258,7 +274,7 @@ def gemm_w4a16_int4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=Non
     _cuda2d(A, "A")
     M, K = A.shape
     N = Wq.shape[0]
-    C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    C = _out(out, M, N, torch.bfloat16, A.device)
     _check("gemm_w4a16_int4", lib().gemm_w4a16_int4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(), M,
                                                      N, K, C.data_ptr(), None, 0, _stream(stream)))
     return C
@@ -271,7 +287,7 @@ def gemm_w4a16_nvfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, Wg: to
     _cuda2d(A, "A")
     M, K = A.shape
     N = Wq.shape[0]
-    C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    C = _out(out, M, N, torch.bfloat16, A.device)
     _check("gemm_w4a16_nvfp4", lib().gemm_w4a16_nvfp4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(),
                                                        Wg.data_ptr(), M, N, K, C.data_ptr(),
                                                        _stream(stream)))
@@ -285,7 +301,7 @@ def gemm_w4a16_mxfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=No
     _cuda2d(A, "A")
     M, K = A.shape
     N = Wq.shape[0]
-    C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device) if out is None else out
+    C = _out(out, M, N, torch.bfloat16, A.device)
     _check("gemm_w4a16_mxfp4", lib().gemm_w4a16_mxfp4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(),
                                                        M, N, K, C.data_ptr(), _stream(stream)))
     return C
@@ -316,7 +332,7 @@ def gemm_fp8_blockwise(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb:
     _cuda2d(qa, "qa")
     M, K = qa.shape
     N = qb.shape[0]
-    C = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
+    C = _out(out, M, N, out_dtype if out is None else out.dtype, qa.device)
     _check("gemm_fp8_blockwise", lib().gemm_fp8_blockwise(
         qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), M, N, K, C.data_ptr(),
         _DTYPE[C.dtype], _stream(stream)))
@@ -342,7 +358,7 @@ def gemm_w4a8(qa: torch.Tensor, sa: torch.Tensor, w_codes: torch.Tensor, w_scale
     _cuda2d(qa, "qa")
     M, K = qa.shape
     N = w_codes.shape[0]
-    C = torch.empty((M, N), dtype=out_dtype, device=qa.device) if out is None else out
+    C = _out(out, M, N, out_dtype if out is None else out.dtype, qa.device)
     _check("gemm_w4a8", lib().gemm_w4a8(
         qa.data_ptr(), sa.data_ptr(), w_codes.data_ptr(), w_scales_kn.data_ptr(), M, N, K,
         C.data_ptr(), _DTYPE[C.dtype], _stream(stream)))
@@ -363,7 +379,7 @@ def grouped_gemm_moe(tokens: torch.Tensor, expert_offsets: torch.Tensor, row_tok
     T, K = tokens.shape
     E = expert_offsets.numel() - 1
     R = row_token.numel()
-    C = torch.empty((R, N), dtype=torch.bfloat16, device=tokens.device) if out is None else out
+    C = _out(out, R, N, torch.bfloat16, tokens.device)
     if ws is None:
         ws = moe_workspace(T, N, K, E, R, tokens.device)
     _check("grouped_gemm_moe", lib().grouped_gemm_moe(

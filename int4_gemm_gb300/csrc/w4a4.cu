@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       }
     }
   }
-  // no CTA leaves while a peer may still multicast into it, arrive on its
+  // no CTA leaves while its peer may still commit to it, arrive on its
   // barriers or read its shared memory
   if constexpr (CL > 1) cluster_barrier_sync();
 }

@@ -94,8 +94,10 @@ def test_prefill_nvfp4_sampled_rows(lib):
     # the benchmark's configuration: A raw (quantized on the fly), B pre-quantized
     bmma = lib.scales_to_mma(bs)
     C = lib.gemm_w4a4_nvfp4(ad, q4.Fp4Operand(bc, bmma, "mma", bg), K, out_dtype=torch.bfloat16)
-    rows = np.random.default_rng(0).choice(M, 12, replace=False)
-    rows = np.concatenate([rows, [0, M - 1]])
+    # one random row in every 128-row half of every 256-row M tile pair, and
+    # the first and last rows
+    rows = np.arange(0, M, 128) + np.random.default_rng(0).integers(0, 128, M // 128)
+    rows = np.unique(np.concatenate([rows, [0, M - 1]]))
     b_hat = oracle.dequantize_nvfp4(*ob)
     a_hat = oracle.dequantize_nvfp4(oa[0][rows], oa[1][rows], oa[2])
     R = a_hat @ b_hat.T
@@ -104,32 +106,47 @@ def test_prefill_nvfp4_sampled_rows(lib):
 
 
 def test_grouped_full_sampled_experts(lib):
+    """Every non-empty expert of the grouped workload: its first and last
+    routed rows and four random ones, on eight sampled columns of every
+    128-column N tile; the largest expert in full."""
     seed = workloads.SEED_BASE + 5
     T, E, N, K = 4096, 64, 2048, 7168
     tok, _, offs, rt = workloads.grouped(seed, experts=False)
     R_rows = int(offs[-1])
     counts = np.diff(offs)
     assert counts[63] == 0 and counts.max() < 1300
+    largest = int(np.argmax(counts))
+    rng = np.random.default_rng(11)
+    cols = np.sort(np.concatenate([t * 128 + rng.choice(128, 8, replace=False)
+                                   for t in range(N // 128)]))
     wc = torch.empty((E, N, K // 2), dtype=torch.uint8, device="cuda")
     sfb = q4.mma_scales_bytes(N, K // 16)
     wsf = torch.empty(E * sfb, dtype=torch.uint8, device="cuda")
     wg = torch.empty(E, dtype=torch.float32, device="cuda")
-    check = [0, 17, 62]
-    oq = {}
+    b_hat = {}
     for e in range(E):
         w = workloads.expert_weight(seed, e, N, K)
         c, s, g = lib.quantize_nvfp4(torch.from_numpy(w).cuda(), scale_layout="mma")
         wc[e].copy_(c), wsf[e * sfb:(e + 1) * sfb].copy_(s), wg[e:e + 1].copy_(g)
-        if e in check:
-            oq[e] = oracle.quantize_nvfp4(w)
-            assert g.item() == float(oq[e][2])
+        if counts[e] == 0:
+            continue
+        oq = oracle.quantize_nvfp4(w, rows=None if e == largest else cols)
+        assert g.item() == float(oq[2])
+        b_hat[e] = oracle.dequantize_nvfp4(*oq)
+    assert len(b_hat) == int(np.count_nonzero(counts)) == 63
     C = lib.grouped_gemm_moe(tok.cuda(), torch.from_numpy(offs).cuda(), torch.from_numpy(rt).cuda(),
                              wc, wsf, wg, N)
     assert C.shape == (R_rows, N)
+    Cf = C.float().cpu().numpy()
+    assert lib.sync_status() == 0
     qa = oracle.quantize_nvfp4(tok.float().numpy())
     a_hat = oracle.dequantize_nvfp4(*qa)
-    for e in check:
-        r0, r1 = offs[e], offs[e + 1]
-        Re = a_hat[rt[r0:r1]] @ oracle.dequantize_nvfp4(*oq[e]).T
-        assert_gemm_close(C[r0:r1].float().cpu().numpy(), Re)
-    assert lib.sync_status() == 0
+    for e, bh in b_hat.items():
+        r0, r1 = int(offs[e]), int(offs[e + 1])
+        if e == largest:
+            sel, ecols = np.arange(r0, r1), np.arange(N)
+        else:
+            inner = rng.choice(np.arange(r0, r1), min(4, r1 - r0), replace=False)
+            sel, ecols = np.unique(np.concatenate([[r0, r1 - 1], inner])), cols
+        Re = a_hat[rt[sel]] @ bh.T
+        assert_gemm_close(Cf[sel][:, ecols], Re)

@@ -12,8 +12,7 @@ import oracle
 import workloads
 from tests._util import assert_gemm_close
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="the W4A8 kernel has not yet had its first GPU run")]
+pytestmark = pytest.mark.gpu
 
 
 def _operands(M, N, K, seed):
