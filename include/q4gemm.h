@@ -83,7 +83,11 @@ typedef enum {
   Q4_OP_GEMM_W4A4_NVFP4 = 1, /* M, N, K; both operands given raw (the largest case) */
   Q4_OP_GEMM_W4A4_MXFP4 = 2,
   Q4_OP_GEMM_W4A16_INT4 = 3,
-  Q4_OP_GROUPED_GEMM_MOE = 4 /* M = number of tokens T, N, K; E and R via q4_workspace_size_moe */
+  Q4_OP_GROUPED_GEMM_MOE = 4, /* M = number of tokens T, N, K; E and R via q4_workspace_size_moe */
+  Q4_OP_GEMM_W4A16_NVFP4 = 5,
+  Q4_OP_GEMM_W4A16_MXFP4 = 6,
+  Q4_OP_GEMM_FP8_BLOCKWISE = 7, /* needs none today: 0 */
+  Q4_OP_GEMM_W4A8 = 8           /* needs none today: 0 */
 } q4_op;
 
 /*
@@ -200,7 +204,10 @@ q4_status gemm_w4a4_mxfp4(const q4_operand* A, const q4_operand* B, int64_t M, i
  * A_bf16 [M, K]; Wq [N, K/2] INT4 codes; Ws [N, K/128] FP16 bits (as written
  * by quantize_int4_g128); C_bf16 [M, N].  FP32 accumulation, one FP32
  * multiply by the scale per group of 128.  K % 128 == 0; any M >= 0 (tuned
- * for M <= 16).  Needs no workspace (ws may be NULL).
+ * for M <= 16).  Alignment: A and Wq 16 bytes, Ws and C 2 bytes.
+ * ws/ws_bytes: q4_workspace_size(Q4_OP_GEMM_W4A16_INT4, ...) is 0 today (the
+ * K-split partial sums meet in distributed shared memory), so ws may be NULL;
+ * the pair keeps every GEMM call alike.
  * Launched with programmatic dependent launch: it starts reading Wq and Ws
  * before the previous kernel in the stream has finished (A and C wait for
  * it).  Wq and Ws must not be written by a preceding kernel that releases its
@@ -225,15 +232,18 @@ q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t*
  * every product with an activation is exact; the sums are FP32, g is applied
  * once in FP32, and the only rounding to bf16 is the final store.
  * K % 128 == 0; any M >= 0 (tuned for M <= 16).  Alignment: A, Wq 16 bytes;
- * NVFP4 Ws 2 bytes, w_tensor_scale 4 bytes.  Launched like gemm_w4a16_int4
- * (programmatic dependent launch; Wq and Ws are read before the previous
- * kernel in the stream has finished, under the same rule as there).
+ * NVFP4 Ws 2 bytes, w_tensor_scale 4 bytes.  ws/ws_bytes as for
+ * gemm_w4a16_int4 (q4_workspace_size(Q4_OP_GEMM_W4A16_NVFP4 or _MXFP4, ...)
+ * is 0 today; ws may be NULL).  Launched like gemm_w4a16_int4 (programmatic
+ * dependent launch; Wq and Ws are read before the previous kernel in the
+ * stream has finished, under the same rule as there).
  */
 q4_status gemm_w4a16_nvfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws,
                            const float* w_tensor_scale, int64_t M, int64_t N, int64_t K,
-                           void* C_bf16, q4_stream_t stream);
+                           void* C_bf16, void* ws, size_t ws_bytes, q4_stream_t stream);
 q4_status gemm_w4a16_mxfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws, int64_t M,
-                           int64_t N, int64_t K, void* C_bf16, q4_stream_t stream);
+                           int64_t N, int64_t K, void* C_bf16, void* ws, size_t ws_bytes,
+                           q4_stream_t stream);
 
 /*
  * Grouped routed-MoE NVFP4 GEMM ("Low-bit inference for very large MoE",
@@ -284,12 +294,14 @@ q4_status quantize_fp8_blockwise(const void* x, int x_dtype, int64_t rows, int64
  * block_rows 1); qb: E4M3 [N, K] with sb float [N / 128, K / 128] (block_rows
  * 128).  C: [M, N] in c_dtype (Q4_F32, or Q4_BF16 rounded to nearest even),
  * 16-byte aligned.  K % 128 == 0, N % 128 == 0; any M.  qa and qb 16-byte
- * aligned.  Asynchronous; operands may come from the previous kernel in the
- * stream (programmatic dependent launch, read only after it has finished).
+ * aligned.  ws/ws_bytes: q4_workspace_size(Q4_OP_GEMM_FP8_BLOCKWISE, ...) is 0
+ * today, so ws may be NULL (the pair keeps every GEMM call alike).
+ * Asynchronous; operands may come from the previous kernel in the stream
+ * (programmatic dependent launch, read only after it has finished).
  */
 q4_status gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qb,
                              const float* sb, int64_t M, int64_t N, int64_t K, void* C,
-                             int c_dtype, q4_stream_t stream);
+                             int c_dtype, void* ws, size_t ws_bytes, q4_stream_t stream);
 
 /*
  * W4A8 ("Low-bit inference for very large MoE", "Kernels on different
@@ -302,13 +314,14 @@ q4_status gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* 
  * w_codes: [N, K/2] INT4 codes as quantize_int4_g128 writes them (16-byte
  * aligned).  w_scales_kn: float [K/128, N], the weight scales converted once
  * by w4a8_weight_scales (16-byte aligned).  C: [M, N] in c_dtype (Q4_F32 or
- * Q4_BF16), 16-byte aligned.  K % 128 == 0, N % 128 == 0; any M.
+ * Q4_BF16), 16-byte aligned.  K % 128 == 0, N % 128 == 0; any M.  ws/ws_bytes:
+ * q4_workspace_size(Q4_OP_GEMM_W4A8, ...) is 0 today, so ws may be NULL.
  */
 q4_status w4a8_weight_scales(const uint16_t* w_scales, int64_t N, int64_t K, float* w_scales_kn,
                              q4_stream_t stream);
 q4_status gemm_w4a8(const uint8_t* qa, const float* sa, const uint8_t* w_codes,
                     const float* w_scales_kn, int64_t M, int64_t N, int64_t K, void* C,
-                    int c_dtype, q4_stream_t stream);
+                    int c_dtype, void* ws, size_t ws_bytes, q4_stream_t stream);
 
 /*
  * gemm_w4a4_nvfp4 without a workspace, for callers that cannot give the

@@ -23,6 +23,8 @@ Q4_OK = 0
 F32, BF16, F16 = 0, 1, 2
 ROWMAJOR, MMA = 0, 1
 OP_QUANTIZE_NVFP4, OP_GEMM_W4A4_NVFP4, OP_GEMM_W4A4_MXFP4, OP_GEMM_W4A16_INT4 = 0, 1, 2, 3
+OP_GROUPED_GEMM_MOE, OP_GEMM_W4A16_NVFP4, OP_GEMM_W4A16_MXFP4 = 4, 5, 6
+OP_GEMM_FP8_BLOCKWISE, OP_GEMM_W4A8 = 7, 8
 
 _DTYPE = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
 _LAYOUT = {"rowmajor": ROWMAJOR, "mma": MMA}
@@ -73,13 +75,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "gemm_w4a4_nvfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "gemm_w4a4_mxfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "gemm_w4a16_int4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
-    _sig(lib, "gemm_w4a16_nvfp4", I, P, P, P, P, I64, I64, I64, P, P)
-    _sig(lib, "gemm_w4a16_mxfp4", I, P, P, P, I64, I64, I64, P, P)
+    _sig(lib, "gemm_w4a16_nvfp4", I, P, P, P, P, I64, I64, I64, P, P, SZ, P)
+    _sig(lib, "gemm_w4a16_mxfp4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
     _sig(lib, "grouped_gemm_moe", I, P, I64, I64, P, P, I64, I, P, P, P, I64, P, P, SZ, P)
     _sig(lib, "quantize_fp8_blockwise", I, P, I, I64, I64, I, P, P, P)
-    _sig(lib, "gemm_fp8_blockwise", I, P, P, P, P, I64, I64, I64, P, I, P)
+    _sig(lib, "gemm_fp8_blockwise", I, P, P, P, P, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "w4a8_weight_scales", I, P, I64, I64, P, P)
-    _sig(lib, "gemm_w4a8", I, P, P, P, P, I64, I64, I64, P, I, P)
+    _sig(lib, "gemm_w4a8", I, P, P, P, P, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "q4_sync_status", I, P)
     _sig(lib, "q4_status_string", ctypes.c_char_p, I)
     _sig(lib, "q4_set_wait_timeout_ms", I, I)
@@ -269,19 +271,21 @@ def gemm_w4a4_nvfp4_noalloc(A: torch.Tensor, B: Fp4Operand, K: int, out_dtype=to
 
 
 def gemm_w4a16_int4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=None,
-                    stream=None) -> torch.Tensor:
-    """C [M, N] bf16 = A [M, K] bf16 . dequant(Wq, Ws)^T."""
+                    stream=None, ws=None) -> torch.Tensor:
+    """C [M, N] bf16 = A [M, K] bf16 . dequant(Wq, Ws)^T.  ``ws``: optional
+    workspace (q4_workspace_size gives 0 for this call today)."""
     _cuda2d(A, "A")
     M, K = A.shape
     N = Wq.shape[0]
     C = _out(out, M, N, torch.bfloat16, A.device)
     _check("gemm_w4a16_int4", lib().gemm_w4a16_int4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(), M,
-                                                     N, K, C.data_ptr(), None, 0, _stream(stream)))
+                                                     N, K, C.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
+                                                     _stream(stream)))
     return C
 
 
 def gemm_w4a16_nvfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, Wg: torch.Tensor,
-                     out=None, stream=None) -> torch.Tensor:
+                     out=None, stream=None, ws=None) -> torch.Tensor:
     """C [M, N] bf16 = A [M, K] bf16 . dequant(W)^T, W NVFP4: codes [N, K/2],
     row-major E4M3 scales [N, K/16], tensor scale Wg (one float32)."""
     _cuda2d(A, "A")
@@ -290,12 +294,13 @@ def gemm_w4a16_nvfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, Wg: to
     C = _out(out, M, N, torch.bfloat16, A.device)
     _check("gemm_w4a16_nvfp4", lib().gemm_w4a16_nvfp4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(),
                                                        Wg.data_ptr(), M, N, K, C.data_ptr(),
+                                                       _ptr(ws), 0 if ws is None else ws.numel(),
                                                        _stream(stream)))
     return C
 
 
 def gemm_w4a16_mxfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=None,
-                     stream=None) -> torch.Tensor:
+                     stream=None, ws=None) -> torch.Tensor:
     """C [M, N] bf16 = A [M, K] bf16 . dequant(W)^T, W MXFP4: codes [N, K/2],
     row-major E8M0 scales [N, K/32]."""
     _cuda2d(A, "A")
@@ -303,7 +308,9 @@ def gemm_w4a16_mxfp4(A: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, out=No
     N = Wq.shape[0]
     C = _out(out, M, N, torch.bfloat16, A.device)
     _check("gemm_w4a16_mxfp4", lib().gemm_w4a16_mxfp4(A.data_ptr(), Wq.data_ptr(), Ws.data_ptr(),
-                                                       M, N, K, C.data_ptr(), _stream(stream)))
+                                                       M, N, K, C.data_ptr(), _ptr(ws),
+                                                       0 if ws is None else ws.numel(),
+                                                       _stream(stream)))
     return C
 
 
@@ -335,7 +342,7 @@ def gemm_fp8_blockwise(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb:
     C = _out(out, M, N, out_dtype if out is None else out.dtype, qa.device)
     _check("gemm_fp8_blockwise", lib().gemm_fp8_blockwise(
         qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), M, N, K, C.data_ptr(),
-        _DTYPE[C.dtype], _stream(stream)))
+        _DTYPE[C.dtype], None, 0, _stream(stream)))
     return C
 
 
@@ -361,7 +368,7 @@ def gemm_w4a8(qa: torch.Tensor, sa: torch.Tensor, w_codes: torch.Tensor, w_scale
     C = _out(out, M, N, out_dtype if out is None else out.dtype, qa.device)
     _check("gemm_w4a8", lib().gemm_w4a8(
         qa.data_ptr(), sa.data_ptr(), w_codes.data_ptr(), w_scales_kn.data_ptr(), M, N, K,
-        C.data_ptr(), _DTYPE[C.dtype], _stream(stream)))
+        C.data_ptr(), _DTYPE[C.dtype], None, 0, _stream(stream)))
     return C
 
 

@@ -98,6 +98,25 @@ q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_byt
   return r == CUDA_SUCCESS ? Q4_OK : Q4_ERR_CUDA;
 }
 
+// A byte tensor viewed as [d2][d1][d0] with element pitches s1 and s2 for d1
+// and d2 (d0 contiguous), boxes of b0 x b1 x b2, optionally 128-byte swizzled.
+q4_status make_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                          uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1,
+                          uint32_t b2, bool swizzle128) {
+  CUtensorMap dummy;
+  q4_status st = make_tmap_2d_u8(&dummy, base, 16, 1, 16, 16, 1, false);  // loads the encoder
+  if (st != Q4_OK) return st;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? Q4_OK : Q4_ERR_CUDA;
+}
+
 namespace {
 
 // Workspace plan of one FP4 GEMM operand given raw or with row-major scales.
@@ -271,8 +290,12 @@ size_t q4_workspace_size(int op, int64_t M, int64_t N, int64_t K) {
     case Q4_OP_QUANTIZE_NVFP4: return 256;
     case Q4_OP_GEMM_W4A4_NVFP4: return gemm_ws_bytes(M, N, K, 16);
     case Q4_OP_GEMM_W4A4_MXFP4: return gemm_ws_bytes(M, N, K, 32);
-    case Q4_OP_GEMM_W4A16_INT4: return 0;
+    case Q4_OP_GEMM_W4A16_INT4:
+    case Q4_OP_GEMM_W4A16_NVFP4:
+    case Q4_OP_GEMM_W4A16_MXFP4: return w4a16_workspace_bytes(M, N, K);
     case Q4_OP_GROUPED_GEMM_MOE: return 0;  // needs E and R: q4_workspace_size_moe
+    case Q4_OP_GEMM_FP8_BLOCKWISE:
+    case Q4_OP_GEMM_W4A8: return 0;
     default: return 0;
   }
 }
@@ -368,46 +391,54 @@ q4_status gemm_w4a4_mxfp4(const q4_operand* A, const q4_operand* B, int64_t M, i
   return gemm_fp4_common(false, A, B, M, N, K, C, c_dtype, ws, ws_bytes, stream);
 }
 
-q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t* Ws, int64_t M,
-                          int64_t N, int64_t K, void* C_bf16, void* ws, size_t ws_bytes,
-                          q4_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
+namespace {
+q4_status w4a16_check(const void* A_bf16, const uint8_t* Wq, const void* Ws, int64_t M, int64_t N,
+                      int64_t K, void* C_bf16, void* ws, size_t ws_bytes) {
   if (M < 0 || N < 0 || K <= 0) return Q4_ERR_INVALID_ARG;
   if (K % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
-  if (ceil_div(N, 128) > 65535 || ceil_div(M, 16) > 65535) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (ceil_div(M, 16) > 65535) return Q4_ERR_UNSUPPORTED_SHAPE;
   if (M == 0 || N == 0) return Q4_OK;
   if (!A_bf16 || !Wq || !Ws || !C_bf16 || !aligned(A_bf16, 16) || !aligned(Wq, 16) ||
-      !aligned(Ws, 2) || !aligned(C_bf16, 2))
+      !aligned(C_bf16, 2))
     return Q4_ERR_INVALID_ARG;
-  return launch_w4a16(A_bf16, Wq, Ws, M, N, K, C_bf16, reinterpret_cast<cudaStream_t>(stream));
+  const size_t need = w4a16_workspace_bytes(M, N, K);
+  if (need && (!ws || !aligned(ws, 256) || ws_bytes < need)) return Q4_ERR_WORKSPACE;
+  return Q4_OK;
+}
+}  // namespace
+
+q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t* Ws, int64_t M,
+                          int64_t N, int64_t K, void* C_bf16, void* ws, size_t ws_bytes,
+                          q4_stream_t stream) {
+  q4_status st = w4a16_check(A_bf16, Wq, Ws, M, N, K, C_bf16, ws, ws_bytes);
+  if (st != Q4_OK || M == 0 || N == 0) return st;
+  if (!aligned(Ws, 2)) return Q4_ERR_INVALID_ARG;
+  return launch_w4a16(A_bf16, Wq, Ws, M, N, K, C_bf16, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 static q4_status w4a16_fp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws,
                            const float* w_g, bool nvfp4, int64_t M, int64_t N, int64_t K,
-                           void* C_bf16, q4_stream_t stream) {
-  if (M < 0 || N < 0 || K <= 0) return Q4_ERR_INVALID_ARG;
-  if (K % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
-  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
-  if (ceil_div(N, 128) > 65535 || ceil_div(M, 16) > 65535) return Q4_ERR_UNSUPPORTED_SHAPE;
-  if (M == 0 || N == 0) return Q4_OK;
-  if (!A_bf16 || !Wq || !Ws || !C_bf16 || !aligned(A_bf16, 16) || !aligned(Wq, 16) ||
-      !aligned(C_bf16, 2) || (nvfp4 && (!w_g || !aligned(w_g, 4) || !aligned(Ws, 2))))
+                           void* C_bf16, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  if (nvfp4 && M > 0 && N > 0 && (!w_g || !aligned(w_g, 4) || !aligned(Ws, 2)))
     return Q4_ERR_INVALID_ARG;
-  return launch_w4a16_fp4(A_bf16, Wq, Ws, w_g, nvfp4, M, N, K, C_bf16,
+  q4_status st = w4a16_check(A_bf16, Wq, Ws, M, N, K, C_bf16, ws, ws_bytes);
+  if (st != Q4_OK || M == 0 || N == 0) return st;
+  return launch_w4a16_fp4(A_bf16, Wq, Ws, w_g, nvfp4, M, N, K, C_bf16, ws, ws_bytes,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 q4_status gemm_w4a16_nvfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws,
                            const float* w_tensor_scale, int64_t M, int64_t N, int64_t K,
-                           void* C_bf16, q4_stream_t stream) {
-  return w4a16_fp4(A_bf16, Wq, Ws, w_tensor_scale, true, M, N, K, C_bf16, stream);
+                           void* C_bf16, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  return w4a16_fp4(A_bf16, Wq, Ws, w_tensor_scale, true, M, N, K, C_bf16, ws, ws_bytes, stream);
 }
 
 q4_status gemm_w4a16_mxfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t* Ws, int64_t M,
-                           int64_t N, int64_t K, void* C_bf16, q4_stream_t stream) {
-  return w4a16_fp4(A_bf16, Wq, Ws, nullptr, false, M, N, K, C_bf16, stream);
+                           int64_t N, int64_t K, void* C_bf16, void* ws, size_t ws_bytes,
+                           q4_stream_t stream) {
+  return w4a16_fp4(A_bf16, Wq, Ws, nullptr, false, M, N, K, C_bf16, ws, ws_bytes, stream);
 }
 
 q4_status quantize_fp8_blockwise(const void* x, int x_dtype, int64_t rows, int64_t K,
@@ -426,7 +457,9 @@ q4_status quantize_fp8_blockwise(const void* x, int x_dtype, int64_t rows, int64
 
 q4_status gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qb,
                              const float* sb, int64_t M, int64_t N, int64_t K, void* C,
-                             int c_dtype, q4_stream_t stream) {
+                             int c_dtype, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  (void)ws;  // needs no workspace (q4_workspace_size gives 0)
+  (void)ws_bytes;
   if (M < 0 || N < 0 || K <= 0 || (c_dtype != Q4_F32 && c_dtype != Q4_BF16))
     return Q4_ERR_INVALID_ARG;
   if (K % 128 || N % 128) return Q4_ERR_UNSUPPORTED_SHAPE;
@@ -452,7 +485,9 @@ q4_status w4a8_weight_scales(const uint16_t* w_scales, int64_t N, int64_t K, flo
 
 q4_status gemm_w4a8(const uint8_t* qa, const float* sa, const uint8_t* w_codes,
                     const float* w_scales_kn, int64_t M, int64_t N, int64_t K, void* C,
-                    int c_dtype, q4_stream_t stream) {
+                    int c_dtype, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  (void)ws;  // needs no workspace (q4_workspace_size gives 0)
+  (void)ws_bytes;
   if (M < 0 || N < 0 || K <= 0 || (c_dtype != Q4_F32 && c_dtype != Q4_BF16))
     return Q4_ERR_INVALID_ARG;
   if (K % 128 || N % 128) return Q4_ERR_UNSUPPORTED_SHAPE;

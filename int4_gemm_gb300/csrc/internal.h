@@ -75,12 +75,14 @@ q4_status launch_gather_rows(const uint8_t* codes, const int32_t* row_token, int
                              int64_t row_bytes, uint8_t* out, cudaStream_t stream);
 q4_status launch_grouped_gemm(const GroupedArgs& a, cudaStream_t stream);
 
+// W4A16 decode GEMMs (w4a16_workspace_bytes is 0: they need no workspace).
+size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int64_t M, int64_t N,
-                       int64_t K, void* C, cudaStream_t stream);
+                       int64_t K, void* C, void* ws, size_t ws_bytes, cudaStream_t stream);
 // FP4 weights: Wsf row-major E4M3 (nvfp4, tensor scale *wg) or E8M0 bytes
 q4_status launch_w4a16_fp4(const void* A, const uint8_t* Wq, const uint8_t* Wsf, const float* wg,
-                           bool nvfp4, int64_t M, int64_t N, int64_t K, void* C,
-                           cudaStream_t stream);
+                           bool nvfp4, int64_t M, int64_t N, int64_t K, void* C, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
 
 // FP8 blockwise: block_rows 1 (activations, blocks (1, 128)) or 128 (weights,
 // 128 x 128); codes [rows, K] E4M3 bytes, scales FP32 row-major per block.
@@ -103,6 +105,12 @@ q4_status launch_w4a8_gemm(const uint8_t* qa, const float* sa, const uint8_t* wq
 q4_status make_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                           bool swizzle128);
+
+// A byte tensor viewed as [d2][d1][d0] (d0 contiguous; s1, s2 the byte
+// pitches of d1 and d2), boxes of b0 x b1 x b2.
+q4_status make_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                          uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1,
+                          uint32_t b2, bool swizzle128);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -512,14 +512,23 @@ q4_status launch_w4a16_fmt(const void* A, const uint8_t* Wq, const void* Wsc, co
 }
 }  // namespace
 
+// The decode kernel keeps its partial sums in distributed shared memory: no
+// workspace.
+size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)M, (void)N, (void)K;
+  return 0;
+}
+
 q4_status launch_w4a16(const void* A, const uint8_t* Wq, const uint16_t* Ws, int64_t M, int64_t N,
-                       int64_t K, void* C, cudaStream_t stream) {
+                       int64_t K, void* C, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws, (void)ws_bytes;
   return launch_w4a16_fmt<kInt4>(A, Wq, Ws, nullptr, M, N, K, C, stream);
 }
 
 q4_status launch_w4a16_fp4(const void* A, const uint8_t* Wq, const uint8_t* Wsf, const float* wg,
-                           bool nvfp4, int64_t M, int64_t N, int64_t K, void* C,
-                           cudaStream_t stream) {
+                           bool nvfp4, int64_t M, int64_t N, int64_t K, void* C, void* ws,
+                           size_t ws_bytes, cudaStream_t stream) {
+  (void)ws, (void)ws_bytes;
   return nvfp4 ? launch_w4a16_fmt<kNvfp4>(A, Wq, Wsf, wg, M, N, K, C, stream)
                : launch_w4a16_fmt<kMxfp4>(A, Wq, Wsf, nullptr, M, N, K, C, stream);
 }

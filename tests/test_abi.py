@@ -55,41 +55,42 @@ def test_host_argument_checks(clib):
     # NVFP4 quantize needs its workspace
     assert clib.quantize_nvfp4(fake, 1, 4, 64, fake, fake, 0, fake, None, 0, None) == -6
     # FP4-weight W4A16: K % 128, a missing tensor scale, misaligned NVFP4 scales
-    assert clib.gemm_w4a16_nvfp4(fake, fake, fake, fake, 4, 4, 100, fake, None) == -2
-    assert clib.gemm_w4a16_mxfp4(fake, fake, fake, 4, 4, 64, fake, None) == -2
-    assert clib.gemm_w4a16_nvfp4(fake, fake, fake, None, 4, 4, 128, fake, None) == -1
+    assert clib.gemm_w4a16_nvfp4(fake, fake, fake, fake, 4, 4, 100, fake, None, 0, None) == -2
+    assert clib.gemm_w4a16_mxfp4(fake, fake, fake, 4, 4, 64, fake, None, 0, None) == -2
+    assert clib.gemm_w4a16_nvfp4(fake, fake, fake, None, 4, 4, 128, fake, None, 0, None) == -1
     # FP8 blockwise: K % 128, N % 128, rows % 128 for weight blocks, bad block height,
     # bad output dtype, misaligned operands
     assert clib.quantize_fp8_blockwise(fake, 1, 4, 100, 1, fake, fake, None) == -2
     assert clib.quantize_fp8_blockwise(fake, 1, 100, 128, 128, fake, fake, None) == -2
     assert clib.quantize_fp8_blockwise(fake, 1, 4, 128, 2, fake, fake, None) == -1
     assert clib.quantize_fp8_blockwise(fake + 8, 1, 4, 128, 1, fake, fake, None) == -1
-    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 128, 100, fake, 1, None) == -2
-    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 100, 128, fake, 1, None) == -2
-    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 128, 128, fake, 2, None) == -1
-    assert clib.gemm_fp8_blockwise(fake + 4, fake, fake, fake, 4, 128, 128, fake, 1, None) == -1
-    assert clib.gemm_fp8_blockwise(None, fake, fake, fake, 0, 128, 128, fake, 1, None) == 0
+    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 128, 100, fake, 1, None, 0, None) == -2
+    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 100, 128, fake, 1, None, 0, None) == -2
+    assert clib.gemm_fp8_blockwise(fake, fake, fake, fake, 4, 128, 128, fake, 2, None, 0, None) == -1
+    assert clib.gemm_fp8_blockwise(fake + 4, fake, fake, fake, 4, 128, 128, fake, 1, None, 0, None) == -1
+    assert clib.gemm_fp8_blockwise(None, fake, fake, fake, 0, 128, 128, fake, 1, None, 0, None) == 0
     # W4A8: K % 128, N % 128, misaligned weight scales or output, bad output dtype
-    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 100, fake, 1, None) == -2
-    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 100, 128, fake, 1, None) == -2
-    assert clib.gemm_w4a8(fake, fake, fake, fake + 4, 4, 128, 128, fake, 1, None) == -1
-    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 128, fake + 8, 1, None) == -1
-    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 128, fake, 2, None) == -1
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 100, fake, 1, None, 0, None) == -2
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 100, 128, fake, 1, None, 0, None) == -2
+    assert clib.gemm_w4a8(fake, fake, fake, fake + 4, 4, 128, 128, fake, 1, None, 0, None) == -1
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 128, fake + 8, 1, None, 0, None) == -1
+    assert clib.gemm_w4a8(fake, fake, fake, fake, 4, 128, 128, fake, 2, None, 0, None) == -1
     assert clib.w4a8_weight_scales(fake, 4, 100, fake, None) == -2
     assert clib.w4a8_weight_scales(fake + 1, 4, 128, fake, None) == -1
-    assert clib.gemm_w4a16_nvfp4(fake, fake, fake + 1, fake, 4, 4, 128, fake, None) == -1
-    assert clib.gemm_w4a16_mxfp4(None, fake, fake, 4, 4, 128, fake, None) == -1
+    assert clib.gemm_w4a16_nvfp4(fake, fake, fake + 1, fake, 4, 4, 128, fake, None, 0, None) == -1
+    assert clib.gemm_w4a16_mxfp4(None, fake, fake, 4, 4, 128, fake, None, 0, None) == -1
     # an unknown rounding mode
     assert clib.quantize_mxfp4_ex(fake, 1, 4, 64, fake, fake, 0, 2, None) == -1
     assert clib.quantize_nvfp4_ex(fake, 1, 4, 64, fake, fake, 0, -1, fake, fake, 256, None) == -1
     # empty problems are no-ops
     assert clib.quantize_int4_g128(None, 1, 0, 128, None, None, None) == 0
     assert clib.gemm_w4a16_int4(None, None, None, 0, 4, 128, None, None, 0, None) == 0
-    assert clib.gemm_w4a16_mxfp4(None, None, None, 0, 4, 128, None, None) == 0
+    assert clib.gemm_w4a16_mxfp4(None, None, None, 0, 4, 128, None, None, 0, None) == 0
 
 
 def test_workspace_sizes(clib):
-    assert clib.q4_workspace_size(3, 16, 8192, 8192) == 0  # W4A16 needs none
+    for op in (3, 5, 6, 7, 8):  # W4A16 (INT4, NVFP4, MXFP4), FP8 blockwise, W4A8: none
+        assert clib.q4_workspace_size(op, 16, 8192, 8192) == 0
     n = clib.q4_workspace_size(1, 8192, 28672, 8192)
     assert n >= 8192 * 4096 + 28672 * 4096  # room for both operands' codes
     assert clib.q4_mma_scales_bytes(130, 5) == 256 * 8

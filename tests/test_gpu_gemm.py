@@ -137,8 +137,11 @@ def test_identity_operand(lib):
     assert np.allclose(C, want, rtol=1e-6, atol=0)
 
 
+# ragged N and M, odd group counts, one group, several blocks of 16 tokens, one
+# row block with a long K, many row blocks with a short K
 W4A16_SHAPES = [(1, 256, 1024), (4, 520, 2048), (16, 1000, 1152), (5, 128, 128),
-                (17, 300, 8192), (33, 256, 512), (16, 2048, 8192)]
+                (17, 300, 8192), (33, 256, 512), (16, 2048, 8192), (8, 128, 8192),
+                (3, 8192, 256), (2, 130, 384)]
 
 
 @pytest.mark.parametrize("shape", W4A16_SHAPES)
@@ -155,7 +158,7 @@ def test_w4a16_int4(lib, shape):
 
 
 W4A16_FP4_SHAPES = [(1, 256, 1024), (4, 520, 2048), (16, 1000, 1152), (5, 128, 128),
-                    (17, 300, 8192), (33, 256, 512)]
+                    (17, 300, 8192), (33, 256, 512), (8, 128, 8192), (3, 8192, 256)]
 
 
 def _fp4_weights(lib, w, fmt):
