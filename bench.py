@@ -11,7 +11,8 @@ pinned host memory and the outputs copied back every step.
 Other workloads (``--workload``): ``decode_nvfp4`` (the decode step with
 NVFP4 weights), ``prefill`` (NVFP4 W4A4, 8192 x 28672 x
 8192, A quantized on the fly), ``moe`` (MXFP4 W4A4, 256 x 2048 x 7168, A
-quantized on the fly), ``grouped`` (64-expert routed NVFP4 MoE),
+quantized on the fly), ``moe_fused`` (the same, A quantized in the GEMM's own
+prologue: one launch), ``grouped`` (64-expert routed NVFP4 MoE),
 ``quantize`` / ``quantize_rne`` (NVFP4 quantization of the prefill
 activations alone, E2M1 ties to the smaller magnitude / to even), ``tiny``.
 
@@ -533,6 +534,7 @@ class Moe(W4A4):
     default_steps = 5000
     kernel = "fp4_gemm_kernel"
     nvfp4 = False
+    launches_per_step = 2  # activation quantizer + GEMM
 
     def config(self):
         return {"workload": f"mxfp4_moe A bf16 {self.M}x{self.K} (0.5% channels x20, quantized on the fly), B MXFP4 {self.N}x{self.K}",
@@ -551,6 +553,39 @@ class Moe(W4A4):
     def oracle_units(self):
         m = min(self.M, 64)
         return m * self.K * 2 + self.o_rows * self.K // 2 + self.o_rows * self.K // 32 + m * self.o_rows * 2
+
+
+class MoeFused(Moe):
+    """The MoE shape through the single-launch call: the GEMM quantizes its
+    bf16 activations in its own prologue (no separate quantizer launch)."""
+    name = "mxfp4_moe_fused"
+    launches_per_step = 1
+    kernel_launches = 1
+
+    def config(self):
+        c = super().config()
+        c["workload"] = c["workload"].replace("quantized on the fly", "quantized in the GEMM prologue")
+        return c
+
+    def setup(self, q4, dev, seed, shape=None):
+        super().setup(q4, dev, seed, shape)
+        self.ws_fused = q4.workspace(q4.OP_GEMM_W4A4_MXFP4_FUSED, self.M, self.N, self.K, dev)
+
+    def step(self, i):
+        self.q4.gemm_w4a4_mxfp4_fused(self.A[i % len(self.A)], self.B[i % len(self.B)], self.K,
+                                      out=self.C, ws=self.ws_fused)
+
+    kernel_only = step
+
+    def kernel_units(self):
+        return self.bytes_per_step()  # the one launch reads raw A itself
+
+    def e2e_step(self, i):
+        self.A[0].copy_(self.A_pin, non_blocking=True)
+        self.q4.gemm_w4a4_mxfp4_fused(self.A[0], self.B[i % len(self.B)], self.K, out=self.C,
+                                      ws=self.ws_fused)
+        self.C_host.copy_(self.C, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
 
 
 class Fp8Blockwise:
@@ -769,13 +804,14 @@ class Grouped:
 
 
 WORKLOADS = {"decode": Decode, "decode_nvfp4": DecodeNvfp4, "prefill": Prefill, "moe": Moe,
+             "moe_fused": MoeFused,
              "grouped": Grouped, "quantize": QuantizeNvfp4, "quantize_rne": QuantizeNvfp4Rne,
              "fp8_blockwise": Fp8Blockwise, "w4a8": W4a8}
 DTYPES = {"decode": "bf16 (exact int4 values) x bf16 -> fp32",
           "decode_nvfp4": "bf16 (exact e2m1 x e4m3 values) x bf16 -> fp32",
           "quantize": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)", "quantize_rne": "bf16 -> e2m1 + e4m3 (fp32 arithmetic)",
           "prefill": "e2m1 x e2m1 -> fp32",
-          "moe": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32",
+          "moe": "e2m1 x e2m1 -> fp32", "moe_fused": "e2m1 x e2m1 -> fp32", "grouped": "e2m1 x e2m1 -> fp32",
           "fp8_blockwise": "e4m3 x e4m3 -> fp32 (block-promoted)",
           "w4a8": "e4m3 x int4 (exact e4m3) -> fp32 (block-promoted)"}
 
@@ -870,7 +906,7 @@ def wl_setup_host(wl, seed):
 
 
 SEEDS = {"decode": workloads.SEED_BASE + 2, "decode_nvfp4": workloads.SEED_BASE + 2,
-         "moe": workloads.SEED_BASE + 3,
+         "moe": workloads.SEED_BASE + 3, "moe_fused": workloads.SEED_BASE + 3,
          "prefill": workloads.SEED_BASE + 4, "grouped": workloads.SEED_BASE + 5,
          "quantize": workloads.SEED_BASE + 4, "quantize_rne": workloads.SEED_BASE + 4,
          "fp8_blockwise": workloads.SEED_BASE + 4, "w4a8": workloads.SEED_BASE + 4}

@@ -87,7 +87,8 @@ typedef enum {
   Q4_OP_GEMM_W4A16_NVFP4 = 5,
   Q4_OP_GEMM_W4A16_MXFP4 = 6,
   Q4_OP_GEMM_FP8_BLOCKWISE = 7, /* needs none today: 0 */
-  Q4_OP_GEMM_W4A8 = 8           /* needs none today: 0 */
+  Q4_OP_GEMM_W4A8 = 8,          /* needs none today: 0 */
+  Q4_OP_GEMM_W4A4_MXFP4_FUSED = 9
 } q4_op;
 
 /*
@@ -195,6 +196,31 @@ q4_status gemm_w4a4_nvfp4(const q4_operand* A, const q4_operand* B, int64_t M, i
 q4_status gemm_w4a4_mxfp4(const q4_operand* A, const q4_operand* B, int64_t M, int64_t N,
                           int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,
                           q4_stream_t stream);
+
+/*
+ * gemm_w4a4_mxfp4 with the activation quantization fused into the GEMM
+ * ("Low-bit inference for very large MoE", "Kernels on different hardware":
+ * the activations are quantized on the fly in the GEMM's prologue; the MXFP4
+ * encode of "Quantization in deployment", "Fake quantization", mxfp4).  One
+ * launch: every CTA first encodes its share of A's 32-element blocks into the
+ * workspace, all CTAs meet at a grid-wide gate, then the main loop runs as in
+ * gemm_w4a4_mxfp4 (results are bit-identical to it with A->raw = A_raw).
+ * A_raw: [M, K] in a_dtype (Q4_F32, Q4_BF16 or Q4_F16), 16-byte aligned.
+ * B, C, c_dtype, K, M, N: as for gemm_w4a4_mxfp4.
+ * ws: q4_workspace_size(Q4_OP_GEMM_W4A4_MXFP4_FUSED, M, N, K) bytes, 256-byte
+ *     aligned.  Its first 256 bytes hold the gate's counters: they must be
+ *     zero before the first call on this workspace (e.g. one cudaMemsetAsync
+ *     when it is allocated), and every call whose kernel finishes without an
+ *     error leaves them zero again, so no reset is needed between calls.
+ *     After a call that latched an error status, zero them again.  Calls
+ *     that share a workspace must be ordered (the same stream).
+ * Where the grid cannot be resident all at once (the gate needs every CTA
+ * running), or M * K / 16 >= 2^31, the call quantizes A in a separate pass
+ * first, with the same results.
+ */
+q4_status gemm_w4a4_mxfp4_fused(const void* A_raw, int a_dtype, const q4_operand* B, int64_t M,
+                                int64_t N, int64_t K, void* C, int c_dtype, void* ws,
+                                size_t ws_bytes, q4_stream_t stream);
 
 /*
  * W4A16 decode GEMM ("Low-bit inference for very large MoE", "Kernels on

@@ -25,6 +25,7 @@ ROWMAJOR, MMA = 0, 1
 OP_QUANTIZE_NVFP4, OP_GEMM_W4A4_NVFP4, OP_GEMM_W4A4_MXFP4, OP_GEMM_W4A16_INT4 = 0, 1, 2, 3
 OP_GROUPED_GEMM_MOE, OP_GEMM_W4A16_NVFP4, OP_GEMM_W4A16_MXFP4 = 4, 5, 6
 OP_GEMM_FP8_BLOCKWISE, OP_GEMM_W4A8 = 7, 8
+OP_GEMM_W4A4_MXFP4_FUSED = 9
 
 _DTYPE = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
 _LAYOUT = {"rowmajor": ROWMAJOR, "mma": MMA}
@@ -74,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     op = ctypes.POINTER(_Operand)
     _sig(lib, "gemm_w4a4_nvfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "gemm_w4a4_mxfp4", I, op, op, I64, I64, I64, P, I, P, SZ, P)
+    _sig(lib, "gemm_w4a4_mxfp4_fused", I, P, I, op, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "gemm_w4a16_int4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
     _sig(lib, "gemm_w4a16_nvfp4", I, P, P, P, P, I64, I64, I64, P, P, SZ, P)
     _sig(lib, "gemm_w4a16_mxfp4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
@@ -133,7 +135,10 @@ def _empty(nbytes: int, device) -> torch.Tensor:
 
 def workspace(op: int, M: int, N: int, K: int, device) -> torch.Tensor:
     n = lib().q4_workspace_size(op, M, N, K)
-    return _empty(max(n, 256), device)
+    ws = _empty(max(n, 256), device)
+    if op == OP_GEMM_W4A4_MXFP4_FUSED:
+        ws[:256].zero_()  # the grid gate's counters start at zero
+    return ws
 
 
 def mma_scales_bytes(rows: int, nsf: int) -> int:
@@ -251,6 +256,27 @@ def gemm_w4a4_nvfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None, ws=None
 def gemm_w4a4_mxfp4(A, B, K: int, out_dtype=torch.bfloat16, stream=None, ws=None,
                     out=None) -> torch.Tensor:
     return _gemm_fp4("gemm_w4a4_mxfp4", OP_GEMM_W4A4_MXFP4, A, B, K, out_dtype, stream, ws, out)
+
+
+def gemm_w4a4_mxfp4_fused(A: torch.Tensor, B, K: int, out_dtype=torch.bfloat16, stream=None,
+                          ws=None, out=None) -> torch.Tensor:
+    """gemm_w4a4_mxfp4 of a raw A in one launch: the GEMM quantizes A in its
+    prologue.  ``ws`` must come from ``workspace(OP_GEMM_W4A4_MXFP4_FUSED,
+    ...)`` (its first 256 bytes are the gate's counters, zero before the first
+    call; each call leaves them zero)."""
+    _cuda2d(A, "A")
+    if A.shape[1] != K:
+        raise ValueError(f"A has K = {A.shape[1]}, not {K}")
+    b, N = _operand(B, K)
+    M = A.shape[0]
+    C = _out(out, M, N, out_dtype, A.device)
+    if ws is None:
+        ws = workspace(OP_GEMM_W4A4_MXFP4_FUSED, M, N, K, A.device)
+    _check("gemm_w4a4_mxfp4_fused",
+           lib().gemm_w4a4_mxfp4_fused(A.data_ptr(), _DTYPE[A.dtype], ctypes.byref(b), M, N, K,
+                                       C.data_ptr(), _DTYPE[out_dtype], ws.data_ptr(), ws.numel(),
+                                       _stream(stream)))
+    return C
 
 
 def gemm_w4a4_nvfp4_noalloc(A: torch.Tensor, B: Fp4Operand, K: int, out_dtype=torch.bfloat16,

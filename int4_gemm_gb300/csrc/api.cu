@@ -290,6 +290,7 @@ size_t q4_workspace_size(int op, int64_t M, int64_t N, int64_t K) {
     case Q4_OP_QUANTIZE_NVFP4: return 256;
     case Q4_OP_GEMM_W4A4_NVFP4: return gemm_ws_bytes(M, N, K, 16);
     case Q4_OP_GEMM_W4A4_MXFP4: return gemm_ws_bytes(M, N, K, 32);
+    case Q4_OP_GEMM_W4A4_MXFP4_FUSED: return 256 + gemm_ws_bytes(M, N, K, 32);
     case Q4_OP_GEMM_W4A16_INT4:
     case Q4_OP_GEMM_W4A16_NVFP4:
     case Q4_OP_GEMM_W4A16_MXFP4: return w4a16_workspace_bytes(M, N, K);
@@ -389,6 +390,43 @@ q4_status gemm_w4a4_mxfp4(const q4_operand* A, const q4_operand* B, int64_t M, i
                           int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,
                           q4_stream_t stream) {
   return gemm_fp4_common(false, A, B, M, N, K, C, c_dtype, ws, ws_bytes, stream);
+}
+
+q4_status gemm_w4a4_mxfp4_fused(const void* A_raw, int a_dtype, const q4_operand* B, int64_t M,
+                                int64_t N, int64_t K, void* C, int c_dtype, void* ws,
+                                size_t ws_bytes, q4_stream_t stream) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M < 0 || N < 0 || K <= 0) return Q4_ERR_INVALID_ARG;
+  if (K % 256) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (c_dtype != Q4_F32 && c_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
+  if (a_dtype != Q4_F32 && a_dtype != Q4_BF16 && a_dtype != Q4_F16) return Q4_ERR_INVALID_ARG;
+  q4_status st;
+  if ((st = check_operand(B, N, false)) != Q4_OK) return st;
+  if (M == 0 || N == 0) return Q4_OK;
+  if (!A_raw || !aligned(A_raw, 16)) return Q4_ERR_INVALID_ARG;
+  if (!C || !aligned(C, 16)) return Q4_ERR_INVALID_ARG;
+  Carver c{static_cast<uint8_t*>(ws), ws_bytes, 0};
+  unsigned* gate = reinterpret_cast<unsigned*>(c.take(256));
+  const OperandPlan pa = plan_operand(c, M, K, 32, false);
+  const OperandPlan pb = plan_operand(c, N, K, 32, false);
+  if (!ws || !aligned(ws, 256) || !c.ok()) return Q4_ERR_WORKSPACE;
+  Fp4GemmArgs g = {};
+  if (M * (K / 16) < ((int64_t)1 << 31)) {  // the prologue's unit indices are 32-bit
+    g.a_raw = A_raw;
+    g.a_dtype = a_dtype;
+    g.a_codes = pa.codes;
+    g.a_scales = pa.sf;
+    g.gate = gate;
+  } else {
+    q4_operand a = {A_raw, a_dtype, nullptr, nullptr, Q4_SCALES_MMA, nullptr};
+    if ((st = resolve_operand(&a, M, K, false, pa, s, &g.a_codes, &g.a_scales, &g.a_g)) != Q4_OK)
+      return st;
+  }
+  if ((st = resolve_operand(B, N, K, false, pb, s, &g.b_codes, &g.b_scales, &g.b_g)) != Q4_OK)
+    return st;
+  g.M = M; g.N = N; g.K = K; g.C = C; g.c_dtype = c_dtype; g.nvfp4 = false;
+  return launch_fp4_gemm(g, s);
 }
 
 namespace {

@@ -51,6 +51,12 @@ struct Fp4GemmArgs {
   void* C;
   int c_dtype;
   bool nvfp4;  // true: E4M3 scales per 16; false: E8M0 per 32
+  // MXFP4 only: A given raw (a_raw, a_dtype); the GEMM quantizes it in its
+  // prologue into a_codes / a_scales (workspace) and counts its CTAs in
+  // *gate, which must be zero at launch
+  const void* a_raw = nullptr;
+  int a_dtype = 0;
+  unsigned* gate = nullptr;
 };
 q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream);
 

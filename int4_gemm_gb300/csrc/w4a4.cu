@@ -30,10 +30,23 @@
 // MMAs and each CTA's accumulator receives its 128 rows.  Each SM thus
 // receives half of the B tile per stage.  The odd CTA's scale writers and
 // epilogue warps report to the even CTA's barriers.
+// QA (MXFP4 with a raw A, gemm_w4a4_mxfp4_fused): the GEMM quantizes its
+// activations itself, in a prologue: warps 1-9 of every CTA encode that CTA's
+// share of A's 32-element blocks into the workspace (codes and
+// tensor-core-layout scales) and the CTA counts itself in a grid-wide gate;
+// meanwhile the producers already stream the first stages' B tiles and issue
+// the A copies once every CTA has passed the gate.  Each element is encoded
+// once; one launch replaces quantizer + GEMM.  The grid is never larger than
+// what is resident at once, so the gate is always reached; its wait is
+// bounded like every other.  The gate is two counters (arrivals, then
+// departures of the two waiting producers of every CTA); the last waiter to
+// leave sets both back to zero, so a workspace that starts at zero stays
+// ready for the next launch without a reset of its own.
 // Every wait is bounded: on timeout the CTA latches Q4_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and exits.
 #include "common.cuh"
 #include "internal.h"
+#include "quant_device.cuh"
 
 #include <algorithm>
 
@@ -122,8 +135,95 @@ struct Params {
   const int32_t* offsets;
   const int32_t* sched;
   int E;
+  // activations quantized in the prologue (QA): raw A, its dtype, where its
+  // codes and tensor-core-layout scales go, and the gate the CTAs count into
+  const void* a_raw;
+  int a_dtype;
+  uint8_t* a_codes_w;
+  uint8_t* a_sf_w;
+  unsigned* gate;
   KernelCtl ctl;
 };
+
+__device__ __forceinline__ void bar_sync_n(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Waits (bounded) until every CTA of the grid has counted itself in gate[0],
+// then orders the copies (async proxy) this thread issues next after the
+// other CTAs' generic-proxy stores it has now seen, and counts itself out in
+// gate[1]; the last of the grid's `waiters` to leave resets both counters
+// (nobody reads them any more in this launch, and the next launch on the
+// workspace reads them only after this one has completed).
+__device__ __forceinline__ bool wait_gate(unsigned* gate, unsigned target, unsigned waiters,
+                                          const KernelCtl& ctl, volatile int* abort_flag) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gate) : "memory");
+    if (v >= target) break;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > ctl.wait_ns) {
+      latch_status(ctl.status, Q4_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  if (atomicAdd(gate + 1, 1u) == waiters - 1) {
+    *reinterpret_cast<volatile unsigned*>(gate) = 0u;
+    *reinterpret_cast<volatile unsigned*>(gate + 1) = 0u;
+  }
+  return true;
+}
+
+// The QA prologue: this CTA's blocks [c B / G, (c + 1) B / G) of the M x K/32
+// MXFP4 blocks of A, one thread per 16 elements (a lane pair per block), by
+// threads t = 0 .. nthr - 1 (whole warps).  A CTA's share is small (a few
+// tens of KB), so its time is load latency: each thread first issues the
+// loads of up to kPU units, then encodes them.
+template <typename T>
+__device__ void mxfp4_prologue(const Params& p, int t, int nthr) {
+  constexpr int kPU = 4;
+  const T* x = static_cast<const T*>(p.a_raw);
+  const uint32_t nblk = (uint32_t)(p.K / 16);  // units per row
+  const int64_t nsf4 = (p.K / 32 + 3) / 4;
+  const int64_t B = p.M * (p.K / 32);
+  const int64_t u_lo = 2 * ((int64_t)blockIdx.x * B / gridDim.x);
+  const int64_t u_hi = 2 * ((int64_t)(blockIdx.x + 1) * B / gridDim.x);
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)kPU * nthr;
+  for (int64_t c0 = u_lo + (t & ~31); c0 < u_hi; c0 += stride) {  // warp-uniform trip count
+    Raw16<T> raw[kPU];
+#pragma unroll
+    for (int i = 0; i < kPU; ++i) {
+      const int64_t u = c0 + (int64_t)i * nthr + lane;
+      if (u < u_hi) load_raw16<T>(x, u * 16, raw[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < kPU; ++i) {
+      const int64_t u = c0 + (int64_t)i * nthr + lane;
+      const bool live = u < u_hi;
+      float v[16];
+      float amax = 0.f;
+      if (live) {
+        unpack16<T>(raw[i], v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the block's other half
+      if (!live) continue;
+      int e;
+      reinterpret_cast<uint2*>(p.a_codes_w)[u] = mxfp4_encode16(v, amax, false, e);
+      if ((u & 1) == 0) {
+        const uint32_t row = (uint32_t)u / nblk;
+        const uint32_t blk = ((uint32_t)u - row * nblk) >> 1;
+        p.a_sf_w[mma_scale_offset(row, blk, nsf4)] = (uint8_t)(e + 127);
+      }
+    }
+  }
+}
 
 // Dense tiles for CM CTAs stacked along M (CM = 2: a CTA pair sharing one
 // 256-wide N tile): cluster tile t -> (m group, n) in bands of 64 M tiles
@@ -170,7 +270,7 @@ __device__ __forceinline__ TileInfo grouped_tile(const Params& p, const int* sch
 // KS > 1: split-K -- a cluster of KS CTAs owns one output tile, each CTA a
 // slice of the K blocks; the FP32 partial tiles are reduced through
 // distributed shared memory in rank order (deterministic).
-template <bool NV, bool GROUPED, int KS = 1, bool P2 = false, int BNT = BN>
+template <bool NV, bool GROUPED, int KS = 1, bool P2 = false, int BNT = BN, bool QA = false>
 __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -190,6 +290,7 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   static_assert(!P2 || (KS == 1 && !GROUPED), "");
   static_assert(KS == 1 || !GROUPED, "");
+  static_assert(!QA || (!NV && !GROUPED), "the prologue quantizes dense MXFP4 activations");
   constexpr int TM = P2 ? 2 : 1;                           // CTAs along M per tile
   constexpr int CL = TM * KS;                              // CTAs per cluster
   const int crank = P2 ? (int)cluster_ctarank() : 0;      // rank in the pair
@@ -239,6 +340,24 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort_flag = &sm->abort;
 
+  // QA: the prologue runs after the setup, while the producers already
+  // stream B (issuing B first measured faster than quantizing first)
+  if constexpr (QA) {
+    if (warp >= 1 && warp < kWriterWarp0 + 4) {  // warps 1-9: the prologue
+      constexpr int kPro = (kWriterWarp0 + 4 - 1) * 32;
+      const int t = threadIdx.x - 32;
+      if (p.a_dtype == Q4_F32) mxfp4_prologue<float>(p, t, kPro);
+      else if (p.a_dtype == Q4_F16) mxfp4_prologue<__half>(p, t, kPro);
+      else mxfp4_prologue<__nv_bfloat16>(p, t, kPro);
+      // the codes and scales are read next by other CTAs' copies (async
+      // proxy); one release after the CTA barrier publishes all its threads'
+      // stores with the arrival
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      bar_sync_n(2, kPro);
+      if (t == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.gate) : "memory");
+    }
+  }
+
   // arrive on the pair leader's copy of a barrier (this CTA's own when not paired)
   auto arrive_leader = [&](uint64_t* bar) {
     if constexpr (P2) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
@@ -256,12 +375,33 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     uint32_t issued_phase[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
     bool alive = true;
+    // QA: A copies of the first stages wait for the gate (B goes out first)
+    bool gate_open = !QA;
+    int n_def = 0, n_issued = 0;
+    uint32_t def_stage[kStages];
+    int def_kb[kStages], def_row[kStages];
+    auto open_gate = [&]() -> bool {
+      bool ok = true;
+      if (lane == 0) {
+        ok = wait_gate(p.gate, gridDim.x, 2 * gridDim.x, p.ctl, abort_flag);
+        for (int i = 0; ok && i < n_def; ++i)
+          tma_load_2d(smem_u32(smem + def_stage[i] * C_::kStageBytes), &tmap_a, def_kb[i] * (BK / 2),
+                      def_row[i], smem_u32(&sm->full[def_stage[i]]));
+      }
+      gate_open = true;
+      n_def = 0;
+      return __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    };
     for (int t = cid; t < total_tiles && alive; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
       const uint32_t bytes = kABytes + C_::kBLoad;
       const int b_row = (GROUPED ? ti.e * (int)p.N : 0) + ti.n0;
       for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!gate_open && n_issued >= kStages && !open_gate()) {
+          alive = false;
+          break;
+        }
         if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
@@ -271,16 +411,24 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
           // A rows: the tile's rows (grouped: rows of the routed copy of the codes)
-          tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
+          if (gate_open) {
+            tma_load_2d(smem_u32(st), &tmap_a, kb * (BK / 2), ti.m_row0, full);
+          } else {
+            def_stage[n_def] = stage, def_kb[n_def] = kb, def_row[n_def] = ti.m_row0;
+            ++n_def;
+          }
           // B codes: the whole tile, or this CTA's 128-row half of the pair's tile
           tma_load_2d(smem_u32(st + kABytes), &tmap_b, kb * (BK / 2),
                       b_row + (P2 ? crank * (BNT / 2) : 0), full);
         }
+        n_def = __shfl_sync(0xffffffffu, n_def, 0);
+        ++n_issued;
         issued[stage] = 1;
         issued_phase[stage] = phase;
         if (++stage == kStages) stage = 0, phase ^= 1;
       }
     }
+    if (!gate_open && alive) open_gate();  // fewer stages than the ring holds
     // drain: every copy this warp issued has landed before the CTA exits
     if (lane == 0) {
       KernelCtl drain = p.ctl;
@@ -391,6 +539,23 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     bool alive = true;
     const int nsf4_a = (int)((p.K / (NV ? 16 : 32) + 3) / 4);
     const int nblk_b = (int)((p.N + 127) / 128);
+    // QA: A scale copies of the first stages wait for the gate
+    bool gate_open = !QA;
+    int n_def = 0, n_issued = 0;
+    uint32_t def_stage[kStages];
+    const uint8_t* def_src[kStages];
+    auto open_gate = [&]() -> bool {
+      bool ok = true;
+      if (lane == 0) {
+        ok = wait_gate(p.gate, gridDim.x, 2 * gridDim.x, p.ctl, abort_flag);
+        for (int i = 0; ok && i < n_def; ++i)
+          bulk_load(smem_u32(smem + def_stage[i] * C_::kStageBytes + C_::kSfaOff), def_src[i],
+                    C_::kSfaBytes, smem_u32(&sm->full[def_stage[i]]));
+      }
+      gate_open = true;
+      n_def = 0;
+      return __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    };
     for (int t = cid; t < total_tiles && alive; t += ncl) {
       const TileInfo ti = tile_at(t);
       if (!ti.ok) continue;
@@ -401,6 +566,10 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       const bool b_hi = BNT > 128 && nb0 + 1 < nblk_b;  // the tile's second 128 B rows exist
       const uint32_t bytes = (a_sf_ok ? C_::kSfaBytes : 0u) + C_::kSfaBytes * (b_hi ? 2 : 1);
       for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!gate_open && n_issued >= kStages && !open_gate()) {
+          alive = false;
+          break;
+        }
         if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
           alive = false;
           break;
@@ -410,17 +579,27 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
           const int64_t jsf = (int64_t)kb * C_::kSfChunks * 512;
-          if (a_sf_ok) bulk_load(smem_u32(st + C_::kSfaOff), sfa + jsf, C_::kSfaBytes, full);
+          if (a_sf_ok) {
+            if (gate_open) {
+              bulk_load(smem_u32(st + C_::kSfaOff), sfa + jsf, C_::kSfaBytes, full);
+            } else {
+              def_stage[n_def] = stage, def_src[n_def] = sfa + jsf;
+              ++n_def;
+            }
+          }
           const uint8_t* sfb0 = sfb + (int64_t)nb0 * nsf4_a * 512 + jsf;
           const uint32_t sfb_s = smem_u32(st + C_::kSfbOff);
           bulk_load(sfb_s, sfb0, C_::kSfaBytes, full);
           if (b_hi) bulk_load(sfb_s + C_::kSfaBytes, sfb0 + nsf4_a * 512, C_::kSfaBytes, full);
         }
+        n_def = __shfl_sync(0xffffffffu, n_def, 0);
+        ++n_issued;
         issued[stage] = 1;
         issued_phase[stage] = phase;
         if (++stage == kStages) stage = 0, phase ^= 1;
       }
     }
+    if (!gate_open && alive) open_gate();  // fewer stages than the ring holds
     if (lane == 0) {
       KernelCtl drain = p.ctl;
       for (int s = 0; s < kStages; ++s)
@@ -686,13 +865,13 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <bool NV, bool GROUPED, int KS = 1, bool P2 = false, int BNT = BN>
+template <bool NV, bool GROUPED, int KS = 1, bool P2 = false, int BNT = BN, bool QA = false>
 q4_status set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4_ERR_CUDA;
   if (!done[dev]) {
-    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, KS, P2, BNT>,
+    Q4_CUDA_TRY(cudaFuncSetAttribute(fp4_gemm_kernel<NV, GROUPED, KS, P2, BNT, QA>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)Cfg<NV, P2, BNT>::kSmemBytes));
     done[dev] = 1;
@@ -701,11 +880,11 @@ q4_status set_smem_attr() {
 }
 
 // Persistent dense launch: single CTAs, or CTA pairs (P2) on 256x256 tiles.
-template <bool NV, bool P2>
+template <bool NV, bool P2, bool QA = false>
 q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                        cudaStream_t stream) {
   q4_status st;
-  if ((st = set_smem_attr<NV, false, 1, P2>()) != Q4_OK) return st;
+  if ((st = set_smem_attr<NV, false, 1, P2, BN, QA>()) != Q4_OK) return st;
   constexpr int CL = P2 ? 2 : 1;
   const int ctiles = ((p.num_m + CL - 1) / CL) * p.num_n;  // cluster tiles
   cudaLaunchConfig_t cfg = {};
@@ -731,25 +910,25 @@ q4_status launch_dense(const CUtensorMap& ta, const CUtensorMap& tb, const Param
   if (!max_active[dev][P2]) {
     int n = 0;
     cfg.gridDim = dim3((unsigned)(num_sms() / CL * CL), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&n, fp4_gemm_kernel<NV, false, 1, P2>, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, fp4_gemm_kernel<NV, false, 1, P2, BN, QA>, &cfg) != cudaSuccess || n <= 0)
       n = num_sms() / CL;
     max_active[dev][P2] = std::min(n, num_sms() / CL);
   }
   const int clusters = std::max(1, std::min(ctiles, max_active[dev][P2]));
   cfg.gridDim = dim3((unsigned)(clusters * CL), 1, 1);
-  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, 1, P2>, ta, tb, p));
+  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, 1, P2, BN, QA>, ta, tb, p));
   return Q4_OK;
 }
 
 // Split-K for problems with few output tiles: KS CTAs (one cluster) per tile,
 // launched as exactly tiles x KS CTAs (one tile per cluster).
-template <bool NV, int KS, int BNT>
+template <bool NV, int KS, int BNT, bool QA = false>
 q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                         cudaStream_t stream) {
   using C_ = Cfg<NV, false, BNT>;
   static_assert(KS * 0 + (BM * C_::kPartStride * 4) <= C_::kStages * C_::kStageBytes, "partial tile fits");
   q4_status st;
-  if ((st = set_smem_attr<NV, false, KS, false, BNT>()) != Q4_OK) return st;
+  if ((st = set_smem_attr<NV, false, KS, false, BNT, QA>()) != Q4_OK) return st;
   const int tiles = p.num_m * p.num_n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * KS), 1, 1);
@@ -767,17 +946,40 @@ q4_status launch_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const Para
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, KS, false, BNT>, ta, tb, p));
+  Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp4_gemm_kernel<NV, false, KS, false, BNT, QA>, ta, tb, p));
   return Q4_OK;
 }
 
-template <bool NV, int BNT>
+// Whether `clusters` clusters of KS CTAs of this split-K instantiation can all
+// be resident at once (the QA prologue's gate needs every CTA running).
+template <bool NV, int KS, int BNT>
+bool splitk_resident(int clusters) {
+  using C_ = Cfg<NV, false, BNT>;
+  if (set_smem_attr<NV, false, KS, false, BNT, true>() != Q4_OK) return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * KS), 1, 1);
+  cfg.blockDim = dim3(block_threads<false>(), 1, 1);
+  cfg.dynamicSmemBytes = C_::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = KS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  return cudaOccupancyMaxActiveClusters(&n, fp4_gemm_kernel<false, false, KS, false, BNT, true>, &cfg) ==
+             cudaSuccess &&
+         n >= clusters;
+}
+
+template <bool NV, int BNT, bool QA = false>
 q4_status dispatch_splitk(int ks, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                           cudaStream_t stream) {
   switch (ks) {  // 2 <= ks <= 4
-    case 2: return launch_splitk<NV, 2, BNT>(ta, tb, p, stream);
-    case 3: return launch_splitk<NV, 3, BNT>(ta, tb, p, stream);
-    default: return launch_splitk<NV, 4, BNT>(ta, tb, p, stream);
+    case 2: return launch_splitk<NV, 2, BNT, QA>(ta, tb, p, stream);
+    case 3: return launch_splitk<NV, 3, BNT, QA>(ta, tb, p, stream);
+    default: return launch_splitk<NV, 4, BNT, QA>(ta, tb, p, stream);
   }
 }
 
@@ -798,6 +1000,38 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   p.num_m = (int)ceil_div(a.M, BM); p.num_n = (int)ceil_div(a.N, BN); p.bn = BN;
   p.ctl.status = device_status_ptr();
   p.ctl.wait_ns = wait_budget_ns();
+  bool qa = a.a_raw != nullptr;  // MXFP4 activations quantized in the prologue
+  if (qa) {
+    if (a.nvfp4) return Q4_ERR_INVALID_ARG;
+    // split-K runs the prologue only when every cluster is resident at once;
+    // otherwise the activations are quantized by a separate pass first
+    const int nkb = (int)(a.K / BK);
+    const int t128 = p.num_m * (int)ceil_div(a.N, 128), t256 = p.num_m * p.num_n;
+    int ks = 0, tiles = 0;
+    bool n128 = false;
+    if (t128 * 2 <= num_sms() && nkb >= 2) ks = std::min(4, std::min(num_sms() / t128, nkb)), tiles = t128, n128 = true;
+    else if (t256 * 2 <= num_sms() && nkb >= 2) ks = std::min(4, std::min(num_sms() / t256, nkb)), tiles = t256;
+    if (ks >= 2) {
+      bool fits;
+      if (n128) fits = ks == 2 ? splitk_resident<false, 2, 128>(tiles) : ks == 3 ? splitk_resident<false, 3, 128>(tiles)
+                                                                               : splitk_resident<false, 4, 128>(tiles);
+      else fits = ks == 2 ? splitk_resident<false, 2, BN>(tiles) : ks == 3 ? splitk_resident<false, 3, BN>(tiles)
+                                                                         : splitk_resident<false, 4, BN>(tiles);
+      if (!fits) {
+        if ((st = launch_quant_mxfp4(a.a_raw, a.a_dtype, a.M, a.K, const_cast<uint8_t*>(a.a_codes),
+                                     const_cast<uint8_t*>(a.a_scales), Q4_SCALES_MMA, stream)) != Q4_OK)
+          return st;
+        qa = false;
+      }
+    }
+  }
+  if (qa) {
+    p.a_raw = a.a_raw;
+    p.a_dtype = a.a_dtype;
+    p.a_codes_w = const_cast<uint8_t*>(a.a_codes);
+    p.a_sf_w = const_cast<uint8_t*>(a.a_scales);
+    p.gate = a.gate;
+  }
   // few output tiles: split K over a cluster so that the grid fills the GPU,
   // on 128-wide N tiles when there are few enough of them (twice the tiles,
   // half the bytes and half the partial tile per CTA).  At most 4 CTAs per
@@ -813,22 +1047,27 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
     Params p128 = p;
     p128.num_n = (int)ceil_div(a.N, 128);
     p128.bn = 128;
+    if (qa) return dispatch_splitk<false, 128, true>(ks, ta, tb128, p128, stream);
     return a.nvfp4 ? dispatch_splitk<true, 128>(ks, ta, tb128, p128, stream)
                    : dispatch_splitk<false, 128>(ks, ta, tb128, p128, stream);
   }
   if (tiles * 2 <= num_sms() && nkb >= 2) {
     const int ks = std::min(4, std::min(num_sms() / tiles, nkb));
-    if (ks >= 2)
+    if (ks >= 2) {
+      if (qa) return dispatch_splitk<false, BN, true>(ks, ta, tb, p, stream);
       return a.nvfp4 ? dispatch_splitk<true, BN>(ks, ta, tb, p, stream)
                      : dispatch_splitk<false, BN>(ks, ta, tb, p, stream);
+    }
   }
   // CTA pairs (2-SM MMA on 256x256 tiles) whenever M spans two tiles: each SM
   // then receives half of each B tile
   if (p.num_m >= 2) {
     CUtensorMap tb2;  // 128-row boxes: each CTA loads its half of the B tile
     if ((st = make_tmap_2d_u8(&tb2, a.b_codes, a.K / 2, a.N, a.K / 2, BK / 2, BN / 2, true)) != Q4_OK) return st;
+    if (qa) return launch_dense<false, true, true>(ta, tb2, p, stream);
     return a.nvfp4 ? launch_dense<true, true>(ta, tb2, p, stream) : launch_dense<false, true>(ta, tb2, p, stream);
   }
+  if (qa) return launch_dense<false, false, true>(ta, tb, p, stream);
   return a.nvfp4 ? launch_dense<true, false>(ta, tb, p, stream) : launch_dense<false, false>(ta, tb, p, stream);
 }
 

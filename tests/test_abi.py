@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["quantize_nvfp4", "quantize_mxfp4", "quantize_int4_g128", "gemm_w4a4_nvfp4",
-                 "gemm_w4a4_mxfp4", "gemm_w4a16_int4", "gemm_w4a16_nvfp4", "gemm_w4a16_mxfp4",
+                 "gemm_w4a4_mxfp4", "gemm_w4a4_mxfp4_fused", "gemm_w4a16_int4", "gemm_w4a16_nvfp4", "gemm_w4a16_mxfp4",
                  "grouped_gemm_moe", "q4_sync_status", "quantize_fp8_blockwise", "gemm_fp8_blockwise", "gemm_w4a8", "w4a8_weight_scales",
                  "q4_workspace_size", "q4_scales_to_mma"]:
         assert want in names
@@ -79,6 +79,10 @@ def test_host_argument_checks(clib):
     assert clib.w4a8_weight_scales(fake + 1, 4, 128, fake, None) == -1
     assert clib.gemm_w4a16_nvfp4(fake, fake, fake + 1, fake, 4, 4, 128, fake, None, 0, None) == -1
     assert clib.gemm_w4a16_mxfp4(None, fake, fake, 4, 4, 128, fake, None, 0, None) == -1
+    # fused MXFP4 GEMM: K % 256, a bad activation or output dtype (all checked before B)
+    assert clib.gemm_w4a4_mxfp4_fused(fake, 1, None, 4, 4, 128, fake, 1, fake, 1 << 20, None) == -2
+    assert clib.gemm_w4a4_mxfp4_fused(fake, 5, None, 4, 4, 256, fake, 1, fake, 1 << 20, None) == -1
+    assert clib.gemm_w4a4_mxfp4_fused(fake, 1, None, 4, 4, 256, fake, 2, fake, 1 << 20, None) == -1
     # an unknown rounding mode
     assert clib.quantize_mxfp4_ex(fake, 1, 4, 64, fake, fake, 0, 2, None) == -1
     assert clib.quantize_nvfp4_ex(fake, 1, 4, 64, fake, fake, 0, -1, fake, fake, 256, None) == -1
@@ -94,6 +98,8 @@ def test_workspace_sizes(clib):
     n = clib.q4_workspace_size(1, 8192, 28672, 8192)
     assert n >= 8192 * 4096 + 28672 * 4096  # room for both operands' codes
     assert clib.q4_mma_scales_bytes(130, 5) == 256 * 8
+    # the fused MXFP4 GEMM: the gate's 256 bytes, then what the two-launch call uses
+    assert clib.q4_workspace_size(9, 256, 2048, 7168) == 256 + clib.q4_workspace_size(2, 256, 2048, 7168)
     assert clib.q4_workspace_size_moe(4096, 2048, 7168, 64, 32768) > 4096 * 3584
 
 

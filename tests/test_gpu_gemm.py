@@ -9,7 +9,7 @@ import torch
 import int4_gemm_gb300 as q4
 import oracle
 import workloads
-from tests._util import assert_gemm_close
+from tests._util import assert_gemm_close, to_mma_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +84,83 @@ def test_w4a4_mxfp4_raw_operands(lib, shape):
     C = lib.gemm_w4a4_mxfp4(ad, torch.from_numpy(b).cuda(), K, out_dtype=torch.bfloat16)
     R = oracle.gemm_w4a4_mxfp4(*oracle.quantize_mxfp4(ad.float().cpu().numpy()), *oracle.quantize_mxfp4(b))
     assert_gemm_close(C.float().cpu().numpy(), R)
+
+
+# MXFP4 with raw activations: the GEMM quantizes them itself, in a prologue,
+# into the workspace.  Shapes for each launch form: split-K on 128-wide N
+# tiles (the MoE shape; a small one), one CTA per 128 x 256 tile (one K
+# block, so no split), and CTA pairs.
+PROLOGUE_SHAPES = [(256, 2048, 7168), (100, 512, 1024), (64, 20480, 256), (1000, 6144, 512)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("shape", PROLOGUE_SHAPES)
+def test_w4a4_mxfp4_prologue_quantization(lib, dtype, shape):
+    """The codes and tensor-core-layout scales the fused call's prologue leaves
+    in the workspace are the oracle's bit for bit, the product matches the
+    oracle's and the two-launch call's bit for bit, and the gate's counters
+    are zero again afterwards."""
+    M, N, K = shape
+    a, b = workloads.mxfp4_pair(M, N, K, seed=sum(shape) + 3)
+    ad = torch.from_numpy(a).to(dtype).cuda()
+    cb, sb = lib.quantize_mxfp4(torch.from_numpy(b).cuda(), scale_layout="mma")
+    Bq = q4.Fp4Operand(cb, sb, "mma")
+    ws = lib.workspace(q4.OP_GEMM_W4A4_MXFP4_FUSED, M, N, K, ad.device)
+    C = lib.gemm_w4a4_mxfp4_fused(ad, Bq, K, out_dtype=torch.float32, ws=ws)
+    assert lib.sync_status() == 0
+    oa = oracle.quantize_mxfp4(ad.float().cpu().numpy())
+    wsh = ws.cpu().numpy()
+    assert not wsh[:256].any()
+    codes0 = 256  # after the gate's 256 bytes
+    assert np.array_equal(wsh[codes0:codes0 + M * K // 2].reshape(M, K // 2), oa[0])
+    sf0 = codes0 + -(-(M * K // 2) // 256) * 256  # the scales follow the codes, 256-byte aligned
+    want = to_mma_layout(oa[1])
+    valid = to_mma_layout(np.ones_like(oa[1])) == 1  # rows past M are padding
+    assert np.array_equal(wsh[sf0:sf0 + want.size][valid], want[valid])
+    R = oracle.gemm_w4a4_mxfp4(*oa, *oracle.quantize_mxfp4(b))
+    assert_gemm_close(C.cpu().numpy(), R)
+    C2 = lib.gemm_w4a4_mxfp4(ad, Bq, K, out_dtype=torch.float32)
+    assert torch.equal(C, C2)
+
+
+def test_w4a4_mxfp4_fused_gate_reuse(lib):
+    """One workspace serves a run of fused calls with different grids (split-K
+    clusters, one CTA per tile, pairs) back to back, unsynchronized: each
+    call's gate starts from the zero the previous one left, and every product
+    equals the two-launch call's."""
+    shapes = [(256, 2048, 7168), (1000, 6144, 512), (100, 512, 1024), (64, 20480, 256),
+              (256, 2048, 7168)]
+    cap = max(q4.lib().q4_workspace_size(q4.OP_GEMM_W4A4_MXFP4_FUSED, *s) for s in shapes)
+    ws = torch.zeros(cap, dtype=torch.uint8, device="cuda")
+    runs = []
+    for i, (M, N, K) in enumerate(shapes * 2):
+        a, b = workloads.mxfp4_pair(M, N, K, seed=100 + i)
+        ad, bd = torch.from_numpy(a).to(torch.bfloat16).cuda(), torch.from_numpy(b).cuda()
+        cb, sb = lib.quantize_mxfp4(bd, scale_layout="mma")
+        Bq = q4.Fp4Operand(cb, sb, "mma")
+        runs.append((ad, Bq, K, lib.gemm_w4a4_mxfp4_fused(ad, Bq, K, ws=ws)))
+    torch.cuda.synchronize()
+    assert lib.sync_status() == 0
+    assert not ws[:256].any()
+    for ad, Bq, K, C in runs:
+        assert torch.equal(C, lib.gemm_w4a4_mxfp4(ad, Bq, K))
+
+
+def test_w4a4_mxfp4_fused_checks(lib):
+    """The fused call checks its arguments on the host: K against A, the
+    workspace's size, and an empty problem launches nothing."""
+    M, N, K = 64, 256, 512
+    a, b = workloads.mxfp4_pair(M, N, K, seed=7)
+    ad = torch.from_numpy(a).to(torch.bfloat16).cuda()
+    cb, sb = lib.quantize_mxfp4(torch.from_numpy(b).cuda(), scale_layout="mma")
+    Bq = q4.Fp4Operand(cb, sb, "mma")
+    with pytest.raises(ValueError):
+        lib.gemm_w4a4_mxfp4_fused(ad, Bq, 2 * K)
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(RuntimeError):
+        lib.gemm_w4a4_mxfp4_fused(ad, Bq, K, ws=small)
+    C = lib.gemm_w4a4_mxfp4_fused(ad[:0], Bq, K)
+    assert C.shape == (0, N)
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
