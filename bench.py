@@ -54,11 +54,6 @@ NCU_TRAFFIC = {
     # kernel of the current code, at the bench's own sizes:
     # w4a16_kernel, mean over the M = 1, 4, 16 launches at N = K = 8192
     "decode": 34.76e6,
-    # fp4_gemm_kernel (CTA pairs) at 8192 x 28672 x 8192, mean of 3 launches
-    # (235 MB read: A and B once each, scales; 435 MB of C written)
-    "prefill": 670.0e6,
-    # split-K fp4_gemm_kernel (128-wide tiles) at 256 x 2048 x 7168 (C stays in L2)
-    "moe": 8.82e6,
     # w4a16_kernel<NVFP4>, mean over the M = 1, 4, 16 launches at N = K = 8192
     "decode_nvfp4": 37.94e6,
 }
@@ -345,7 +340,8 @@ class QuantizeNvfp4:
     def config(self):
         return {"workload": f"nvfp4_quantize A bf16 {self.M}x{self.K} (the prefill activations) -> codes + "
                             f"MMA-layout E4M3 scales + tensor scale, E2M1 ties: {self.rounding}",
-                "M": self.M, "K": self.K, "l2": "input larger than L2 (134 MB)"}
+                "M": self.M, "K": self.K, "l2": "input larger than L2 (134 MB)",
+                "bytes": "one read of x + codes + scales (the amax pass's read of x is overhead)"}
 
     def setup(self, q4, dev, seed, shape=None):
         self.q4 = q4
@@ -377,9 +373,11 @@ class QuantizeNvfp4:
     kernel_only = step
 
     def units_per_step(self):
-        # x read twice (the tensor scale needs the whole tensor's amax before any
-        # element is encoded, and x is larger than L2), codes and scales written
-        return 2 * self.M * self.K * 2 + self.M * self.K // 2 + self.M * self.K // 16
+        # the method's bytes: one read of x, codes and scales written.  The
+        # implementation reads x twice (the tensor scale needs the whole
+        # tensor's amax before any element is encoded); the second read is
+        # overhead, not work, and is not counted
+        return self.M * self.K * 2 + self.M * self.K // 2 + self.M * self.K // 16
 
     kernel_units = units_per_step
 
@@ -401,7 +399,7 @@ class QuantizeNvfp4:
         oracle.quantize_nvfp4(self.o_x, rounding=self.rounding)
 
     def oracle_units(self):
-        return 2 * self.o_rows * self.K * 2 + self.o_rows * self.K // 2 + self.o_rows * self.K // 16
+        return self.o_rows * self.K * 2 + self.o_rows * self.K // 2 + self.o_rows * self.K // 16
 
     def oracle_sample_text(self):
         return (f"the first {self.o_rows} rows as their own tensor (amax, E4M3 block scales, "
@@ -594,7 +592,8 @@ class Fp8Blockwise:
     name = "fp8_blockwise"
     unit = "TFLOP/s"
     bound = "tensor"
-    tensor_over_bf16 = 2.0  # nominal dense FP8 : BF16 on GB300 (4.5 vs 2.25 PFLOP/s)
+    tensor_fmt = "fp8"  # the roofline peak: a library FP8 GEMM measured live
+    tensor_over_bf16 = 2.0  # else nominal dense FP8 : BF16 on GB300 (4.5 vs 2.25 PFLOP/s)
     default_steps = 200
     kernel = "fp8_gemm_kernel"
     launches_per_step = 2  # activation quantizer + GEMM
@@ -879,7 +878,61 @@ def run_reference(args, dist):
 
 def peak_text(wl):
     r = getattr(wl, "tensor_over_bf16", FP4_OVER_BF16)
-    return f"bf16_tflops x {r:g} (nominal {'FP8' if r == 2.0 else 'FP4'}:BF16)"
+    return f"bf16_tflops_sustained x {r:g} (nominal {'FP8' if r == 2.0 else 'FP4'}:BF16)"
+
+
+def library_peak(fmt: str, dev, n: int = 8192, reps: int = 10, seconds: float = 1.5):
+    """Dense tensor-core peaks of this GPU for ``fmt`` ("nvfp4" or "fp8"),
+    measured the way the bf16 peaks are: a library GEMM (torch._scaled_mm on
+    cuBLASLt) of n x n x n, as a burst (best of ``reps`` single launches on a
+    rested GPU, CUDA events) and sustained (back to back for ``seconds``, the
+    rate over the last two thirds, under the power cap).  Returns
+    (burst TFLOP/s, sustained TFLOP/s, description), or (None, None, why) when
+    the library path is missing."""
+    try:
+        g = torch.Generator(device=dev).manual_seed(0)
+        if fmt == "nvfp4":
+            a = torch.randint(0, 256, (n, n // 2), device=dev, dtype=torch.uint8, generator=g)
+            b = torch.randint(0, 256, (n, n // 2), device=dev, dtype=torch.uint8, generator=g)
+            a, b = a.view(torch.float4_e2m1fn_x2), b.view(torch.float4_e2m1fn_x2)
+            sa = torch.ones(n * (n // 16), device=dev).to(torch.float8_e4m3fn)  # tensor-core layout
+            sb = torch.ones(n * (n // 16), device=dev).to(torch.float8_e4m3fn)
+            what = "NVFP4 (E2M1, E4M3 block scales of 16)"
+        else:
+            a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+            b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+            sa = sb = torch.ones((), device=dev)
+            what = "FP8 E4M3 (per-tensor scales)"
+        run = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+        flop = 2.0 * n ** 3
+        run()
+        torch.cuda.synchronize()
+        time.sleep(1.0)  # rest before the burst
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(reps):
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        burst = flop / best / 1e12
+        per = max(1, int(seconds / 3 / best))  # launches per third
+        for _ in range(per):
+            run()
+        e0.record()
+        for _ in range(2 * per):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        sustained = flop * 2 * per / (e0.elapsed_time(e1) / 1e3) / 1e12
+        del a, b
+        torch.cuda.empty_cache()
+        return burst, sustained, (f"measured live: torch._scaled_mm {what} {n}^3 (cuBLASLt), "
+                                  f"burst = best of {reps} launches, sustained = back to back "
+                                  f"for {seconds:g} s")
+    except Exception as e:  # no FP4/FP8 library path in this torch build
+        return None, None, f"library {fmt} GEMM unavailable ({type(e).__name__})"
 
 
 def wl_setup_host(wl, seed):
@@ -944,6 +997,10 @@ def main():
     wl.setup(q4, dev, args.seed, shape)
     K = args.steps or wl.default_steps
     W = max(3, args.warmup)
+    # a tensor-bound kernel's roofline peak: the library GEMM of its type,
+    # measured here before the timed steps
+    lib_peaks = (library_peak(getattr(wl, "tensor_fmt", "nvfp4"), dev) if wl.bound == "tensor"
+                 else (None, None, ""))
     for i in range(W):
         wl.step(i)
     torch.cuda.synchronize()
@@ -982,18 +1039,24 @@ def main():
 
     # the dominant kernel alone, in the same graph form
     pk, src = peaks()
+    lib_src = ""
     if wl.bound == "hbm":
         peak, punit = pk["hbm_gbs"], "GB/s"
     else:
-        ratio = getattr(wl, "tensor_over_bf16", FP4_OVER_BF16)
-        peak, punit = pk["bf16_tflops"] * ratio, "TFLOP/s"
+        punit = "TFLOP/s"
+        # the kernel below runs hundreds of launches back to back: the
+        # library's sustained rate is its peak (the burst rate is reported too)
+        peak, lib_src = lib_peaks[1], lib_peaks[2]
+        if peak is None:  # nominal ratio to the measured bf16 peak, said so below
+            peak = pk["bf16_tflops_sustained"] * getattr(wl, "tensor_over_bf16", FP4_OVER_BF16)
     kg = torch.cuda.CUDAGraph()
     with torch.cuda.graph(kg):
         for i in range(G):
             wl.kernel_only(i)
     kg.replay()
     torch.cuda.synchronize()
-    reps = max(1, K // G // 2)
+    # at least 200 launches of the kernel, whatever the step count
+    reps = max(K // G // 2, -(-200 // (G * wl.kernel_launches)))
     e0.record()
     for _ in range(reps):
         kg.replay()
@@ -1006,7 +1069,10 @@ def main():
     roofline = {"bound": wl.bound, "achieved": achieved, "peak": peak, "unit": punit,
                 "frac": achieved / peak, "traffic": NCU_TRAFFIC.get(args.workload),
                 "kernel": wl.kernel, "avg_launch_us": avg_s * 1e6,
-                "peak_source": f"{src} ({'hbm_gbs' if punit == 'GB/s' else peak_text(wl)})"}
+                "peak_burst": lib_peaks[0],
+                "peak_source": (f"{src} (hbm_gbs)" if punit == "GB/s" else
+                                lib_src if lib_src.startswith("measured") else
+                                f"{src} ({peak_text(wl)}); {lib_src}")}
 
     # end to end through the public API: host buffers, copies inside the timed region
     n_e2e = min(K, 2000 if wl.unit == "GB/s" else 50)

@@ -118,7 +118,11 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
 // hardware convert keeps the sign of a negative zero.
 // Persistent: each CTA walks tiles of 256 units (one per thread), a 4-slot
 // ring of bulk copies (one thread issues them) keeping three tiles in flight
-// while the threads work on the fourth.
+// while the threads work on the fourth.  The grid walks the tiles from the
+// last to the first: the amax pass before it reads x from the first element to
+// the last, so the part of x it read last (up to the size of L2) is still in
+// L2 when this pass starts, and the codes are stored with the streaming hint
+// so that they do not push it out.
 constexpr int kQStages = 4;
 constexpr int kQUnits = kThreads;
 
@@ -137,10 +141,13 @@ __global__ void __launch_bounds__(kThreads, 4)
   __shared__ int s_abort;
   const uint32_t ntiles = (um.units + kQUnits - 1) / kQUnits;
   const uint32_t tid = threadIdx.x;
-  auto tile_of = [&](uint32_t i) { return blockIdx.x + i * gridDim.x; };
+  // the CTA's i-th tile: index blockIdx.x + i G of the walk, which runs from
+  // the last tile down to the first
+  auto idx_of = [&](uint32_t i) { return blockIdx.x + i * gridDim.x; };
+  auto tile_of = [&](uint32_t i) { return ntiles - 1 - idx_of(i); };
   auto issue = [&](uint32_t i) {  // the CTA's i-th tile into slot i % kQStages
+    if (idx_of(i) >= ntiles) return;
     const uint32_t tile = tile_of(i);
-    if (tile >= ntiles) return;
     const uint32_t n = min((uint32_t)kQUnits, um.units - tile * kQUnits);
     const uint32_t bar = smem_u32(&full[i % kQStages]);
     mbar_arrive_expect_tx(bar, n * 16 * (uint32_t)sizeof(T));
@@ -160,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   const float g = s_g, c6g = s_c6g;
 
   uint32_t i = 0;
-  for (; tile_of(i) < ntiles; ++i) {
+  for (; idx_of(i) < ntiles; ++i) {
     if (tid == 0 && !mbar_wait(smem_u32(&full[i % kQStages]), (i / kQStages) & 1, ctl, &s_abort))
       s_abort = 1;
     __syncthreads();  // the tile has landed; every thread is done with slot (i - 1) % kQStages
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         packed.y |= cvt_e2m1x2(y[8 + 2 * j], y[8 + 2 * j + 1]) << (8 * j);
       }
     }
-    reinterpret_cast<uint2*>(codes)[u] = packed;
+    __stcs(reinterpret_cast<uint2*>(codes) + u, packed);
 
     const uint32_t rl = um.row_of(u);
     const int64_t row = um.row0 + rl, blk = u - rl * um.nblk;
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   if (tid == 0 && s_abort) {
     KernelCtl drain = ctl;
     for (uint32_t k = i; k < i + kQStages - 1; ++k)
-      if (tile_of(k) < ntiles) mbar_wait(smem_u32(&full[k % kQStages]), (k / kQStages) & 1, drain, nullptr);
+      if (idx_of(k) < ntiles) mbar_wait(smem_u32(&full[k % kQStages]), (k / kQStages) & 1, drain, nullptr);
   }
 }
 
