@@ -884,9 +884,9 @@ def peak_text(wl):
 def library_peak(fmt: str, dev, n: int = 8192, reps: int = 10, seconds: float = 1.5):
     """Dense tensor-core peaks of this GPU for ``fmt`` ("nvfp4" or "fp8"),
     measured the way the bf16 peaks are: a library GEMM (torch._scaled_mm on
-    cuBLASLt) of n x n x n, as a burst (best of ``reps`` single launches on a
-    rested GPU, CUDA events) and sustained (back to back for ``seconds``, the
-    rate over the last two thirds, under the power cap).  Returns
+    cuBLASLt) of n x n x n, as a burst (the best of ``reps`` groups of 5
+    back-to-back launches, CUDA events) and sustained (back to back for
+    ``seconds``, the rate over the last two thirds, under the power cap).  Returns
     (burst TFLOP/s, sustained TFLOP/s, description), or (None, None, why) when
     the library path is missing."""
     try:
@@ -905,17 +905,18 @@ def library_peak(fmt: str, dev, n: int = 8192, reps: int = 10, seconds: float = 
             what = "FP8 E4M3 (per-tensor scales)"
         run = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
         flop = 2.0 * n ** 3
-        run()
+        for _ in range(5):
+            run()
         torch.cuda.synchronize()
-        time.sleep(1.0)  # rest before the burst
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         best = float("inf")
-        for _ in range(reps):
+        for _ in range(reps):  # short back-to-back groups: clocks up, power cap not yet reached
             e0.record()
-            run()
+            for _ in range(5):
+                run()
             e1.record()
             torch.cuda.synchronize()
-            best = min(best, e0.elapsed_time(e1) / 1e3)
+            best = min(best, e0.elapsed_time(e1) / 1e3 / 5)
         burst = flop / best / 1e12
         per = max(1, int(seconds / 3 / best))  # launches per third
         for _ in range(per):
@@ -929,7 +930,7 @@ def library_peak(fmt: str, dev, n: int = 8192, reps: int = 10, seconds: float = 
         del a, b
         torch.cuda.empty_cache()
         return burst, sustained, (f"measured live: torch._scaled_mm {what} {n}^3 (cuBLASLt), "
-                                  f"burst = best of {reps} launches, sustained = back to back "
+                                  f"burst = best of {reps} groups of 5 launches, sustained = back to back "
                                   f"for {seconds:g} s")
     except Exception as e:  # no FP4/FP8 library path in this torch build
         return None, None, f"library {fmt} GEMM unavailable ({type(e).__name__})"
