@@ -148,6 +148,7 @@ constexpr uint32_t kGTileBytes = GBM * GBK;       // one operand tile of one K b
 constexpr uint32_t kGStageBytes = 2 * kGTileBytes;
 constexpr int kPromoWarp0 = 2, kPromoWarps = 8;
 constexpr int kBandM = 32;                       // M tiles per band of the tile order
+constexpr int kSP = 4;                           // K blocks of scale prefetch in registers
 constexpr int kGThreads = (kPromoWarp0 + kPromoWarps) * 32;
 constexpr uint32_t kGSmemBytes = kGStages * kGStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(kGSmemBytes <= 232448, "shared memory");
@@ -323,27 +324,40 @@ __global__ void __launch_bounds__(kGThreads, 1)
       float acc[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0.f;
-      float sa_n = __ldg(sa_row), sb_n = __ldg(sb_row);
-      for (int kb = 0; kb < KB; ++kb, ++gk) {
-        const uint32_t slot = gk % kSlots, sphase = (gk / kSlots) & 1;
-        const float sc = sa_n * sb_n;
-        if (kb + 1 < KB) sa_n = __ldg(sa_row + kb + 1), sb_n = __ldg(sb_row + kb + 1);
-        if (!mbar_wait(smem_u32(&sm->slot_full[slot]), sphase, p.ctl, abort_flag)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(t_lane + slot * GBN, r0);
-        tmem_ld_32x32b_x32(t_lane + slot * GBN + 32, r1);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->slot_empty[slot]));
+      // the scales of K block kb + kSP are requested while block kb is
+      // promoted: a K block takes a few hundred ns, an L2 load about a us
+      float sa_q[kSP], sb_q[kSP];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = fmaf(__uint_as_float(r0[j]), sc, acc[j]);
-          acc[32 + j] = fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
+      for (int i = 0; i < kSP; ++i) {
+        sa_q[i] = i < KB ? __ldg(sa_row + i) : 0.f;
+        sb_q[i] = i < KB ? __ldg(sb_row + i) : 0.f;
+      }
+      for (int kb0 = 0; kb0 < KB && alive; kb0 += kSP) {
+#pragma unroll
+        for (int i = 0; i < kSP; ++i) {
+          const int kb = kb0 + i;
+          if (kb >= KB || !alive) continue;
+          const uint32_t slot = gk % kSlots, sphase = (gk / kSlots) & 1;
+          const float sc = sa_q[i] * sb_q[i];
+          if (kb + kSP < KB) sa_q[i] = __ldg(sa_row + kb + kSP), sb_q[i] = __ldg(sb_row + kb + kSP);
+          if (!mbar_wait(smem_u32(&sm->slot_full[slot]), sphase, p.ctl, abort_flag)) {
+            alive = false;
+            continue;
+          }
+          tc_fence_after();
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(t_lane + slot * GBN, r0);
+          tmem_ld_32x32b_x32(t_lane + slot * GBN + 32, r1);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->slot_empty[slot]));
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            acc[j] = fmaf(__uint_as_float(r0[j]), sc, acc[j]);
+            acc[32 + j] = fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
+          }
+          ++gk;
         }
       }
       if (!alive || !row_ok) continue;

@@ -16,9 +16,10 @@
 //               5-stage ring, and the K block's 128 weight scales (FP32, from
 //               the [K/128, N] copy made by w4a8_weight_scales) into a 16-deep
 //               ring of scale buffers;
-//   warps 2, 3  converters: each thread expands the nibbles of two B rows to
-//               E4M3 bytes (a 16-entry byte-permute table) and writes them in
-//               the 128-byte-swizzled layout the MMA reads;
+//   warps 2, 3  converters: each thread expands eight 16-byte chunks of INT4
+//               codes to E4M3 bytes (a 16-entry byte-permute table), a warp
+//               reading eight whole rows at a time, and writes them in the
+//               128-byte-swizzled layout the MMA reads;
 //   warp 1      MMA issuer: four tcgen05.mma kind::f8f6f4 per K block into one
 //               of four 128-column TMEM slots;
 //   warps 4..11 promotion: slot * s16[n, kb] * sa[m, kb] into 64 FP32 registers
@@ -40,6 +41,7 @@ constexpr int kWStages = 5;
 constexpr int kWSlots = 4;                            // TMEM accumulator slots, 128 columns each
 constexpr int kScaleBufs = 16;                        // weight-scale buffers, one K block each
 constexpr int kBandM = 32;                            // M tiles per band of the tile order
+constexpr int kSP = 4;                                // K blocks of scale prefetch in registers
 constexpr uint32_t kATileBytes = WBM * WBK;           // E4M3 A tile
 constexpr uint32_t kBTileBytes = WBN * WBK;           // E4M3 B tile after conversion
 constexpr uint32_t kBCodeBytes = WBN * WBK / 2;       // INT4 B tile as loaded
@@ -53,7 +55,8 @@ constexpr uint32_t kWSmemBytes =
 static_assert(kWStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 static_assert(kWSmemBytes <= 232448, "shared memory");
 static_assert(kWSlots * WBN <= 512, "TMEM columns");
-static_assert(kConvWarps * 2 * 32 == WBN, "two B rows per converter thread");
+constexpr int kConvItems = WBN * 4 / (kConvWarps * 32);  // 16-byte code chunks per converter thread
+static_assert(kConvItems * kConvWarps * 32 == WBN * 4, "the converters cover the B tile");
 
 struct WSmem {
   uint64_t full[kWStages];      // A tile and INT4 tile landed
@@ -242,9 +245,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __syncwarp();
   } else if (warp < kPromWarp0) {
     // ------------------------------------------------------------ converters
-    // thread (warp c, lane l) converts B rows 64 c + l and 64 c + 32 + l; the
-    // 16-byte chunk j of row r goes to r * 128 + ((j ^ (r % 8)) * 16), the
-    // 128-byte swizzle the MMA's shared-memory descriptors describe
+    // item it = (row r = it / 4, 16-byte code chunk i = it % 4) of the K block;
+    // the converter threads take items it = 64 k + 32 c + lane, so that a
+    // warp's 32 loads cover 8 whole rows (512 contiguous bytes: no bank
+    // conflict).  Code chunk i becomes output chunks 2i and 2i + 1 of row r,
+    // stored at r * 128 + ((j ^ (r % 8)) * 16): the 128-byte swizzle the
+    // MMA's shared-memory descriptors describe
     const int cw = warp - kConvWarp0;
     uint32_t stage = 0, phase = 0;
     bool alive = true;
@@ -258,18 +264,16 @@ __global__ void __launch_bounds__(kWThreads, 1)
         const uint8_t* src = st + kATileBytes + kBTileBytes;
         uint8_t* dst = st + kATileBytes;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int r = cw * 64 + rr * 32 + lane;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {  // 16 code bytes = output chunks 2i and 2i + 1
-            const uint4 w = *reinterpret_cast<const uint4*>(src + r * 64 + i * 16);
-            const uint2 e0 = int4x8_to_e4m3(w.x), e1 = int4x8_to_e4m3(w.y);
-            const uint2 e2 = int4x8_to_e4m3(w.z), e3 = int4x8_to_e4m3(w.w);
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i) ^ (r & 7)) << 4)) =
-                make_uint4(e0.x, e0.y, e1.x, e1.y);
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i + 1) ^ (r & 7)) << 4)) =
-                make_uint4(e2.x, e2.y, e3.x, e3.y);
-          }
+        for (int k = 0; k < kConvItems; ++k) {
+          const int it = k * kConvWarps * 32 + cw * 32 + lane;
+          const int r = it >> 2, i = it & 3;
+          const uint4 w = *reinterpret_cast<const uint4*>(src + r * 64 + i * 16);
+          const uint2 e0 = int4x8_to_e4m3(w.x), e1 = int4x8_to_e4m3(w.y);
+          const uint2 e2 = int4x8_to_e4m3(w.z), e3 = int4x8_to_e4m3(w.w);
+          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i) ^ (r & 7)) << 4)) =
+              make_uint4(e0.x, e0.y, e1.x, e1.y);
+          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i + 1) ^ (r & 7)) << 4)) =
+              make_uint4(e2.x, e2.y, e3.x, e3.y);
         }
         fence_proxy_async_smem();  // the tensor cores read what these threads wrote
         __syncwarp();
@@ -293,40 +297,50 @@ __global__ void __launch_bounds__(kWThreads, 1)
       float acc[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0.f;
-      float sa_n = __ldg(sa_row);
-      for (int kb = 0; kb < KB; ++kb, ++gk) {
-        const uint32_t slot = gk % kWSlots, sphase = (gk / kWSlots) & 1;
-        const uint32_t b = gk % kScaleBufs;
-        const float sa_k = sa_n;
-        if (kb + 1 < KB) sa_n = __ldg(sa_row + kb + 1);
-        if (!mbar_wait(smem_u32(&sm->slot_full[slot]), sphase, p.ctl, abort_flag) ||
-            !mbar_wait(smem_u32(&sm->sc_full[b]), (gk / kScaleBufs) & 1, p.ctl, abort_flag)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(t_lane + slot * WBN, r0);
-        tmem_ld_32x32b_x32(t_lane + slot * WBN + 32, r1);
-        tmem_ld_wait();
-        const float4* sw = reinterpret_cast<const float4*>(sbuf + b * WBN + h * 64);
+      // the scale of K block kb + kSP is requested while block kb is
+      // promoted: a K block takes a few hundred ns, an L2 load about a us
+      float sa_q[kSP];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 s0 = sw[v], s1 = sw[8 + v];
-          acc[4 * v] = fmaf(__uint_as_float(r0[4 * v]) * s0.x, sa_k, acc[4 * v]);
-          acc[4 * v + 1] = fmaf(__uint_as_float(r0[4 * v + 1]) * s0.y, sa_k, acc[4 * v + 1]);
-          acc[4 * v + 2] = fmaf(__uint_as_float(r0[4 * v + 2]) * s0.z, sa_k, acc[4 * v + 2]);
-          acc[4 * v + 3] = fmaf(__uint_as_float(r0[4 * v + 3]) * s0.w, sa_k, acc[4 * v + 3]);
-          acc[32 + 4 * v] = fmaf(__uint_as_float(r1[4 * v]) * s1.x, sa_k, acc[32 + 4 * v]);
-          acc[32 + 4 * v + 1] = fmaf(__uint_as_float(r1[4 * v + 1]) * s1.y, sa_k, acc[32 + 4 * v + 1]);
-          acc[32 + 4 * v + 2] = fmaf(__uint_as_float(r1[4 * v + 2]) * s1.z, sa_k, acc[32 + 4 * v + 2]);
-          acc[32 + 4 * v + 3] = fmaf(__uint_as_float(r1[4 * v + 3]) * s1.w, sa_k, acc[32 + 4 * v + 3]);
+      for (int i = 0; i < kSP; ++i) sa_q[i] = i < KB ? __ldg(sa_row + i) : 0.f;
+      for (int kb0 = 0; kb0 < KB && alive; kb0 += kSP) {
+#pragma unroll
+        for (int i = 0; i < kSP; ++i) {
+          const int kb = kb0 + i;
+          if (kb >= KB || !alive) continue;
+          const uint32_t slot = gk % kWSlots, sphase = (gk / kWSlots) & 1;
+          const uint32_t b = gk % kScaleBufs;
+          const float sa_k = sa_q[i];
+          if (kb + kSP < KB) sa_q[i] = __ldg(sa_row + kb + kSP);
+          if (!mbar_wait(smem_u32(&sm->slot_full[slot]), sphase, p.ctl, abort_flag) ||
+              !mbar_wait(smem_u32(&sm->sc_full[b]), (gk / kScaleBufs) & 1, p.ctl, abort_flag)) {
+            alive = false;
+            continue;
+          }
+          tc_fence_after();
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(t_lane + slot * WBN, r0);
+          tmem_ld_32x32b_x32(t_lane + slot * WBN + 32, r1);
+          tmem_ld_wait();
+          const float4* sw = reinterpret_cast<const float4*>(sbuf + b * WBN + h * 64);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const float4 s0 = sw[v], s1 = sw[8 + v];
+            acc[4 * v] = fmaf(__uint_as_float(r0[4 * v]) * s0.x, sa_k, acc[4 * v]);
+            acc[4 * v + 1] = fmaf(__uint_as_float(r0[4 * v + 1]) * s0.y, sa_k, acc[4 * v + 1]);
+            acc[4 * v + 2] = fmaf(__uint_as_float(r0[4 * v + 2]) * s0.z, sa_k, acc[4 * v + 2]);
+            acc[4 * v + 3] = fmaf(__uint_as_float(r0[4 * v + 3]) * s0.w, sa_k, acc[4 * v + 3]);
+            acc[32 + 4 * v] = fmaf(__uint_as_float(r1[4 * v]) * s1.x, sa_k, acc[32 + 4 * v]);
+            acc[32 + 4 * v + 1] = fmaf(__uint_as_float(r1[4 * v + 1]) * s1.y, sa_k, acc[32 + 4 * v + 1]);
+            acc[32 + 4 * v + 2] = fmaf(__uint_as_float(r1[4 * v + 2]) * s1.z, sa_k, acc[32 + 4 * v + 2]);
+            acc[32 + 4 * v + 3] = fmaf(__uint_as_float(r1[4 * v + 3]) * s1.w, sa_k, acc[32 + 4 * v + 3]);
+          }
+          // the slot goes back after the scale buffer has been read (its refill
+          // waits, through the MMA, for this arrival)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->slot_empty[slot]));
+          ++gk;
         }
-        // the slot goes back after the scale buffer has been read (its refill
-        // waits, through the MMA, for this arrival)
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm->slot_empty[slot]));
       }
       if (!alive || !row_ok) continue;
       const int64_t col0 = n0 + h * 64;
