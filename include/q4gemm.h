@@ -280,17 +280,22 @@ q4_status gemm_w4a16_mxfp4(const void* A_bf16, const uint8_t* Wq, const uint8_t*
  *   [expert_offsets[e], expert_offsets[e+1])
  * expert_offsets: device int32 [E+1], non-decreasing, expert_offsets[0] = 0,
  * expert_offsets[E] = R.  row_token: device int32 [R], values in [0, T).
- * W_codes: [E, N, K/2]; W_scales: E consecutive Q4_SCALES_MMA tensors of
- * q4_mma_scales_bytes(N, K/16) bytes; W_tensor_scales: device float [E].
+ * W: the E experts' NVFP4 weights as one operand (raw must be NULL): codes
+ * [E, N, K/2]; scales in W->scale_layout, either E consecutive
+ * Q4_SCALES_MMA tensors of q4_mma_scales_bytes(N, K/16) bytes each or
+ * Q4_SCALES_ROWMAJOR [E, N, K/16] bytes (re-laid out into the workspace on
+ * every call: pre-convert with q4_scales_to_mma for speed); tensor_scale:
+ * device float [E], one per expert.
  * C_bf16: [R, N].  K % 256 == 0.  An expert with no rows is legal.
- * ws: q4_workspace_size_moe(T, N, K, E, R) bytes; it holds the quantized
- * tokens, their codes copied in routed order (R * K/2 bytes), the routed
- * scales and the expert schedule.
+ * ws: q4_workspace_size_moe(T, N, K, E, R) bytes, plus
+ * E * q4_mma_scales_bytes(N, K/16) more with row-major weight scales; it
+ * holds the quantized tokens, their codes copied in routed order (R * K/2
+ * bytes), the routed scales, the expert schedule (and the re-laid-out weight
+ * scales).
  */
 q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            const int32_t* expert_offsets, const int32_t* row_token, int64_t R,
-                           int E, const uint8_t* W_codes, const uint8_t* W_scales,
-                           const float* W_tensor_scales, int64_t N, void* C_bf16, void* ws,
+                           int E, const q4_operand* W, int64_t N, void* C_bf16, void* ws,
                            size_t ws_bytes, q4_stream_t stream);
 
 /*

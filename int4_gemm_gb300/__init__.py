@@ -79,7 +79,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "gemm_w4a16_int4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
     _sig(lib, "gemm_w4a16_nvfp4", I, P, P, P, P, I64, I64, I64, P, P, SZ, P)
     _sig(lib, "gemm_w4a16_mxfp4", I, P, P, P, I64, I64, I64, P, P, SZ, P)
-    _sig(lib, "grouped_gemm_moe", I, P, I64, I64, P, P, I64, I, P, P, P, I64, P, P, SZ, P)
+    _sig(lib, "grouped_gemm_moe", I, P, I64, I64, P, P, I64, I, op, I64, P, P, SZ, P)
     _sig(lib, "quantize_fp8_blockwise", I, P, I, I64, I64, I, P, P, P)
     _sig(lib, "gemm_fp8_blockwise", I, P, P, P, P, I64, I64, I64, P, I, P, SZ, P)
     _sig(lib, "w4a8_weight_scales", I, P, I64, I64, P, P)
@@ -398,15 +398,21 @@ def gemm_w4a8(qa: torch.Tensor, sa: torch.Tensor, w_codes: torch.Tensor, w_scale
     return C
 
 
-def moe_workspace(T: int, N: int, K: int, E: int, R: int, device) -> torch.Tensor:
-    return _empty(max(int(lib().q4_workspace_size_moe(T, N, K, E, R)), 256), device)
+def moe_workspace(T: int, N: int, K: int, E: int, R: int, device,
+                  w_scale_layout: str = "mma") -> torch.Tensor:
+    n = int(lib().q4_workspace_size_moe(T, N, K, E, R))
+    if w_scale_layout == "rowmajor":  # room for the weight scales in the tensor-core layout
+        n += E * mma_scales_bytes(N, K // 16)
+    return _empty(max(n, 256), device)
 
 
 def grouped_gemm_moe(tokens: torch.Tensor, expert_offsets: torch.Tensor, row_token: torch.Tensor,
                      w_codes: torch.Tensor, w_scales: torch.Tensor, w_tensor_scales: torch.Tensor,
-                     N: int, ws: Optional[torch.Tensor] = None, out=None, stream=None) -> torch.Tensor:
+                     N: int, ws: Optional[torch.Tensor] = None, out=None, stream=None,
+                     w_scale_layout: str = "mma") -> torch.Tensor:
     """C [R, N] bf16: routed rows times their expert's NVFP4 weights.
-    w_codes [E, N, K/2]; w_scales: E stacked MMA-layout scale tensors;
+    w_codes [E, N, K/2]; w_scales: E stacked MMA-layout scale tensors, or
+    [E, N, K/16] row-major bytes with ``w_scale_layout="rowmajor"``;
     w_tensor_scales [E] float32; expert_offsets [E+1] / row_token [R] int32."""
     _cuda2d(tokens, "tokens")
     T, K = tokens.shape
@@ -414,11 +420,12 @@ def grouped_gemm_moe(tokens: torch.Tensor, expert_offsets: torch.Tensor, row_tok
     R = row_token.numel()
     C = _out(out, R, N, torch.bfloat16, tokens.device)
     if ws is None:
-        ws = moe_workspace(T, N, K, E, R, tokens.device)
+        ws = moe_workspace(T, N, K, E, R, tokens.device, w_scale_layout)
+    w = _Operand(None, 0, w_codes.data_ptr(), w_scales.data_ptr(), _LAYOUT[w_scale_layout],
+                 w_tensor_scales.data_ptr())
     _check("grouped_gemm_moe", lib().grouped_gemm_moe(
         tokens.data_ptr(), T, K, expert_offsets.data_ptr(), row_token.data_ptr(), R, E,
-        w_codes.data_ptr(), w_scales.data_ptr(), w_tensor_scales.data_ptr(), N, C.data_ptr(),
-        ws.data_ptr(), ws.numel(), _stream(stream)))
+        ctypes.byref(w), N, C.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return C
 
 

@@ -542,11 +542,15 @@ q4_status gemm_w4a8(const uint8_t* qa, const float* sa, const uint8_t* w_codes,
 
 q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
                            const int32_t* expert_offsets, const int32_t* row_token, int64_t R,
-                           int E, const uint8_t* W_codes, const uint8_t* W_scales,
-                           const float* W_tensor_scales, int64_t N, void* C_bf16, void* ws,
+                           int E, const q4_operand* W, int64_t N, void* C_bf16, void* ws,
                            size_t ws_bytes, q4_stream_t stream) {
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (T < 0 || K <= 0 || R < 0 || E < 0 || N < 0) return Q4_ERR_INVALID_ARG;
+  if (!W || W->raw) return Q4_ERR_INVALID_ARG;  // the experts' weights come quantized
+  if (W->scale_layout != Q4_SCALES_MMA && W->scale_layout != Q4_SCALES_ROWMAJOR) return Q4_ERR_INVALID_ARG;
+  const uint8_t* W_codes = W->codes;
+  const uint8_t* W_scales = W->scales;
+  const float* W_tensor_scales = W->tensor_scale;
   if (K % 256) return Q4_ERR_UNSUPPORTED_SHAPE;
   if (E > 1024 || T > INT32_MAX / 2 || R > INT32_MAX / 2 || (int64_t)E * N > INT32_MAX / 2)
     return Q4_ERR_UNSUPPORTED_SHAPE;
@@ -560,8 +564,22 @@ q4_status grouped_gemm_moe(const void* tokens_bf16, int64_t T, int64_t K,
     return Q4_ERR_INVALID_ARG;
   Carver c{static_cast<uint8_t*>(ws), ws_bytes, 0};
   const MoePlan pl = plan_moe(c, T, K, E, R);
+  const bool w_rowmajor = W->scale_layout == Q4_SCALES_ROWMAJOR;
+  const size_t w_sf_bytes = mma_scales_bytes(N, K / 16);  // one expert, tensor-core layout
+  uint8_t* w_sf_mma = w_rowmajor ? c.take((size_t)E * w_sf_bytes) : nullptr;
   if (!ws || !aligned(ws, 256) || !c.ok()) return Q4_ERR_WORKSPACE;
   q4_status st;
+  if (w_rowmajor) {  // [E, N, K/16] row-major -> E tensor-core-layout tensors
+    if (N % 128 == 0) {  // whole 128-row blocks: the E experts form one tensor of E N rows
+      if ((st = launch_scales_to_mma(W_scales, (int64_t)E * N, K / 16, w_sf_mma, s)) != Q4_OK) return st;
+    } else {
+      for (int e = 0; e < E; ++e)
+        if ((st = launch_scales_to_mma(W_scales + (int64_t)e * N * (K / 16), N, K / 16,
+                                       w_sf_mma + (size_t)e * w_sf_bytes, s)) != Q4_OK)
+          return st;
+    }
+    W_scales = w_sf_mma;
+  }
   // the tokens are quantized once, as one tensor with one tensor scale
   Q4_CUDA_TRY(cudaMemsetAsync(pl.amax, 0, sizeof(unsigned), s));
   if ((st = launch_amax(tokens_bf16, Q4_BF16, T * K, pl.amax, s)) != Q4_OK) return st;

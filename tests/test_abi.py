@@ -83,6 +83,14 @@ def test_host_argument_checks(clib):
     assert clib.gemm_w4a4_mxfp4_fused(fake, 1, None, 4, 4, 128, fake, 1, fake, 1 << 20, None) == -2
     assert clib.gemm_w4a4_mxfp4_fused(fake, 5, None, 4, 4, 256, fake, 1, fake, 1 << 20, None) == -1
     assert clib.gemm_w4a4_mxfp4_fused(fake, 1, None, 4, 4, 256, fake, 2, fake, 1 << 20, None) == -1
+    # grouped MoE: the weights operand must be given, quantized, with a known scale layout
+    import int4_gemm_gb300 as q4
+    args = (fake, 8, 256, fake, fake, 16, 2)
+    assert clib.grouped_gemm_moe(*args, None, 256, fake, fake, 1 << 30, None) == -1
+    raw = q4._Operand(fake, 1, fake, fake, 1, fake)
+    assert clib.grouped_gemm_moe(*args, ctypes.byref(raw), 256, fake, fake, 1 << 30, None) == -1
+    bad = q4._Operand(None, 0, fake, fake, 7, fake)
+    assert clib.grouped_gemm_moe(*args, ctypes.byref(bad), 256, fake, fake, 1 << 30, None) == -1
     # an unknown rounding mode
     assert clib.quantize_mxfp4_ex(fake, 1, 4, 64, fake, fake, 0, 2, None) == -1
     assert clib.quantize_nvfp4_ex(fake, 1, 4, 64, fake, fake, 0, -1, fake, fake, 256, None) == -1

@@ -383,16 +383,19 @@ def _grouped_case(T, E, N, K, top, seed):
     return tok, offs, rt, ws
 
 
+@pytest.mark.parametrize("layout", ["mma", "rowmajor"])
 @pytest.mark.parametrize("case", [(64, 5, 512, 512, 2), (300, 8, 320, 768, 4), (40, 3, 256, 256, 1)])
-def test_grouped_moe(lib, case):
+def test_grouped_moe(lib, case, layout):
+    """Both weight-scale layouts (row-major ones are re-laid out by the call;
+    N = 320 is not a whole number of 128-row blocks)."""
     T, E, N, K, top = case
     tok, offs, rt, ws = _grouped_case(T, E, N, K, top, seed=T + E)
     wc, wsf, wg = [], [], []
     for w in ws:
-        c, s, g = lib.quantize_nvfp4(torch.from_numpy(w).cuda(), scale_layout="mma")
-        wc.append(c), wsf.append(s), wg.append(g)
+        c, s, g = lib.quantize_nvfp4(torch.from_numpy(w).cuda(), scale_layout=layout)
+        wc.append(c), wsf.append(s.reshape(-1)), wg.append(g)
     C = lib.grouped_gemm_moe(tok.cuda(), torch.from_numpy(offs).cuda(), torch.from_numpy(rt).cuda(),
-                             torch.stack(wc), torch.cat(wsf), torch.cat(wg), N)
+                             torch.stack(wc), torch.cat(wsf), torch.cat(wg), N, w_scale_layout=layout)
     R = oracle.grouped_gemm_moe(tok.float().numpy(), offs, rt, [oracle.quantize_nvfp4(w) for w in ws])
     assert_gemm_close(C.float().cpu().numpy(), R)
     assert lib.sync_status() == 0
