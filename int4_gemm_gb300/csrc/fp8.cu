@@ -391,6 +391,278 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
 }
 
+
+// ------------------------------------------------------------------ GEMM, CTA pairs
+// For M > 128: a cluster of two CTAs computes one 256 x 256 tile with the
+// 2-SM MMA (tcgen05.mma.cta_group::2.kind::f8f6f4, 256 x 256 x 32 per
+// instruction).  CTA rank r loads A rows m0 + 128 r .. and B rows n0 + 128 r ..
+// of each K block into its own stage; the even CTA issues the MMAs for both
+// and each CTA's TMEM receives its 128 rows x 256 columns.  Per CTA and K
+// block that is 32 KB of copies for 128 x 256 x 128 products: half the bytes
+// per product of the 128 x 128 kernel, and a quarter of the MMA instructions.
+//   warp 0      TMA producer (own A rows, own half of B) -> local `full`;
+//   warp 1      even CTA: MMA issuer (waits for its own `full` and for the odd
+//               CTA's relay on `pair_full`), two 256-column TMEM slots;
+//               odd CTA: relay (waits for its `full`, arrives on the even
+//               CTA's `pair_full`);
+//   warps 2..9  promotion: lane quarter warp % 4, column half (warp - 2) / 4
+//               (128 columns, 128 FP32 registers per thread); each reads its
+//               slot in eight 16-column loads and arrives on the even CTA's
+//               `slot_empty` (16 arrivals: 8 warps x 2 CTAs).
+constexpr int kPStages = 6;
+constexpr int kPSlots = 2;                          // TMEM slots of 256 columns
+constexpr int PBN = 256;                            // pair tile N (128 B rows per CTA)
+constexpr uint32_t kPStageBytes = 2 * kGTileBytes;  // A rows + this CTA's half of B
+constexpr uint32_t kPSmemBytes = kPStages * kPStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(kPSmemBytes <= 232448, "shared memory");
+static_assert(kPSlots * PBN <= 512, "TMEM columns");
+
+struct PSmem {
+  uint64_t full[kPStages];       // this CTA's copies of the stage landed
+  uint64_t pair_full[kPStages];  // even CTA: the odd CTA's copies landed (relay)
+  uint64_t empty[kPStages];      // the stage's MMAs are done (both CTAs)
+  uint64_t slot_full[kPSlots];   // the slot holds one K block's product (both CTAs)
+  uint64_t slot_empty[kPSlots];  // even CTA: every promotion warp of the pair read it
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(PSmem) <= 256, "barrier block");
+
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b, const Fp8Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  pdl_wait();  // operands and scales may come from the previous kernel
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  PSmem* sm = reinterpret_cast<PSmem*>(smem + kPStages * kPStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();  // 0: issues the pair's MMAs
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int KB = (int)(p.K / GBK);
+  const int num_pm = (int)((p.M + 2 * GBM - 1) / (2 * GBM)), num_pn = (int)((p.N + PBN - 1) / PBN);
+  const int total_tiles = num_pm * num_pn;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->pair_full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int s = 0; s < kPSlots; ++s) {
+      mbar_init(smem_u32(&sm->slot_full[s]), 1);
+      mbar_init(smem_u32(&sm->slot_empty[s]), 2 * kPromoWarps);
+    }
+    mbar_init(smem_u32(&sm->mma_done), 1);
+    sm->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sm->tmem_base), kPSlots * PBN);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier_sync();  // the peer's barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort_flag = &sm->abort;
+  // Pair tiles in bands of kBandM / 2 M tiles (the same 32 x 128 rows of A in
+  // L2 as the single-CTA kernel), M fastest inside a band.
+  auto tile_mn = [&](int t, int& m0, int& n0) {
+    constexpr int kBand = kBandM / 2;
+    const int band_tiles = kBand * num_pn;
+    const int band = t / band_tiles, r = t - band * band_tiles;
+    const int gm = min(kBand, num_pm - band * kBand);
+    m0 = (band * kBand + r % gm) * 2 * GBM;
+    n0 = (r / gm) * PBN;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    int issued[kPStages];
+    uint32_t issued_phase[kPStages];
+    for (int s = 0; s < kPStages; ++s) issued[s] = 0, issued_phase[s] = 0;
+    bool alive = true;
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint8_t* st = smem + stage * kPStageBytes;
+        const uint32_t full = smem_u32(&sm->full[stage]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, kPStageBytes);
+          tma_load_2d(smem_u32(st), &tmap_a, kb * GBK, m0 + rank * GBM, full);
+          tma_load_2d(smem_u32(st + kGTileBytes), &tmap_b, kb * GBK, n0 + rank * (PBN / 2), full);
+        }
+        issued[stage] = 1;
+        issued_phase[stage] = phase;
+        if (++stage == kPStages) stage = 0, phase ^= 1;
+      }
+    }
+    // drain: every copy this warp issued has landed before the CTA exits
+    if (lane == 0) {
+      KernelCtl drain = p.ctl;
+      for (int s = 0; s < kPStages; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = f8_idesc(2 * GBM, PBN);
+      uint32_t stage = 0, phase = 0, gk = 0;
+      bool alive = true;
+      for (int t = cid; t < total_tiles && alive; t += ncl) {
+        for (int kb = 0; kb < KB; ++kb, ++gk) {
+          const uint32_t slot = gk % kPSlots, sphase = (gk / kPSlots) & 1;
+          if (!mbar_wait<true>(smem_u32(&sm->slot_empty[slot]), sphase ^ 1, p.ctl, abort_flag) ||
+              !mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag) ||
+              !mbar_wait<true>(smem_u32(&sm->pair_full[stage]), phase, p.ctl, abort_flag)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * kPStageBytes);
+          const uint32_t d = tmem + slot * PBN;
+#pragma unroll
+          for (uint32_t k = 0; k < GBK / 32; ++k) {
+            const uint64_t ad = smem_desc(st + 32 * k, 16, 1024, 2);
+            const uint64_t bd = smem_desc(st + kGTileBytes + 32 * k, 16, 1024, 2);
+            tc_mma_f8_pair(d, ad, bd, idesc, k != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(smem_u32(&sm->empty[stage]), 3);    // the stage is free in both CTAs
+          tc_commit_pair_mc(smem_u32(&sm->slot_full[slot]), 3);  // both halves of the slot are ready
+          if (++stage == kPStages) stage = 0, phase ^= 1;
+        }
+      }
+      // all MMAs this thread issued are complete before TMEM is released
+      tc_commit_pair_mc(smem_u32(&sm->mma_done), 1);
+      KernelCtl drain = p.ctl;
+      mbar_wait(smem_u32(&sm->mma_done), 0, drain, nullptr);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- relay (odd CTA)
+      uint32_t stage = 0, phase = 0;
+      const uint32_t leader_pair_full = mapa_shared(smem_u32(&sm->pair_full[0]), 0);
+      bool alive = true;
+      for (int t = cid; t < total_tiles && alive; t += ncl) {
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_cluster(leader_pair_full + stage * 8);
+          if (++stage == kPStages) stage = 0, phase ^= 1;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ promotion + store
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int h = (warp - kPromoWarp0) >> 2;   // column half of the 256-column slot
+    const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16) + h * 128;
+    const uint32_t leader_slot_empty = mapa_shared(smem_u32(&sm->slot_empty[0]), 0);
+    uint32_t gk = 0;
+    bool alive = true;
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      const int64_t row = m0 + rank * GBM + q * 32 + lane;
+      const int64_t col0 = n0 + h * 128;
+      const bool row_ok = row < p.M, col_ok = col0 < p.N;
+      const float* sa_row = p.sa + (row_ok ? row : p.M - 1) * KB;
+      const float* sb_row = p.sb + (col_ok ? col0 / 128 : 0) * KB;
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      // the scales of K block kb + kSP are requested while block kb is promoted
+      float sa_q[kSP], sb_q[kSP];
+#pragma unroll
+      for (int i = 0; i < kSP; ++i) {
+        sa_q[i] = i < KB ? __ldg(sa_row + i) : 0.f;
+        sb_q[i] = i < KB ? __ldg(sb_row + i) : 0.f;
+      }
+      for (int kb0 = 0; kb0 < KB && alive; kb0 += kSP) {
+#pragma unroll
+        for (int i = 0; i < kSP; ++i) {
+          const int kb = kb0 + i;
+          if (kb >= KB || !alive) continue;
+          const uint32_t slot = gk % kPSlots, sphase = (gk / kPSlots) & 1;
+          const float sc = sa_q[i] * sb_q[i];
+          if (kb + kSP < KB) sa_q[i] = __ldg(sa_row + kb + kSP), sb_q[i] = __ldg(sb_row + kb + kSP);
+          if (!mbar_wait(smem_u32(&sm->slot_full[slot]), sphase, p.ctl, abort_flag)) {
+            alive = false;
+            continue;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // 16 columns per load
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(t_lane + slot * PBN + c * 16, r);
+            tmem_ld_wait();
+            if (c == 7) {  // the slot's columns of this warp are all in registers
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(leader_slot_empty + slot * 8);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[16 * c + j] = fmaf(__uint_as_float(r[j]), sc, acc[16 * c + j]);
+          }
+          ++gk;
+        }
+      }
+      if (!alive || !row_ok || !col_ok) continue;
+      if (p.c_dtype == Q4_BF16) {
+        uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.C) + row * p.N + col0);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * v + 2 * i], acc[8 * v + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          out[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        float4* out = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + row * p.N + col0);
+#pragma unroll
+        for (int v = 0; v < 32; ++v)
+          out[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier_sync();  // the pair's MMAs are complete in both CTAs
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kPSlots * PBN);
+  }
+  // no CTA leaves while its peer may still arrive on its barriers
+  cluster_barrier_sync();
+}
+
 }  // namespace
 
 q4_status launch_quant_fp8(const void* x, int dtype, int64_t rows, int64_t K, int block_rows,
@@ -440,6 +712,40 @@ q4_status launch_fp8_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb,
   p.sa = sa, p.sb = sb, p.C = C, p.c_dtype = c_dtype;
   p.num_m = (int)ceil_div(M, GBM), p.num_n = (int)(N / GBN);
   p.ctl = KernelCtl{device_status_ptr(), wait_budget_ns()};
+  if (M > GBM) {  // CTA pairs on 256 x 256 tiles
+    static int pair_attr[64] = {0};
+    static int max_pairs[64] = {0};
+    if (!pair_attr[dev]) {
+      Q4_CUDA_TRY(cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kPSmemBytes));
+      pair_attr[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kGThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (!max_pairs[dev]) {  // persistent: as many pairs as are resident at once
+      int n = 0;
+      cfg.gridDim = dim3((unsigned)(num_sms() / 2 * 2), 1, 1);
+      if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+        n = num_sms() / 2;
+      max_pairs[dev] = std::min(n, num_sms() / 2);
+    }
+    const int64_t ptiles = ceil_div(M, 2 * GBM) * ceil_div(N, 256);
+    const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(ptiles, max_pairs[dev]));
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, fp8_gemm_pair_kernel, ta, tb, p));
+    return Q4_OK;
+  }
   const int tiles = p.num_m * p.num_n;
   const unsigned grid = (unsigned)std::min(tiles, num_sms());
   return launch_pdl(fp8_gemm_kernel, grid, kGThreads, kGSmemBytes, stream, ta, tb, p);
