@@ -606,7 +606,7 @@ class Fp8Blockwise:
     tensor_fmt = "fp8"  # the roofline peak: a library FP8 GEMM measured live
     tensor_over_bf16 = 2.0  # else nominal dense FP8 : BF16 on GB300 (4.5 vs 2.25 PFLOP/s)
     default_steps = 200
-    kernel = "fp8_gemm_kernel"
+    kernel = "fp8_gemm_pair_kernel"  # CTA pairs (M > 128)
     launches_per_step = 2  # activation quantizer + GEMM
     kernel_launches = 1
     oracle_grain = 128
