@@ -357,9 +357,8 @@ q4_status gemm_w4a8(const uint8_t* qa, const float* sa, const uint8_t* w_codes,
 /*
  * gemm_w4a4_nvfp4 without a workspace, for callers that cannot give the
  * library any device memory beyond inputs and outputs: a plugin or custom-op
- * interface that passes only input and output buffers, an engine whose memory
- * pool is fully reserved at start-up, or code running while a stream is being
- * captured (where cudaMalloc is not allowed).  The pages have no counterpart:
+ * interface that passes only input and output buffers, or an engine whose
+ * memory pool is fully reserved at start-up.  The pages have no counterpart:
  * this is a deployment convenience, not a step of the method.
  *
  * Computes exactly what gemm_w4a4_nvfp4 computes with A given raw (A [M, K]
@@ -375,8 +374,7 @@ q4_status gemm_w4a8(const uint8_t* qa, const float* sa, const uint8_t* w_codes,
  * All calls share that array and it keeps the last call's contents, so calls
  * that overlap on the GPU (several streams or host threads) race: serialize
  * them.  The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, once per device, with that device current); make that
- * first call before any stream capture.
+ * (cudaGetSymbolAddress, once per device, with that device current).
  */
 q4_status gemm_w4a4_nvfp4_noalloc(const void* A, int a_dtype, const q4_operand* B, int64_t M,
                                   int64_t N, int64_t K, void* C, int c_dtype, q4_stream_t stream);

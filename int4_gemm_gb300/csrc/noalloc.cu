@@ -4,10 +4,8 @@
 //
 // The regular entry point quantizes the activations into a caller-provided
 // workspace.  Some callers have no way to provide one: a plugin or custom-op
-// interface that passes only input and output buffers, an engine whose memory
-// pool is fully reserved at start-up, or code that runs while a stream is being
-// captured (cudaMalloc is not allowed then and would synchronize the device
-// otherwise).  This variant keeps its scratch -- the quantized activations and
+// interface that passes only input and output buffers, or an engine whose
+// memory pool is fully reserved at start-up.  This variant keeps its scratch -- the quantized activations and
 // their scales, the amax accumulator and the tensor scale -- in one file-scope
 // device array of fixed size, so nothing is allocated per call.
 //
@@ -18,8 +16,7 @@
 //  * every call uses the same array, so calls that overlap on the GPU (other
 //    streams, other host threads) race; serialize them;
 //  * the first call on each device looks up the array's device address with
-//    cudaGetSymbolAddress (once per device, with that device current); make
-//    that first call before any stream capture.
+//    cudaGetSymbolAddress (once per device, with that device current).
 #include <mutex>
 
 #include "common.cuh"

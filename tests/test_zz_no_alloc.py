@@ -1,8 +1,8 @@
 """The no-allocation variant of the NVFP4 W4A4 GEMM.
 
 Some callers cannot give the library a workspace (a plugin interface that
-passes only inputs and outputs, an engine whose memory pool is fully reserved,
-code running during stream capture).  gemm_w4a4_nvfp4_noalloc keeps its
+passes only inputs and outputs, an engine whose memory pool is fully
+reserved).  gemm_w4a4_nvfp4_noalloc keeps its
 scratch in a fixed per-GPU device array instead.  These checks call it through
 the C ABI and compare it with gemm_w4a4_nvfp4 (the workspace entry point) on
 two calls in a row -- the second with different activations, so a scratch
