@@ -75,8 +75,12 @@ def test_fp8_quantizer_values_next_to_e4m3_midpoints(lib):
     assert np.array_equal(codes.cpu().numpy(), oc)
 
 
+# M <= 128: one CTA per 128 x 128 tile; M > 128: CTA pairs on 256 x 256 tiles,
+# incl. an odd CTA holding one row (257), N a multiple of 128 but not of 256
+# (the pair tile's second half absent: 640, 128), one K block (128)
 FP8_SHAPES = [(128, 128, 128), (1, 128, 1024), (200, 256, 512), (130, 384, 896),
-              (2048, 1536, 512), (1000, 2048, 1280)]
+              (2048, 1536, 512), (1000, 2048, 1280), (257, 640, 256), (384, 128, 384),
+              (129, 256, 128)]
 
 
 @pytest.mark.parametrize("shape", FP8_SHAPES)
