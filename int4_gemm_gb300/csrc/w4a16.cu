@@ -318,9 +318,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             if constexpr (FMT == kNvfp4) {
+              // E4M3 scale x 2^116 (exact, normal: 2^107 .. 448 * 2^116), so
+              // that one multiply gives code * scale * 2^-10; the 2^10 goes
+              // back with the tensor scale
               const uint32_t b2 = (spk[r][gl >> 1] >> ((gl & 1) * 16)) & 0xFFFFu;
-              s2[r][0] = bf16x2_splat(e4m3_value(b2 & 0xFFu));
-              s2[r][1] = bf16x2_splat(e4m3_value(b2 >> 8));
+              s2[r][0] = bf16x2_splat(e4m3_value(b2 & 0xFFu) * 0x1p116f);
+              s2[r][1] = bf16x2_splat(e4m3_value(b2 >> 8) * 0x1p116f);
             } else {
               s2[r][0] = s2[r][1] = bf16x2_splat(e8m0_value((spk[r][gl >> 2] >> ((gl & 3) * 8)) & 0xFFu));
             }
@@ -337,14 +340,25 @@ __global__ void __launch_bounds__(kThreads, 2)
               const uint32_t ls = lo & 0x88888888u, hs = hi & 0x88888888u;
               const uint32_t sl = s2[2 * t][w >> 1], sh = s2[2 * t + 1][w >> 1];
               uint32_t pl[4], ph[4];
-              pl[0] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<0>(lo, ls), kTwo126), sl);
-              pl[1] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<1>(lo, ls), kTwo126), sl);
-              pl[2] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<2>(lo, ls), kTwo126), sl);
-              pl[3] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<3>(lo, ls), kTwo126), sl);
-              ph[0] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<0>(hi, hs), kTwo126), sh);
-              ph[1] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<1>(hi, hs), kTwo126), sh);
-              ph[2] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<2>(hi, hs), kTwo126), sh);
-              ph[3] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<3>(hi, hs), kTwo126), sh);
+              if constexpr (FMT == kNvfp4) {  // code * 2^-126 times scale * 2^116
+                pl[0] = bf16x2_mul(e2m1_pair_bits<0>(lo, ls), sl);
+                pl[1] = bf16x2_mul(e2m1_pair_bits<1>(lo, ls), sl);
+                pl[2] = bf16x2_mul(e2m1_pair_bits<2>(lo, ls), sl);
+                pl[3] = bf16x2_mul(e2m1_pair_bits<3>(lo, ls), sl);
+                ph[0] = bf16x2_mul(e2m1_pair_bits<0>(hi, hs), sh);
+                ph[1] = bf16x2_mul(e2m1_pair_bits<1>(hi, hs), sh);
+                ph[2] = bf16x2_mul(e2m1_pair_bits<2>(hi, hs), sh);
+                ph[3] = bf16x2_mul(e2m1_pair_bits<3>(hi, hs), sh);
+              } else {  // E8M0 scales span 2^-127 .. 2^127: times 2^126, then the scale
+                pl[0] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<0>(lo, ls), kTwo126), sl);
+                pl[1] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<1>(lo, ls), kTwo126), sl);
+                pl[2] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<2>(lo, ls), kTwo126), sl);
+                pl[3] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<3>(lo, ls), kTwo126), sl);
+                ph[0] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<0>(hi, hs), kTwo126), sh);
+                ph[1] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<1>(hi, hs), kTwo126), sh);
+                ph[2] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<2>(hi, hs), kTwo126), sh);
+                ph[3] = bf16x2_mul(bf16x2_mul(e2m1_pair_bits<3>(hi, hs), kTwo126), sh);
+              }
 #pragma unroll
               for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -439,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---- rank q adds rows [q * per, (q + 1) * per) over the source ranks in order
   // and applies the NVFP4 tensor scale (read after the dependency wait)
-  const float gsc = FMT == kNvfp4 ? __ldg(wg) : 1.f;
+  // NVFP4: the tensor scale, times the 2^10 the weights were scaled down by
+  // (exact: a power of two)
+  const float gsc = FMT == kNvfp4 ? __ldg(wg) * 1024.0f : 1.f;
   const int r_lo = rank * per, r_hi = min(kRows, r_lo + per);
   const int tq = (mt + 3) / 4;  // groups of four tokens
   for (int e = tid; e < (r_hi - r_lo) * tq; e += kThreads) {
