@@ -680,7 +680,7 @@ class W4a8(Fp8Blockwise):
     """W4A8: A quantized on the fly into FP8 (1, 128) blocks, INT4 g128 weights
     converted to E4M3 inside the GEMM (their FP16 group scales in the promotion)."""
     name = "w4a8"
-    kernel = "w4a8_gemm_kernel"
+    kernel = "w4a8_gemm_pair_kernel"  # CTA pairs (M > 128)
 
     def config(self):
         return {"workload": f"w4a8 A bf16 {self.M}x{self.K} (FP8 1x128 blocks, quantized on the fly), "

@@ -373,6 +373,322 @@ __global__ void __launch_bounds__(kWThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ CTA pairs
+// For M > 128: the same pipeline on 256 x 256 tiles with the 2-SM MMA
+// (tcgen05.mma.cta_group::2.kind::f8f6f4, 256 x 256 x 32).  CTA rank r copies
+// A rows m0 + 128 r .. and the INT4 codes of B rows n0 + 128 r .. of each K
+// block, its converters expand its half of B, and the even CTA issues the
+// MMAs once its own converted stage is ready and the odd CTA's relay lane has
+// arrived on its `pair_full`.  Both CTAs copy the K block's 256 weight scales
+// (the tile's columns); two 256-column TMEM slots; each promotion warp owns a
+// lane quarter x 128 columns (128 FP32 registers per thread) and arrives on
+// the even CTA's `slot_empty` (16 arrivals) after it has read the slot and the
+// scale buffer.  A scale buffer is refilled (K block g, buffer g % 16) after
+// the MMAs of block g - 5 completed in both CTAs, which were issued after
+// every promotion of block g - 7 had read its buffer.
+constexpr int kPStages = 5;
+constexpr int kPSlots = 2;
+constexpr int PBN = 256;                                   // pair tile N
+constexpr uint32_t kPScaleBufBytes = PBN * sizeof(float);  // one K block's tile columns
+constexpr uint32_t kPSmemBytes =
+    kPStages * kWStageBytes + kScaleBufs * kPScaleBufBytes + 1024 /*align*/ + 512 /*barriers*/;
+static_assert(kPSmemBytes <= 232448, "shared memory");
+static_assert(kPSlots * PBN <= 512, "TMEM columns");
+
+struct PSmem {
+  uint64_t full[kPStages];       // this CTA's A tile and INT4 tile landed
+  uint64_t b_ready[kPStages];    // this CTA's half of B converted
+  uint64_t pair_full[kPStages];  // even CTA: the odd CTA's stage is converted (relay)
+  uint64_t empty[kPStages];      // the stage's MMAs are done (both CTAs)
+  uint64_t slot_full[kPSlots];
+  uint64_t slot_empty[kPSlots];  // even CTA: every promotion warp of the pair is done
+  uint64_t sc_full[kScaleBufs];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(PSmem) <= 512, "barrier block");
+
+constexpr uint32_t kPIdesc = (1u << 4) | ((uint32_t)(PBN >> 3) << 17) | ((uint32_t)((2 * WBM) >> 4) << 24);
+
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kPIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    w4a8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                          const __grid_constant__ CUtensorMap tmap_w, const W4a8Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  pdl_wait();  // operands and scales may come from the previous kernel
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  float* sbuf = reinterpret_cast<float*>(smem + kPStages * kWStageBytes);
+  PSmem* sm = reinterpret_cast<PSmem*>(smem + kPStages * kWStageBytes + kScaleBufs * kPScaleBufBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();  // 0: issues the pair's MMAs
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int KB = (int)(p.K / WBK);
+  const int num_pm = (int)((p.M + 2 * WBM - 1) / (2 * WBM)), num_pn = (int)((p.N + PBN - 1) / PBN);
+  const int total_tiles = num_pm * num_pn;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->b_ready[s]), kConvWarps);
+      mbar_init(smem_u32(&sm->pair_full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int s = 0; s < kPSlots; ++s) {
+      mbar_init(smem_u32(&sm->slot_full[s]), 1);
+      mbar_init(smem_u32(&sm->slot_empty[s]), 2 * kPromWarps);
+    }
+    for (int b = 0; b < kScaleBufs; ++b) mbar_init(smem_u32(&sm->sc_full[b]), 1);
+    mbar_init(smem_u32(&sm->mma_done), 1);
+    sm->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_w);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sm->tmem_base), kPSlots * PBN);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier_sync();  // the peer's barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort_flag = &sm->abort;
+  auto tile_mn = [&](int t, int& m0, int& n0) {  // pair tiles in bands of kBandM / 2
+    constexpr int kBand = kBandM / 2;
+    const int band_tiles = kBand * num_pn;
+    const int band = t / band_tiles, r = t - band * band_tiles;
+    const int gm = min(kBand, num_pm - band * kBand);
+    m0 = (band * kBand + r % gm) * 2 * WBM;
+    n0 = (r / gm) * PBN;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0, gk = 0;
+    int issued[kPStages];
+    uint32_t issued_phase[kPStages];
+    for (int s = 0; s < kPStages; ++s) issued[s] = 0, issued_phase[s] = 0;
+    bool alive = true;
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      // the tile's weight-scale columns (a tile past N by 128 columns copies 128)
+      const uint32_t sc_bytes = (uint32_t)min((int64_t)PBN, p.N - n0) * 4u;
+      for (int kb = 0; kb < KB; ++kb, ++gk) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint8_t* st = smem + stage * kWStageBytes;
+        if (lane == 0) {
+          const uint32_t full = smem_u32(&sm->full[stage]);
+          mbar_arrive_expect_tx(full, kATileBytes + kBCodeBytes);
+          tma_load_2d(smem_u32(st), &tmap_a, kb * WBK, m0 + rank * WBM, full);
+          tma_load_2d(smem_u32(st + kATileBytes + kBTileBytes), &tmap_w, kb * (WBK / 2),
+                      n0 + rank * (PBN / 2), full);
+          const uint32_t b = gk % kScaleBufs;
+          const uint32_t scb = smem_u32(&sm->sc_full[b]);
+          mbar_arrive_expect_tx(scb, sc_bytes);
+          bulk_load(smem_u32(sbuf + b * PBN), p.wsc + (int64_t)kb * p.N + n0, sc_bytes, scb);
+        }
+        issued[stage] = 1;
+        issued_phase[stage] = phase;
+        if (++stage == kPStages) stage = 0, phase ^= 1;
+      }
+    }
+    if (lane == 0) {
+      KernelCtl drain = p.ctl;
+      for (int s = 0; s < kPStages; ++s)
+        if (issued[s]) mbar_wait(smem_u32(&sm->full[s]), issued_phase[s], drain, nullptr);
+      for (uint32_t g = gk > (uint32_t)kScaleBufs ? gk - kScaleBufs : 0u; g < gk; ++g)
+        mbar_wait(smem_u32(&sm->sc_full[g % kScaleBufs]), (g / kScaleBufs) & 1, drain, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      uint32_t stage = 0, phase = 0, gk = 0;
+      bool alive = true;
+      for (int t = cid; t < total_tiles && alive; t += ncl) {
+        for (int kb = 0; kb < KB; ++kb, ++gk) {
+          const uint32_t slot = gk % kPSlots, sphase = (gk / kPSlots) & 1;
+          // b_ready implies full: the converters waited for the stage's copies
+          if (!mbar_wait<true>(smem_u32(&sm->slot_empty[slot]), sphase ^ 1, p.ctl, abort_flag) ||
+              !mbar_wait(smem_u32(&sm->b_ready[stage]), phase, p.ctl, abort_flag) ||
+              !mbar_wait<true>(smem_u32(&sm->pair_full[stage]), phase, p.ctl, abort_flag)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * kWStageBytes);
+          const uint32_t d = tmem + slot * PBN;
+#pragma unroll
+          for (uint32_t k = 0; k < WBK / 32; ++k)
+            mma_e4m3_pair(d, smem_desc(st + 32 * k, 16, 1024, 2),
+                          smem_desc(st + kATileBytes + 32 * k, 16, 1024, 2), k != 0 ? 1u : 0u);
+          tc_commit_pair_mc(smem_u32(&sm->empty[stage]), 3);
+          tc_commit_pair_mc(smem_u32(&sm->slot_full[slot]), 3);
+          if (++stage == kPStages) stage = 0, phase ^= 1;
+        }
+      }
+      tc_commit_pair_mc(smem_u32(&sm->mma_done), 1);
+      KernelCtl drain = p.ctl;
+      mbar_wait(smem_u32(&sm->mma_done), 0, drain, nullptr);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- relay (odd CTA)
+      uint32_t stage = 0, phase = 0;
+      const uint32_t leader_pair_full = mapa_shared(smem_u32(&sm->pair_full[0]), 0);
+      bool alive = true;
+      for (int t = cid; t < total_tiles && alive; t += ncl) {
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->b_ready[stage]), phase, p.ctl, abort_flag)) {
+            alive = false;
+            break;
+          }
+          mbar_arrive_cluster(leader_pair_full + stage * 8);
+          if (++stage == kPStages) stage = 0, phase ^= 1;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < kPromWarp0) {
+    // ------------------------------------------------------------ converters
+    // the same item order and swizzle as the single-CTA kernel, on this CTA's
+    // 128 rows of the tile's B
+    const int cw = warp - kConvWarp0;
+    uint32_t stage = 0, phase = 0;
+    bool alive = true;
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.ctl, abort_flag)) {
+          alive = false;
+          break;
+        }
+        uint8_t* st = smem + stage * kWStageBytes;
+        const uint8_t* src = st + kATileBytes + kBTileBytes;
+        uint8_t* dst = st + kATileBytes;
+#pragma unroll
+        for (int k = 0; k < kConvItems; ++k) {
+          const int it = k * kConvWarps * 32 + cw * 32 + lane;
+          const int r = it >> 2, i = it & 3;
+          const uint4 w = *reinterpret_cast<const uint4*>(src + r * 64 + i * 16);
+          const uint2 e0 = int4x8_to_e4m3(w.x), e1 = int4x8_to_e4m3(w.y);
+          const uint2 e2 = int4x8_to_e4m3(w.z), e3 = int4x8_to_e4m3(w.w);
+          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i) ^ (r & 7)) << 4)) =
+              make_uint4(e0.x, e0.y, e1.x, e1.y);
+          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * i + 1) ^ (r & 7)) << 4)) =
+              make_uint4(e2.x, e2.y, e3.x, e3.y);
+        }
+        fence_proxy_async_smem();  // the tensor cores read what these threads wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->b_ready[stage]));
+        if (++stage == kPStages) stage = 0, phase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ promotion + store
+    const int q = warp & 3;                   // TMEM lane quarter this warp may access
+    const int h = (warp - kPromWarp0) >> 2;   // column half of the 256-column slot
+    const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16) + h * 128;
+    const uint32_t leader_slot_empty = mapa_shared(smem_u32(&sm->slot_empty[0]), 0);
+    uint32_t gk = 0;
+    bool alive = true;
+    for (int t = cid; t < total_tiles && alive; t += ncl) {
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      const int64_t row = m0 + rank * WBM + q * 32 + lane;
+      const int64_t col0 = n0 + h * 128;
+      const bool row_ok = row < p.M, col_ok = col0 < p.N;
+      const float* sa_row = p.sa + (row_ok ? row : p.M - 1) * KB;
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      float sa_q[kSP];
+#pragma unroll
+      for (int i = 0; i < kSP; ++i) sa_q[i] = i < KB ? __ldg(sa_row + i) : 0.f;
+      for (int kb0 = 0; kb0 < KB && alive; kb0 += kSP) {
+#pragma unroll
+        for (int i = 0; i < kSP; ++i) {
+          const int kb = kb0 + i;
+          if (kb >= KB || !alive) continue;
+          const uint32_t slot = gk % kPSlots, sphase = (gk / kPSlots) & 1;
+          const uint32_t b = gk % kScaleBufs;
+          const float sa_k = sa_q[i];
+          if (kb + kSP < KB) sa_q[i] = __ldg(sa_row + kb + kSP);
+          if (!mbar_wait(smem_u32(&sm->slot_full[slot]), sphase, p.ctl, abort_flag) ||
+              !mbar_wait(smem_u32(&sm->sc_full[b]), (gk / kScaleBufs) & 1, p.ctl, abort_flag)) {
+            alive = false;
+            continue;
+          }
+          tc_fence_after();
+          const float4* sw = reinterpret_cast<const float4*>(sbuf + b * PBN + h * 128);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {  // 8 columns per load
+            uint32_t r[8];
+            tmem_ld_32x32b_x8(t_lane + slot * PBN + c * 8, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              const float4 s4 = sw[2 * c + v];  // zero past N (not stored then)
+              acc[8 * c + 4 * v] = fmaf(__uint_as_float(r[4 * v]) * s4.x, sa_k, acc[8 * c + 4 * v]);
+              acc[8 * c + 4 * v + 1] = fmaf(__uint_as_float(r[4 * v + 1]) * s4.y, sa_k, acc[8 * c + 4 * v + 1]);
+              acc[8 * c + 4 * v + 2] = fmaf(__uint_as_float(r[4 * v + 2]) * s4.z, sa_k, acc[8 * c + 4 * v + 2]);
+              acc[8 * c + 4 * v + 3] = fmaf(__uint_as_float(r[4 * v + 3]) * s4.w, sa_k, acc[8 * c + 4 * v + 3]);
+            }
+          }
+          // the slot and the scale buffer go back together (their refills wait,
+          // through the MMA, for this arrival)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(leader_slot_empty + slot * 8);
+          ++gk;
+        }
+      }
+      if (!alive || !row_ok || !col_ok) continue;
+      if (p.c_dtype == Q4_BF16) {
+        uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.C) + row * p.N + col0);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * v + 2 * i], acc[8 * v + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          out[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        float4* out = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) + row * p.N + col0);
+#pragma unroll
+        for (int v = 0; v < 32; ++v)
+          out[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier_sync();  // the pair's MMAs are complete in both CTAs
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kPSlots * PBN);
+  }
+  // no CTA leaves while its peer may still arrive on its barriers
+  cluster_barrier_sync();
+}
+
 // FP16 scale bits [N, KB] -> FP32 [KB, N] (the layout whose K-block rows the
 // GEMM copies whole).
 __global__ void __launch_bounds__(256)
@@ -414,6 +730,40 @@ q4_status launch_w4a8_gemm(const uint8_t* qa, const float* sa, const uint8_t* wq
   p.sa = sa, p.wsc = wsc, p.C = C, p.c_dtype = c_dtype;
   p.num_m = (int)ceil_div(M, WBM), p.num_n = (int)(N / WBN);
   p.ctl = KernelCtl{device_status_ptr(), wait_budget_ns()};
+  if (M > WBM) {  // CTA pairs on 256 x 256 tiles
+    static int pair_attr[64] = {0};
+    static int max_pairs[64] = {0};
+    if (!pair_attr[dev]) {
+      Q4_CUDA_TRY(cudaFuncSetAttribute(w4a8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kPSmemBytes));
+      pair_attr[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kWThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (!max_pairs[dev]) {  // persistent: as many pairs as are resident at once
+      int n = 0;
+      cfg.gridDim = dim3((unsigned)(num_sms() / 2 * 2), 1, 1);
+      if (cudaOccupancyMaxActiveClusters(&n, w4a8_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+        n = num_sms() / 2;
+      max_pairs[dev] = std::min(n, num_sms() / 2);
+    }
+    const int64_t ptiles = ceil_div(M, 2 * WBM) * ceil_div(N, 256);
+    const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(ptiles, max_pairs[dev]));
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    Q4_CUDA_TRY(cudaLaunchKernelEx(&cfg, w4a8_gemm_pair_kernel, ta, tw, p));
+    return Q4_OK;
+  }
   const int tiles = p.num_m * p.num_n;
   const unsigned grid = (unsigned)std::min(tiles, num_sms());
   return launch_pdl(w4a8_gemm_kernel, grid, kWThreads, kWSmemBytes, stream, ta, tw, p);

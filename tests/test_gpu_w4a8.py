@@ -30,8 +30,13 @@ def test_w4a8_weight_scales_conversion(lib):
     assert np.array_equal(got.cpu().numpy(), want)
 
 
+# M <= 128: one CTA per 128 x 128 tile; M > 128: CTA pairs on 256 x 256
+# tiles, incl. an odd CTA holding one row (257), N a multiple of 128 but not
+# of 256 (the pair tile's second half and its weight scales absent: 384, 640,
+# 128), one K block (128)
 W4A8_SHAPES = [(128, 128, 128), (1, 128, 1024), (200, 256, 512), (130, 384, 896),
-               (2048, 1536, 512), (1000, 2048, 2304)]
+               (2048, 1536, 512), (1000, 2048, 2304), (257, 640, 256), (384, 128, 384),
+               (129, 256, 128)]
 
 
 @pytest.mark.parametrize("shape", W4A8_SHAPES)
