@@ -67,6 +67,13 @@ NCU_TRAFFIC = {
     # amax_kernel and nvfp4_kernel, mean per launch over 2 steps (ncu flushes L2
     # before each kernel, so the encode pass's reuse of x from L2 is not in it)
     "quantize": 141.0e6,
+    "quantize_rne": 141.0e6,
+    # fp8_gemm_pair_kernel at 8192 x 28672 x 8192, mean of 3 launches (681 MB
+    # read: B once per band of 4096 A rows; 450 MB of C written)
+    "fp8_blockwise": 1131.1e6,
+    # w4a8_gemm_pair_kernel at 8192 x 28672 x 8192, mean of 3 launches (385 MB
+    # read, 445 MB written)
+    "w4a8": 830.2e6,
 }
 
 
