@@ -285,6 +285,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[
                : "r"(taddr)
                : "memory");
 }
+// Two FP32 fused multiply-adds in one instruction (fma.rn.f32x2): a_i =
+// RN(x_i * s_i + a_i) for i = 0, 1, each rounded exactly as fmaf rounds it.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float s0, float s1) {
+  asm("{\n\t.reg .b64 a, x, s;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\tmov.b64 s, {%4, %5};\n\t"
+      "fma.rn.f32x2 a, x, s, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1), "f"(s0), "f"(s1));
+}
+// Two FP32 products in one instruction (mul.rn.f32x2), each rounded as x * s is.
+__device__ __forceinline__ void mul2(float& d0, float& d1, float x0, float x1, float s0, float s1) {
+  asm("{\n\t.reg .b64 d, x, s;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 s, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, x, s;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(x0), "f"(x1), "f"(s0), "f"(s1));
+}
 // ---- CTA pairs (cta_group::2): every tcgen05 operation of a kernel that uses
 // the 2-SM MMA carries the pair qualifier.  Both CTAs of the pair allocate
 // (collectively: the same columns in both), relinquish and free.

@@ -625,7 +625,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
               if (lane == 0) mbar_arrive_cluster(leader_slot_empty + slot * 8);
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[16 * c + j] = fmaf(__uint_as_float(r[j]), sc, acc[16 * c + j]);
+            for (int j = 0; j < 16; j += 2)  // two columns per instruction
+              fma2(acc[16 * c + j], acc[16 * c + j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]), sc, sc);
           }
           ++gk;
         }

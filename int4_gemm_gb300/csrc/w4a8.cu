@@ -640,12 +640,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tmem_ld_32x32b_x8(t_lane + slot * PBN + c * 8, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              const float4 s4 = sw[2 * c + v];  // zero past N (not stored then)
-              acc[8 * c + 4 * v] = fmaf(__uint_as_float(r[4 * v]) * s4.x, sa_k, acc[8 * c + 4 * v]);
-              acc[8 * c + 4 * v + 1] = fmaf(__uint_as_float(r[4 * v + 1]) * s4.y, sa_k, acc[8 * c + 4 * v + 1]);
-              acc[8 * c + 4 * v + 2] = fmaf(__uint_as_float(r[4 * v + 2]) * s4.z, sa_k, acc[8 * c + 4 * v + 2]);
-              acc[8 * c + 4 * v + 3] = fmaf(__uint_as_float(r[4 * v + 3]) * s4.w, sa_k, acc[8 * c + 4 * v + 3]);
+            for (int v = 0; v < 2; ++v) {  // two columns per instruction
+              const float4 s4 = sw[2 * c + v];  // stale past N (not stored then)
+              float t0, t1, t2, t3;
+              mul2(t0, t1, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), s4.x, s4.y);
+              mul2(t2, t3, __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]), s4.z, s4.w);
+              fma2(acc[8 * c + 4 * v], acc[8 * c + 4 * v + 1], t0, t1, sa_k, sa_k);
+              fma2(acc[8 * c + 4 * v + 2], acc[8 * c + 4 * v + 3], t2, t3, sa_k, sa_k);
             }
           }
           // the slot and the scale buffer go back together (their refills wait,
