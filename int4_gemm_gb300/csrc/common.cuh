@@ -302,6 +302,14 @@ __device__ __forceinline__ void mul2(float& d0, float& d1, float x0, float x1, f
       : "=f"(d0), "=f"(d1)
       : "f"(x0), "f"(x1), "f"(s0), "f"(s1));
 }
+// Two FP32 differences in one instruction (sub.rn.f32x2), each rounded as x - y is.
+__device__ __forceinline__ void sub2(float& d0, float& d1, float x0, float x1, float y0, float y1) {
+  asm("{\n\t.reg .b64 d, x, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, x, y;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
 // ---- CTA pairs (cta_group::2): every tcgen05 operation of a kernel that uses
 // the 2-SM MMA carries the pair qualifier.  Both CTAs of the pair allocate
 // (collectively: the same columns in both), relinquish and free.

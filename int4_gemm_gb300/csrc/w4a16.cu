@@ -419,11 +419,12 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float slo = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? plo >> 16 : plo)));
           const float shi = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? phi >> 16 : phi)));
 #pragma unroll
-          for (int s = 0; s < TS; ++s) {
-            acc[t][s][0] = fmaf(part[t][s][0] - c0v[s], slo, acc[t][s][0]);
-            acc[t][s][1] = fmaf(part[t][s][1] - c1v[s], slo, acc[t][s][1]);
-            acc[t][s][2] = fmaf(part[t][s][2] - c0v[s], shi, acc[t][s][2]);
-            acc[t][s][3] = fmaf(part[t][s][3] - c1v[s], shi, acc[t][s][3]);
+          for (int s = 0; s < TS; ++s) {  // pairs of tokens per instruction, same rounding
+            float d0, d1, d2, d3;
+            sub2(d0, d1, part[t][s][0], part[t][s][1], c0v[s], c1v[s]);
+            sub2(d2, d3, part[t][s][2], part[t][s][3], c0v[s], c1v[s]);
+            fma2(acc[t][s][0], acc[t][s][1], d0, d1, slo, slo);
+            fma2(acc[t][s][2], acc[t][s][3], d2, d3, shi, shi);
           }
         }
       }
