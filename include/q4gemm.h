@@ -188,7 +188,12 @@ q4_status q4_scales_to_mma(const uint8_t* src, int64_t rows, int64_t nsf, uint8_
  *   MXFP4: x_hat = e2m1(code) * 2^(scale - 127)
  * c_dtype is Q4_F32 or Q4_BF16 (round to nearest even).  K % 256 == 0; M and
  * N are arbitrary (M, N >= 0).  Raw operands are quantized on the fly (see
- * q4_operand).  ws: q4_workspace_size(op, M, N, K) bytes.
+ * q4_operand).  ws: q4_workspace_size(op, M, N, K) bytes.  For shapes with
+ * few output tiles the GEMM splits K over a cluster of CTAs; with a
+ * workspace of that full size their partial sums meet in it (through L2),
+ * otherwise (ws NULL or smaller, allowed when both operands come quantized
+ * with Q4_SCALES_MMA scales) in distributed shared memory, with the same
+ * result bit for bit.
  */
 q4_status gemm_w4a4_nvfp4(const q4_operand* A, const q4_operand* B, int64_t M, int64_t N,
                           int64_t K, void* C, int c_dtype, void* ws, size_t ws_bytes,

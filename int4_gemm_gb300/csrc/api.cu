@@ -192,11 +192,24 @@ q4_status resolve_operand(const q4_operand* op, int64_t rows, int64_t K, bool nv
   return Q4_OK;
 }
 
+// The operands' quantized copies, then room for split-K partial sums.
 size_t gemm_ws_bytes(int64_t M, int64_t N, int64_t K, int block) {
   Carver c{nullptr, 0, 0};
   plan_operand(c, M, K, block, block == 16);
   plan_operand(c, N, K, block, block == 16);
+  c.take(fp4_splitk_partial_bytes(M, N, K, num_sms()));
   return c.used;
+}
+
+// The split-K partial region at the end of a carved workspace, when ws holds
+// it (otherwise the partial sums meet in distributed shared memory).
+void plan_partials(Carver& c, void* ws, int64_t M, int64_t N, int64_t K, Fp4GemmArgs& g) {
+  const size_t bytes = fp4_splitk_partial_bytes(M, N, K, num_sms());
+  uint8_t* part = c.take(bytes);
+  if (bytes && ws && aligned(ws, 256) && c.ok()) {
+    g.part_ws = part;
+    g.part_ws_bytes = bytes;
+  }
 }
 
 struct MoePlan {
@@ -245,6 +258,7 @@ q4_status gemm_fp4_common(bool nv, const q4_operand* A, const q4_operand* B, int
   const OperandPlan pb = plan_operand(c, N, K, block, nv);
   if (need_ws && (!ws || !aligned(ws, 256) || !c.ok())) return Q4_ERR_WORKSPACE;
   Fp4GemmArgs g = {};
+  plan_partials(c, ws, M, N, K, g);
   if ((st = resolve_operand(A, M, K, nv, pa, s, &g.a_codes, &g.a_scales, &g.a_g)) != Q4_OK) return st;
   if ((st = resolve_operand(B, N, K, nv, pb, s, &g.b_codes, &g.b_scales, &g.b_g)) != Q4_OK) return st;
   g.M = M; g.N = N; g.K = K; g.C = C; g.c_dtype = c_dtype; g.nvfp4 = nv;
@@ -412,6 +426,7 @@ q4_status gemm_w4a4_mxfp4_fused(const void* A_raw, int a_dtype, const q4_operand
   const OperandPlan pb = plan_operand(c, N, K, 32, false);
   if (!ws || !aligned(ws, 256) || !c.ok()) return Q4_ERR_WORKSPACE;
   Fp4GemmArgs g = {};
+  plan_partials(c, ws, M, N, K, g);
   if (M * (K / 16) < ((int64_t)1 << 31)) {  // the prologue's unit indices are 32-bit
     g.a_raw = A_raw;
     g.a_dtype = a_dtype;

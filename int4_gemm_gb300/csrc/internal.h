@@ -57,8 +57,12 @@ struct Fp4GemmArgs {
   const void* a_raw = nullptr;
   int a_dtype = 0;
   unsigned* gate = nullptr;
+  // split-K partial sums (optional): used when at least the launch's need
+  void* part_ws = nullptr;
+  size_t part_ws_bytes = 0;
 };
 q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream);
+size_t fp4_splitk_partial_bytes(int64_t M, int64_t N, int64_t K, int nsms);
 
 // Grouped (routed MoE) NVFP4 GEMM on a pre-quantized token tensor.
 struct GroupedArgs {

@@ -142,6 +142,9 @@ struct Params {
   uint8_t* a_codes_w;
   uint8_t* a_sf_w;
   unsigned* gate;
+  // split-K: [tile][rank][BNT / 4][BM] float4 partial sums in global memory
+  // (they meet in L2); nullptr: through distributed shared memory
+  float4* part_g;
   KernelCtl ctl;
 };
 
@@ -616,6 +619,31 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
       if (!mbar_wait(smem_u32(&sm->acc_full), tcount & 1, p.ctl, abort_flag)) break;
       tc_fence_after();
       if constexpr (KS > 1) {
+        if (p.part_g) {
+          // split-K through L2: this CTA's FP32 partial tile -> its slot of the
+          // workspace, [BNT / 4][BM] float4 (a warp stores 512 contiguous bytes)
+          const bool has_k = kb_end > kb_begin;
+          float4* dst = p.part_g + (size_t)(cid * KS + krank) * (BNT / 4) * BM + (q * 32 + lane);
+#pragma unroll 1
+          for (int c0 = 0; c0 < BNT / 32; c0 += 4) {  // four 32-column loads per TMEM wait
+            uint32_t r[4][32];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (c0 + g) * 32, r[g]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[(size_t)((c0 + g) * 8 + v) * BM] =
+                    has_k ? make_float4(__uint_as_float(r[g][4 * v]), __uint_as_float(r[g][4 * v + 1]),
+                                        __uint_as_float(r[g][4 * v + 2]), __uint_as_float(r[g][4 * v + 3]))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          tc_fence_before();
+          ++tcount;
+          continue;
+        }
         // split-K: this CTA's FP32 partial tile -> shared memory (the ring is idle:
         // every copy of this CTA's K slice was consumed before acc_full)
         float* part = reinterpret_cast<float*>(smem) + (q * 32 + lane) * kPartStride;
@@ -715,6 +743,56 @@ __global__ void __launch_bounds__(block_threads<GROUPED>(), 1)
     else tmem_dealloc(tmem, kTmemCols);
   }
   if constexpr (KS > 1) {
+   if (p.part_g) {
+    // rank q reduces rows [q * 128 / KS, (q + 1) * 128 / KS) of the tile over
+    // all ranks' partials in L2, in rank order, applies gA * gB and stores.
+    // The cluster barrier (release / acquire at cluster scope) orders every
+    // rank's partial stores before these loads; no CTA touches another's
+    // shared memory, so none waits for the others afterwards.
+    float alpha = 1.f;
+    if constexpr (NV) alpha = __ldg(p.a_g) * __ldg(p.b_g);
+    cluster_barrier_sync();
+    const int t = cid;  // one tile per cluster
+    if (t < total_tiles && !*abort_flag) {
+      const TileInfo ti = tile_at(t);
+      const int rows = (BM + KS - 1) / KS;
+      const int r_lo = krank * rows, r_hi = min(BM, r_lo + rows);
+      const int nr = r_hi - r_lo;
+      const float4* src = p.part_g + (size_t)cid * KS * (BNT / 4) * BM;
+      for (int e = threadIdx.x; e < nr * (BNT / 4); e += blockDim.x) {
+        const int c4 = e / nr, r = r_lo + e % nr;  // consecutive threads: consecutive rows
+        float4 sum = __ldcg(src + (size_t)c4 * BM + r);
+#pragma unroll
+        for (int qq = 1; qq < KS; ++qq) {
+          const float4 v = __ldcg(src + (size_t)(qq * (BNT / 4) + c4) * BM + r);
+          sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+        }
+        const int row = ti.m_row0 + r, col = ti.n0 + 4 * c4;
+        if (row >= ti.m_end || col >= p.N) continue;
+        const float o[4] = {sum.x * alpha, sum.y * alpha, sum.z * alpha, sum.w * alpha};
+        if (p.c_dtype == Q4_BF16) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.N + col;
+          if (col + 4 <= p.N && (p.N % 4) == 0) {  // 8-byte aligned: one store
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]), hi = __floats2bfloat162_rn(o[2], o[3]);
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t*>(&lo);
+            w.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(out) = w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (col + i < p.N) out[i] = __float2bfloat16_rn(o[i]);
+          }
+        } else {
+          float* out = reinterpret_cast<float*>(p.C) + (int64_t)row * p.N + col;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (col + i < p.N) out[i] = o[i];
+        }
+      }
+    }
+    return;
+   }
     // rank q reduces rows [q * 128 / KS, (q + 1) * 128 / KS) of the tile over all
     // ranks' partials, in rank order, then applies gA * gB and stores
     float alpha = 1.f;
@@ -986,6 +1064,18 @@ q4_status dispatch_splitk(int ks, const CUtensorMap& ta, const CUtensorMap& tb, 
 
 }  // namespace
 
+// Workspace bytes for the split-K partial sums of an M x N x K FP4 GEMM: the
+// most the launch below can take (clusters of up to 4 CTAs), 0 when the shape
+// does not split K.  nsms: the SM count the launch will see.
+size_t fp4_splitk_partial_bytes(int64_t M, int64_t N, int64_t K, int nsms) {
+  if (M <= 0 || N <= 0 || K / BK < 2) return 0;
+  const int64_t num_m = ceil_div(M, BM);
+  const int64_t t128 = num_m * ceil_div(N, 128), t256 = num_m * ceil_div(N, (int64_t)BN);
+  if (t128 * 2 <= nsms) return (size_t)t128 * 4 * BM * 128 * sizeof(float);
+  if (t256 * 2 <= nsms) return (size_t)t256 * 4 * BM * BN * sizeof(float);
+  return 0;
+}
+
 q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0) return Q4_OK;
   CUtensorMap ta, tb;
@@ -1040,6 +1130,11 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   // one-CTA-per-SM blocks are not all resident at once.
   const int nkb = (int)(a.K / BK);
   const int tiles128 = p.num_m * (int)ceil_div(a.N, 128), tiles = p.num_m * p.num_n;
+  // split-K partials meet in L2 when the caller's workspace holds them
+  auto part_ws = [&](int t, int ks, int bnt) -> float4* {
+    const size_t need = (size_t)t * ks * BM * bnt * sizeof(float);
+    return a.part_ws && a.part_ws_bytes >= need ? static_cast<float4*>(a.part_ws) : nullptr;
+  };
   if (tiles128 * 2 <= num_sms() && nkb >= 2) {
     const int ks = std::min(4, std::min(num_sms() / tiles128, nkb));
     CUtensorMap tb128;
@@ -1047,6 +1142,7 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
     Params p128 = p;
     p128.num_n = (int)ceil_div(a.N, 128);
     p128.bn = 128;
+    p128.part_g = part_ws(tiles128, ks, 128);
     if (qa) return dispatch_splitk<false, 128, true>(ks, ta, tb128, p128, stream);
     return a.nvfp4 ? dispatch_splitk<true, 128>(ks, ta, tb128, p128, stream)
                    : dispatch_splitk<false, 128>(ks, ta, tb128, p128, stream);
@@ -1054,6 +1150,7 @@ q4_status launch_fp4_gemm(const Fp4GemmArgs& a, cudaStream_t stream) {
   if (tiles * 2 <= num_sms() && nkb >= 2) {
     const int ks = std::min(4, std::min(num_sms() / tiles, nkb));
     if (ks >= 2) {
+      p.part_g = part_ws(tiles, ks, BN);
       if (qa) return dispatch_splitk<false, BN, true>(ks, ta, tb, p, stream);
       return a.nvfp4 ? dispatch_splitk<true, BN>(ks, ta, tb, p, stream)
                      : dispatch_splitk<false, BN>(ks, ta, tb, p, stream);

@@ -2,6 +2,8 @@
 M / N tails, single and many K blocks, more tiles than SMs, both operand paths
 (raw operands quantized on the fly, pre-quantized operands in either scale
 layout) and both output types."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -161,6 +163,31 @@ def test_w4a4_mxfp4_fused_checks(lib):
         lib.gemm_w4a4_mxfp4_fused(ad, Bq, K, ws=small)
     C = lib.gemm_w4a4_mxfp4_fused(ad[:0], Bq, K)
     assert C.shape == (0, N)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("shape", [(256, 2048, 7168), (128, 4096, 8192), (100, 1000, 1024),
+                                   (64, 9000, 512)])
+def test_w4a4_splitk_reductions_agree(lib, fmt, shape):
+    """Few output tiles: split K over a cluster.  With a full workspace the
+    ranks' partial sums meet in it (L2); without one (the C call with ws =
+    NULL) they meet in distributed shared memory.  Both add them in rank order,
+    so the results agree bit for bit."""
+    M, N, K = shape
+    a, b = (_nv_pair if fmt == "nvfp4" else workloads.mxfp4_pair)(M, N, K, seed=M + K)
+    quant = lib.quantize_nvfp4 if fmt == "nvfp4" else lib.quantize_mxfp4
+    qa, qb = quant(torch.from_numpy(a).cuda(), scale_layout="mma"), quant(torch.from_numpy(b).cuda(), scale_layout="mma")
+    A = q4.Fp4Operand(*qa[:2], "mma", qa[2] if fmt == "nvfp4" else None)
+    B = q4.Fp4Operand(*qb[:2], "mma", qb[2] if fmt == "nvfp4" else None)
+    f = lib.gemm_w4a4_nvfp4 if fmt == "nvfp4" else lib.gemm_w4a4_mxfp4
+    C1 = f(A, B, K, out_dtype=torch.float32)  # full workspace
+    C2 = torch.empty_like(C1)
+    oa, ob = q4._operand(A, K)[0], q4._operand(B, K)[0]
+    fn = lib.lib().gemm_w4a4_nvfp4 if fmt == "nvfp4" else lib.lib().gemm_w4a4_mxfp4
+    assert fn(ctypes.byref(oa), ctypes.byref(ob), M, N, K, C2.data_ptr(), q4.F32, None, 0,
+              torch.cuda.current_stream().cuda_stream) == 0
+    assert torch.equal(C1, C2)
+    assert lib.sync_status() == 0
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
