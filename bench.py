@@ -59,11 +59,11 @@ NCU_TRAFFIC = {
     # fp4_gemm_kernel (CTA pairs) at 8192 x 28672 x 8192, mean of 3 launches
     # (231 MB read: A and B once each, scales; 435 MB of C written)
     "prefill": 666.5e6,
-    # split-K fp4_gemm_kernel (128-wide tiles) at 256 x 2048 x 7168, mean of 3
-    # launches (C stays in L2)
-    "moe": 8.82e6,
+    # split-K fp4_gemm_kernel (128-wide tiles, partial sums through L2) at
+    # 256 x 2048 x 7168, mean of 3 launches (C and the partials stay in L2)
+    "moe": 8.83e6,
     # the same with the activation quantization in its prologue (reads raw A)
-    "moe_fused": 11.57e6,
+    "moe_fused": 11.59e6,
     # amax_kernel and nvfp4_kernel, mean per launch over 2 steps (ncu flushes L2
     # before each kernel, so the encode pass's reuse of x from L2 is not in it)
     "quantize": 141.0e6,
