@@ -252,47 +252,77 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
 
-    // ---- stage the present tokens' activations, permuted per fragment.  kSplit
-    // threads share one (group, token): each loads its 16 / kSplit pieces of 16
-    // bytes at once, stores them permuted and sums its values in a fixed
-    // order; the partial sums meet in a fixed shuffle order (deterministic).
-    // Columns of absent tokens are left as they are: their results are never
-    // stored.
+    // ---- stage the present tokens' activations, permuted per fragment, and
+    // 136 * sum of each (group, token) for the INT4 offset.  Columns of absent
+    // tokens are left as they are: their results are never stored.
+    //  * 16-token blocks: one warp load covers 512 contiguous bytes of one
+    //    token's row (two groups): lane l holds 16-byte piece l & 15 of group
+    //    2 * pair + (l >> 4), so every sector fetched is used whole (with one
+    //    thread per 64 bytes, as below, this staging took 1.1 us longer per
+    //    launch).  Warp w takes the (token, group pair) units u * 8 + w, four
+    //    loads in flight per lane; the 16 lanes of a (group, token) add their
+    //    sums in a fixed shuffle order.
+    //  * up to 8 tokens: 4 threads per (group, token), each with 4 pieces of
+    //    16 bytes at once (this measured faster than the warp form at M = 4);
+    //    partial sums meet in a fixed shuffle order.
     if (gi0 == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     else __syncthreads();  // every warp is done with the previous chunk
-    {
-      constexpr int kSplit = kThreads / (kChunk * kTp);  // 4 (TS = 1) or 2 (TS = 2)
-      constexpr int kPer = 16 / kSplit;                   // pieces per thread
-      const int pair = tid / kSplit, part = tid % kSplit;
+    // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}, and
+    // the sum of the eight values in a fixed order
+    auto put = [&](const uint4& x, int gi, int w, int tok, int cq, float& sum) {
+      uint4 v;
+      v.x = __byte_perm(x.x, x.z, 0x5410);
+      v.y = __byte_perm(x.x, x.z, 0x7632);
+      v.z = __byte_perm(x.y, x.w, 0x5410);
+      v.w = __byte_perm(x.y, x.w, 0x7632);
+      act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
+      if constexpr (FMT == kInt4) {
+        const uint32_t e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          sum += __uint_as_float(e[i] << 16) + __uint_as_float(e[i] & 0xFFFF0000u);
+      }
+    };
+    if constexpr (TS == 2) {
+      const int half = lane >> 4, q = lane & 15, cq = q >> 2, w = q & 3;
+#pragma unroll
+      for (int u0 = 0; u0 < 8; u0 += 4) {
+        uint4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (u0 + u) * kWarps + warp, tok = unit >> 2, gi = 2 * (unit & 3) + half;
+          if (tok < mt && gi < gc)
+            x[u] = reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K + (int64_t)(c0 + gi) * 128)[q];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (u0 + u) * kWarps + warp, tok = unit >> 2, gi = 2 * (unit & 3) + half;
+          if (tok >= mt) continue;  // the same for the whole warp
+          float sum = 0.f;
+          if (gi < gc) put(x[u], gi, w, tok, cq, sum);
+          if constexpr (FMT == kInt4) {  // FP4 weights have no offset to remove
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (q == 0 && gi < gc) csum[gi * kTok + tok] = 136.0f * sum;
+          }
+        }
+      }
+    } else {
+      const int pair = tid / 4, part = tid % 4;
       const int gi = pair / kTp, tok = pair % kTp;
       float sum = 0.f;
       if (gi < gc && tok < mt) {
         const uint4* src = reinterpret_cast<const uint4*>(A + (int64_t)(m0 + tok) * K +
-                                                          (int64_t)(c0 + gi) * 128) + part * kPer;
-        uint4 x[kPer];
+                                                          (int64_t)(c0 + gi) * 128) + part * 4;
+        uint4 x[4];
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) x[u] = src[u];
+        for (int u = 0; u < 4; ++u) x[u] = src[u];
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int q = part * kPer + u, cq = q >> 2, w = q & 3;
-          uint4 v;
-          // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}
-          v.x = __byte_perm(x[u].x, x[u].z, 0x5410);
-          v.y = __byte_perm(x[u].x, x[u].z, 0x7632);
-          v.z = __byte_perm(x[u].y, x[u].w, 0x5410);
-          v.w = __byte_perm(x[u].y, x[u].w, 0x7632);
-          act[((gi * 4 + w) * kTp + tok) * 4 + cq] = v;
-          if constexpr (FMT == kInt4) {
-            const uint32_t e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              sum += __uint_as_float(e[i] << 16) + __uint_as_float(e[i] & 0xFFFF0000u);
-          }
-        }
+        for (int u = 0; u < 4; ++u) put(x[u], gi, u, tok, part, sum);  // piece 4 part + u
       }
-      if constexpr (FMT == kInt4) {  // FP4 weights have no offset to remove
-#pragma unroll
-        for (int o = 1; o < kSplit; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if constexpr (FMT == kInt4) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         if (part == 0 && gi < gc && tok < mt) csum[gi * kTok + tok] = 136.0f * sum;
       }
     }
