@@ -77,6 +77,32 @@ NCU_TRAFFIC = {
 }
 
 
+def read_probe_rate(q4, dev, nbytes: float) -> float:
+    """GB/s of q4_read_probe streaming `nbytes` per launch, launches back to
+    back in a CUDA graph over rotating buffers (> 2 x L2 in total)."""
+    nbytes = max(16, int(nbytes) // 16 * 16)
+    nbuf = max(2, -(-300_000_000 // nbytes))
+    bufs = [torch.ones(nbytes, dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+    sink = torch.zeros(int(q4.lib().q4_read_probe_sink_words()), dtype=torch.int32, device=dev)
+    inner = nbuf * -(-30 // nbuf)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(inner):
+            q4.read_probe(bufs[i % nbuf], sink)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(3, -(-300 // inner))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    del bufs
+    return nbytes * inner * reps / t / 1e9
+
+
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -206,6 +232,7 @@ class Decode:
     Ms = (1, 4, 16)
     copies = 8  # 8 x 34.6 MB of weights rotate, > 2 x L2
     kernel = "w4a16_kernel"
+    read_probe = True
 
     def config(self):
         return {"workload": "w4a16_decode N=K=8192 INT4-g128 weights, bf16 A, M=1,4,16 per step",
@@ -551,6 +578,7 @@ class Moe(W4A4):
     kernel = "fp4_gemm_kernel"
     nvfp4 = False
     launches_per_step = 2  # activation quantizer + GEMM
+    read_probe = True
 
     def config(self):
         return {"workload": f"mxfp4_moe A bf16 {self.M}x{self.K} (0.5% channels x20, quantized on the fly), B MXFP4 {self.N}x{self.K}",
@@ -1092,6 +1120,16 @@ def main():
                 "peak_source": (f"{src} (hbm_gbs)" if punit == "GB/s" else
                                 lib_src if lib_src.startswith("measured") else
                                 f"{src} ({peak_text(wl)}); {lib_src}")}
+
+    if wl.bound == "hbm" and getattr(wl, "read_probe", False):
+        # context for the fraction: a bare read of the same bytes per launch
+        nb = per_launch
+        rp = read_probe_rate(q4, dev, nb)
+        roofline["read_probe"] = {
+            "gbs": rp, "bytes_per_launch": int(nb), "frac_of_peak": rp / peak,
+            "kernel_over_probe": achieved / rp,
+            "what": "the library's bare 16-byte-load read (q4_read_probe) of the same bytes per "
+                    "launch, launches back to back in a CUDA graph over rotating buffers > 2 x L2"}
 
     # end to end through the public API: host buffers, copies inside the timed region
     n_e2e = min(K, 2000 if wl.unit == "GB/s" else 50)

@@ -408,6 +408,19 @@ int q4_set_wait_timeout_ms(int ms);
  * without faulting or hanging the GPU. */
 q4_status q4_selftest_wait_timeout(q4_stream_t stream);
 
+/*
+ * Measurement aid (not a step of the method): read-bandwidth probe.  Streams
+ * `bytes` from src once with 16-byte loads (8 CTAs of 256 threads per SM,
+ * four loads in flight per thread) and XORs what it reads into sink[0 ..
+ * q4_read_probe_sink_words()) so that the loads are kept.  Timed over the
+ * same bytes per launch and launch pattern as an HBM-bound kernel, it gives
+ * the rate a bare read of that size reaches.  src: device, 16-byte aligned;
+ * bytes % 16 == 0 (0: no-op); sink: device, 4-byte aligned, written with
+ * atomic XOR (contents meaningless).  Q4_ERR_INVALID_ARG otherwise.
+ */
+size_t q4_read_probe_sink_words(void);
+q4_status q4_read_probe(const void* src, size_t bytes, unsigned* sink, q4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

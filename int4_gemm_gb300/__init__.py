@@ -88,6 +88,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     _sig(lib, "q4_status_string", ctypes.c_char_p, I)
     _sig(lib, "q4_set_wait_timeout_ms", I, I)
     _sig(lib, "q4_selftest_wait_timeout", I, P)
+    _sig(lib, "q4_read_probe_sink_words", SZ)
+    _sig(lib, "q4_read_probe", I, P, SZ, P, P)
     _sig(lib, "gemm_w4a4_nvfp4_noalloc", I, P, I, op, I64, I64, I64, P, I, P)
     _sig(lib, "q4_noalloc_scratch_bytes", SZ)
     _sig(lib, "q4_noalloc_required_bytes", SZ, I64, I64)
@@ -444,3 +446,15 @@ def sync_status(stream=None) -> int:
 
 def set_wait_timeout_ms(ms: int) -> int:
     return int(lib().q4_set_wait_timeout_ms(ms))
+
+
+def read_probe(src: torch.Tensor, sink: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Measurement aid: one bare streaming read of ``src`` (q4_read_probe).
+    Returns the sink (int32 words, contents meaningless)."""
+    if not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    if sink is None:
+        sink = torch.zeros(int(lib().q4_read_probe_sink_words()), dtype=torch.int32, device=src.device)
+    _check("q4_read_probe", lib().q4_read_probe(src.data_ptr(), src.numel() * src.element_size(),
+                                                sink.data_ptr(), _stream(stream)))
+    return sink

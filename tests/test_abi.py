@@ -94,6 +94,12 @@ def test_host_argument_checks(clib):
     # an unknown rounding mode
     assert clib.quantize_mxfp4_ex(fake, 1, 4, 64, fake, fake, 0, 2, None) == -1
     assert clib.quantize_nvfp4_ex(fake, 1, 4, 64, fake, fake, 0, -1, fake, fake, 256, None) == -1
+    # the read probe: 16-byte aligned source, whole 16-byte words, a sink
+    assert clib.q4_read_probe(None, 16, fake, None) == -1
+    assert clib.q4_read_probe(fake + 1, 16, fake, None) == -1
+    assert clib.q4_read_probe(fake, 17, fake, None) == -1
+    assert clib.q4_read_probe(fake, 16, None, None) == -1
+    assert clib.q4_read_probe(fake, 0, None, None) == 0
     # empty problems are no-ops
     assert clib.quantize_int4_g128(None, 1, 0, 128, None, None, None) == 0
     assert clib.gemm_w4a16_int4(None, None, None, 0, 4, 128, None, None, 0, None) == 0

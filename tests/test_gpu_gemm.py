@@ -426,3 +426,15 @@ def test_grouped_moe(lib, case, layout):
     R = oracle.grouped_gemm_moe(tok.float().numpy(), offs, rt, [oracle.quantize_nvfp4(w) for w in ws])
     assert_gemm_close(C.float().cpu().numpy(), R)
     assert lib.sync_status() == 0
+
+
+def test_read_probe_reads_every_word_once(lib):
+    """The bandwidth probe folds what it reads into its sink with XOR: the XOR
+    of the sink words equals the XOR of every 32-bit word of the source, so
+    each word was read exactly once (sizes off the grid's stride included)."""
+    for n in (16, 4096 + 16, 34_603_008, 8_830_000 // 16 * 16):
+        src = torch.randint(-2**31, 2**31 - 1, (n // 4,), dtype=torch.int32, device="cuda")
+        sink = lib.read_probe(src)
+        want = np.bitwise_xor.reduce(src.cpu().numpy().view(np.uint32))
+        got = np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))
+        assert got == want
