@@ -297,28 +297,56 @@ def test_w4a16_fp4_weights(lib, shape, fmt):
     assert lib.sync_status() == 0
 
 
+@pytest.mark.parametrize("c", [1.0, 3.0e-7, 3.0e5])
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
-def test_w4a16_fp4_identity_activations_give_the_weights(lib, fmt):
-    """A = I (and a tensor scale of 1): every output is one dequantized weight,
-    e2m1 x block scale, which bf16 holds exactly -- so the output must equal
-    the oracle's dequantization bit for bit, for every code (the subnormal
-    0.5 included) and scale met."""
+def test_w4a16_fp4_identity_activations_give_the_weights(lib, fmt, c):
+    """A = c I (and a tensor scale of 1): every output is one dequantized
+    weight, e2m1 x block scale, times c -- at most 14 significant bits, so
+    FP32 holds it and the only rounding is the store to bf16.  The output must
+    equal the oracle's, bit for bit, for every code (the subnormal 0.5
+    included) and scale met, with activations of ordinary size and ones far
+    outside the f16 range (3e-7, 3e5)."""
     K, N = 256, 384
     w = workloads.normal(workloads.rng_for(31, 2), (N, K), 0.02)
     w[5, 3:40] *= 300.0  # large blocks next to small ones in the same rows
     w[9, 100:140] *= 1e-3
     q, oq = _fp4_weights(lib, w, fmt)
-    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    cb = torch.tensor(c, dtype=torch.bfloat16)
+    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda") * cb.cuda()
     for m0 in range(0, K, 128):
         A = eye[m0:m0 + 128].contiguous()
         if fmt == "nvfp4":
             one = torch.ones(1, dtype=torch.float32, device="cuda")
             C = lib.gemm_w4a16_nvfp4(A, q[0], q[1], one)
-            want = oracle.dequantize_nvfp4(oq[0], oq[1], np.float32(1.0))[:, m0:m0 + 128].T
+            deq = oracle.dequantize_nvfp4(oq[0], oq[1], np.float32(1.0))[:, m0:m0 + 128].T
         else:
             C = lib.gemm_w4a16_mxfp4(A, *q)
-            want = oracle.dequantize_mxfp4(*oq)[:, m0:m0 + 128].T
-        assert np.array_equal(C.float().cpu().numpy(), want.astype(np.float32))
+            deq = oracle.dequantize_mxfp4(*oq)[:, m0:m0 + 128].T
+        exact = deq.astype(np.float64) * float(cb)
+        assert np.array_equal(exact.astype(np.float32).astype(np.float64), exact)
+        want = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16)
+        assert torch.equal(C.cpu(), want)
+    assert lib.sync_status() == 0
+
+
+@pytest.mark.parametrize("M", [4, 16])
+def test_w4a16_nvfp4_activations_outside_f16_range(lib, M):
+    """Activations that f16 could not hold (above 65504, or below 2^-17 in
+    magnitude where f16 would round them) next to ordinary ones, in groups of
+    both CTAs of the K split: the products stay exact (bf16 x bf16 in the
+    MMA) and the output agrees with the oracle."""
+    N, K = 512, 2048  # 16 groups, 8 per CTA
+    A, w = workloads.decode(M, seed=77 + M, N=N, K=K)
+    a = A.float()
+    a[0, 130] = 3.0e5      # group 1: above 65504
+    a[M - 1, 700] = -7.0e4  # group 5
+    a[1, 1500] = 3.0e-7    # group 11 (the second CTA's fourth): f16 would round it
+    a[2, 1900] = 2.0 ** -20  # group 14: an f16 subnormal power of two, exact
+    A = a.to(torch.bfloat16)
+    q, oq = _fp4_weights(lib, w, "nvfp4")
+    C = lib.gemm_w4a16_nvfp4(A.cuda(), *q)
+    R = oracle.gemm_w4a16_nvfp4(A.float().numpy(), *oq)
+    assert_gemm_close(C.float().cpu().numpy(), R)
     assert lib.sync_status() == 0
 
 
