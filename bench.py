@@ -53,8 +53,9 @@ NCU_TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
     # kernel of the current code, at the bench's own sizes:
     # w4a16_kernel, mean over the M = 1, 4, 16 launches at N = K = 8192
+    # (captured again after the 16-token staging change: 34.66 / 34.71 / 34.92 MB)
     "decode": 34.76e6,
-    # w4a16_kernel<NVFP4>, mean over the M = 1, 4, 16 launches at N = K = 8192
+    # w4a16_kernel<NVFP4>, the same (37.84 / 37.89 / 38.09 MB)
     "decode_nvfp4": 37.94e6,
     # fp4_gemm_kernel (CTA pairs) at 8192 x 28672 x 8192, mean of 3 launches
     # (231 MB read: A and B once each, scales; 435 MB of C written)
