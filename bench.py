@@ -55,8 +55,8 @@ NCU_TRAFFIC = {
     # w4a16_kernel, mean over the M = 1, 4, 16 launches at N = K = 8192
     # (captured again after the 16-token staging change: 34.66 / 34.71 / 34.92 MB)
     "decode": 34.76e6,
-    # w4a16_kernel<NVFP4>, the same (37.84 / 37.89 / 38.09 MB)
-    "decode_nvfp4": 37.94e6,
+    # w4a16_kernel<NVFP4> (f16 form), the same (37.80 / 37.85 / 38.05 MB)
+    "decode_nvfp4": 37.90e6,
     # fp4_gemm_kernel (CTA pairs) at 8192 x 28672 x 8192, mean of 3 launches
     # (231 MB read: A and B once each, scales; 435 MB of C written)
     "prefill": 666.5e6,

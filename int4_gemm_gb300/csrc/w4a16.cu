@@ -16,6 +16,11 @@
 //    one as soon as its own weight loads are issued.
 //  * Nibbles become exact bf16 integers with one LOP3 (mask, flip the sign
 //    bit, OR the exponent of 128) and one bf16x2 subtraction of 136.
+//  * NVFP4 weights: the hardware E2M1 convert gives f16 code pairs, one f16
+//    multiply applies the block scale (exact), and the MMAs run in f16 on
+//    f16 activations, for every group of 128 columns whose activations are
+//    all f16 values; other groups (a value below 2^-17 or above 65504) use
+//    bf16 weights built bit by bit, also exact.
 //  * The products q * a are exact in the MMA and are summed in FP32; the FP16
 //    group scale is applied once per group of 128 in FP32 (per-group
 //    promotion), so the only rounding to bf16 is the final store.
@@ -91,6 +96,34 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
+// The four E2M1 code pairs of a 32-bit word (byte j = codes 2j, 2j + 1, the
+// first in the low nibble) as f16x2 values, the first in the low half: the
+// hardware convert, exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// f16x2 of (lo, hi); exact when both are f16 values
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// The bf16 value in f16 without rounding (zero, infinities and NaN included)?
+__device__ __forceinline__ bool f16_exact(float v) {
+  return __half2float(__float2half_rn(v)) == v || v != v;
+}
+
 // Scale bytes -> float (exact; finite encodings only).  E4M3: bias 7, three
 // mantissa bits, subnormals m * 2^-9.  E8M0: 2^(b - 127), byte 0 = 2^-127.
 __device__ __forceinline__ float e4m3_value(uint32_t b) {
@@ -125,6 +158,20 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&a)[4], int i) {
+  return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3];
 }
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
@@ -196,6 +243,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   // 16-byte scale loads need 8 groups per row and a 16-byte aligned Ws (the
   // interface only asks for 2-byte alignment)
   const bool s16 = (ngroups & 7) == 0 && (reinterpret_cast<uintptr_t>(Ws) & 15) == 0;
+
+  if constexpr (FMT == kNvfp4) {  // the group mask of the f16 form starts clear
+    if (tid == 0) *reinterpret_cast<unsigned*>(csum) = 0u;
+    __syncthreads();
+  }
 
   float acc[2][TS][4];  // [tile][token set][fragment]
 #pragma unroll
@@ -269,7 +321,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     else __syncthreads();  // every warp is done with the previous chunk
     // {x0,x1 | x2,x3 | x4,x5 | x6,x7} -> {x0,x4 | x1,x5 | x2,x6 | x3,x7}, and
     // the sum of the eight values in a fixed order
+    bool exact = true;  // NVFP4: every activation this thread staged is an f16 value
     auto put = [&](const uint4& x, int gi, int w, int tok, int cq, float& sum) {
+      if constexpr (FMT == kNvfp4) {
+        const uint32_t e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          exact = exact && f16_exact(__uint_as_float(e[i] << 16)) &&
+                  f16_exact(__uint_as_float(e[i] & 0xFFFF0000u));
+      }
       uint4 v;
       v.x = __byte_perm(x.x, x.z, 0x5410);
       v.y = __byte_perm(x.x, x.z, 0x7632);
@@ -326,10 +386,39 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (part == 0 && gi < gc && tok < mt) csum[gi * kTok + tok] = 136.0f * sum;
       }
     }
-    __syncthreads();
+    // NVFP4, per group of the chunk: when every staged activation of the
+    // group is an f16 value, its MMAs run in f16 (the weights come from the
+    // hardware E2M1 convert, see below) and its staged slots become f16 pairs
+    // in natural order, in place (each 16-byte slot holds the same eight
+    // columns in either form); a group with any other value (below 2^-17 in
+    // magnitude or above 65504, about 1 in 10^5 of N(0, 1) data) keeps the
+    // bf16 form.  Every thread staged values of one group only, so one bit per
+    // thread marks the groups that stay bf16.
+    unsigned bf16_groups = 0u;
+    if constexpr (FMT == kNvfp4) {
+      unsigned* s_bad = reinterpret_cast<unsigned*>(csum);  // NVFP4 has no offset sums
+      const int my_gi = TS == 2 ? 2 * (warp & 3) + (lane >> 4) : (tid / 4) / kTp;
+      const unsigned m = __reduce_or_sync(0xffffffffu, exact ? 0u : 1u << (my_gi & 31));
+      if (lane == 0 && m) atomicOr(s_bad, m);
+      __syncthreads();
+      bf16_groups = *s_bad;
+      for (int e = tid; e < kChunk * 4 * kTp * 4; e += kThreads) {
+        if ((bf16_groups >> (e / (4 * kTp * 4))) & 1u) continue;
+        const uint4 v = act[e];  // {x0,x4 | x1,x5 | x2,x6 | x3,x7} in bf16
+        uint4 h;
+        h.x = f16x2_of(__uint_as_float(v.x << 16), __uint_as_float(v.y << 16));
+        h.y = f16x2_of(__uint_as_float(v.z << 16), __uint_as_float(v.w << 16));
+        h.z = f16x2_of(__uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y & 0xFFFF0000u));
+        h.w = f16x2_of(__uint_as_float(v.z & 0xFFFF0000u), __uint_as_float(v.w & 0xFFFF0000u));
+        act[e] = h;  // {x0,x1 | x2,x3 | x4,x5 | x6,x7} in f16
+      }
+      __syncthreads();  // every thread has read the mask: the next chunk may set it again
+      if (tid == 0) *s_bad = 0u;
+    } else {
+      __syncthreads();
+    }
 
-#pragma unroll
-    for (int gl = 0; gl < kChunk; ++gl) {
+    auto group = [&](int gl) {
       if (gl < gc) {
         const int gi = gi0 + gl;
         cp_async_wait<kRing - 1>();  // this thread's copies of group gi have landed
@@ -338,6 +427,49 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           wv[i] = *reinterpret_cast<const uint4*>(ring + ((slot * 4 + i) * kThreads + tid) * 16);
+        if constexpr (FMT == kNvfp4) {
+          if (!((bf16_groups >> gl) & 1u)) {
+            // NVFP4, f16 form: code pairs (2j, 2j + 1) by the hardware convert,
+            // times the E4M3 scale x 2^-10 in f16 -- exact, subnormals included
+            // (at most 6 significant bits, multiples of 2^-20 up to 2.625) --
+            // against f16 activations in natural order.  The 2^10 goes back
+            // with the tensor scale, as in the bf16 form.
+            uint32_t s16[4][2];  // [row][half of this thread's 32 columns]
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const uint32_t b2 = (pick4(spk[r], gl >> 1) >> ((gl & 1) * 16)) & 0xFFFFu;
+              const float lo = e4m3_value(b2 & 0xFFu) * 0x1p-10f, hi = e4m3_value(b2 >> 8) * 0x1p-10f;
+              s16[r][0] = f16x2_of(lo, lo);
+              s16[r][1] = f16x2_of(hi, hi);
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint4 bf[TS];
+#pragma unroll
+              for (int s = 0; s < TS; ++s) bf[s] = act[((gl * 4 + w) * kTp + lrow + 8 * s) * 4 + quad];
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                uint32_t pl[4], ph[4];
+                e2m1x8_to_f16x2(word(wv[2 * t], w), pl);
+                e2m1x8_to_f16x2(word(wv[2 * t + 1], w), ph);
+                const uint32_t sl = s16[2 * t][w >> 1], sh = s16[2 * t + 1][w >> 1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  pl[j] = f16x2_mul(pl[j], sl);
+                  ph[j] = f16x2_mul(ph[j], sh);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int s = 0; s < TS; ++s)
+                    mma_f16_16816(acc[t][s], pl[2 * h], ph[2 * h], pl[2 * h + 1], ph[2 * h + 1],
+                                  h ? bf[s].z : bf[s].x, h ? bf[s].w : bf[s].y);
+              }
+            }
+            issue(gi + kRing);  // refill the slot just read
+            return;
+          }
+        }
         if constexpr (FMT != kInt4) {
           // FP4: the block scale is folded into each weight, exactly in bf16
           // (e2m1 x E4M3 has at most 6 significant bits; e2m1 x 2^e is exact
@@ -351,16 +483,15 @@ __global__ void __launch_bounds__(kThreads, 2)
               // E4M3 scale x 2^116 (exact, normal: 2^107 .. 448 * 2^116), so
               // that one multiply gives code * scale * 2^-10; the 2^10 goes
               // back with the tensor scale
-              const uint32_t b2 = (spk[r][gl >> 1] >> ((gl & 1) * 16)) & 0xFFFFu;
+              const uint32_t b2 = (pick4(spk[r], gl >> 1) >> ((gl & 1) * 16)) & 0xFFFFu;
               s2[r][0] = bf16x2_splat(e4m3_value(b2 & 0xFFu) * 0x1p116f);
               s2[r][1] = bf16x2_splat(e4m3_value(b2 >> 8) * 0x1p116f);
             } else {
-              s2[r][0] = s2[r][1] = bf16x2_splat(e8m0_value((spk[r][gl >> 2] >> ((gl & 3) * 8)) & 0xFFu));
+              s2[r][0] = s2[r][1] = bf16x2_splat(e8m0_value((pick4(spk[r], gl >> 2) >> ((gl & 3) * 8)) & 0xFFu));
             }
           }
           constexpr uint32_t kTwo126 = 0x7E807E80u;  // bf16x2 of 2^126
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
+          auto fp4_word = [&](int w) {
             uint4 bf[TS];
 #pragma unroll
             for (int s = 0; s < TS; ++s) bf[s] = act[((gl * 4 + w) * kTp + lrow + 8 * s) * 4 + quad];
@@ -368,7 +499,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int t = 0; t < 2; ++t) {
               const uint32_t lo = word(wv[2 * t], w), hi = word(wv[2 * t + 1], w);
               const uint32_t ls = lo & 0x88888888u, hs = hi & 0x88888888u;
-              const uint32_t sl = s2[2 * t][w >> 1], sh = s2[2 * t + 1][w >> 1];
+              const uint32_t sl = (w >> 1) ? s2[2 * t][1] : s2[2 * t][0];
+              const uint32_t sh = (w >> 1) ? s2[2 * t + 1][1] : s2[2 * t + 1][0];
               uint32_t pl[4], ph[4];
               if constexpr (FMT == kNvfp4) {  // code * 2^-126 times scale * 2^116
                 pl[0] = bf16x2_mul(e2m1_pair_bits<0>(lo, ls), sl);
@@ -396,9 +528,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                   mma_bf16_16816(acc[t][s], pl[2 * h], ph[2 * h], pl[2 * h + 1], ph[2 * h + 1],
                                  h ? bf[s].z : bf[s].x, h ? bf[s].w : bf[s].y);
             }
+          };
+          if constexpr (FMT == kNvfp4) {  // the rare bf16 form: kept short, one word at a time
+#pragma unroll 1
+            for (int w = 0; w < 4; ++w) fp4_word(w);
+          } else {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) fp4_word(w);
           }
           issue(gi + kRing);  // refill the slot just read
-          continue;
+          return;
         }
         float part[2][TS][4];
 #pragma unroll
@@ -445,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const uint32_t plo = spk[2 * t][gl >> 1], phi = spk[2 * t + 1][gl >> 1];
+          const uint32_t plo = pick4(spk[2 * t], gl >> 1), phi = pick4(spk[2 * t + 1], gl >> 1);
           const float slo = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? plo >> 16 : plo)));
           const float shi = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? phi >> 16 : phi)));
 #pragma unroll
@@ -458,6 +597,17 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
+    };
+    // NVFP4 keeps one copy of the group code (it holds two forms): with the
+    // eight groups unrolled, launches of the 8- and 16-token kernels in turn
+    // ran 10% slower than either alone (51.6 against 47.3 us per step of
+    // three launches rolled).
+    if constexpr (FMT == kNvfp4) {
+#pragma unroll 1
+      for (int gl = 0; gl < kChunk; ++gl) group(gl);
+    } else {
+#pragma unroll
+      for (int gl = 0; gl < kChunk; ++gl) group(gl);
     }
   }
   cp_async_wait<0>();  // no copy may still target this CTA's shared memory at exit
@@ -581,3 +731,4 @@ q4_status launch_w4a16_fp4(const void* A, const uint8_t* Wq, const uint8_t* Wsf,
 }
 
 }  // namespace q4
+
