@@ -537,63 +537,63 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int w = 0; w < 4; ++w) fp4_word(w);
           }
           issue(gi + kRing);  // refill the slot just read
-          return;
-        }
-        float part[2][TS][4];
+        } else {  // INT4: per-group promotion of the MMA sums
+          float part[2][TS][4];
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int s = 0; s < TS; ++s)
+            for (int s = 0; s < TS; ++s)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) part[t][s][i] = 0.f;
+              for (int i = 0; i < 4; ++i) part[t][s][i] = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint4 bf[TS];
+          for (int w = 0; w < 4; ++w) {
+            uint4 bf[TS];
 #pragma unroll
-          for (int s = 0; s < TS; ++s) bf[s] = act[((gl * 4 + w) * kTp + lrow + 8 * s) * 4 + quad];
+            for (int s = 0; s < TS; ++s) bf[s] = act[((gl * 4 + w) * kTp + lrow + 8 * s) * 4 + quad];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              // nibble pairs (i, i + 4) of the row's word sit at bits 4i.. and 16 + 4i..
+              const uint32_t lo = word(wv[2 * t], w), hi = word(wv[2 * t + 1], w);
+              uint32_t pl[4], ph[4];
+              pl[0] = nib_pair_to_bf16x2(lo);
+              pl[1] = nib_pair_to_bf16x2(lo >> 4);
+              pl[2] = nib_pair_to_bf16x2(lo >> 8);
+              pl[3] = nib_pair_to_bf16x2(lo >> 12);
+              ph[0] = nib_pair_to_bf16x2(hi);
+              ph[1] = nib_pair_to_bf16x2(hi >> 4);
+              ph[2] = nib_pair_to_bf16x2(hi >> 8);
+              ph[3] = nib_pair_to_bf16x2(hi >> 12);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int s = 0; s < TS; ++s)
+                  mma_bf16_16816(part[t][s], pl[2 * h], ph[2 * h], pl[2 * h + 1], ph[2 * h + 1],
+                                 h ? bf[s].z : bf[s].x, h ? bf[s].w : bf[s].y);
+            }
+          }
+          issue(gi + kRing);  // refill the slot just read (the registers hold its data)
+          // per-group promotion: remove the offset, then one FP32 multiply by the
+          // FP16 scale of each row
+          float c0v[TS], c1v[TS];
+#pragma unroll
+          for (int s = 0; s < TS; ++s) {
+            const float2 cc = *reinterpret_cast<const float2*>(&csum[gl * kTok + s * 8 + 2 * quad]);
+            c0v[s] = cc.x;
+            c1v[s] = cc.y;
+          }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            // nibble pairs (i, i + 4) of the row's word sit at bits 4i.. and 16 + 4i..
-            const uint32_t lo = word(wv[2 * t], w), hi = word(wv[2 * t + 1], w);
-            uint32_t pl[4], ph[4];
-            pl[0] = nib_pair_to_bf16x2(lo);
-            pl[1] = nib_pair_to_bf16x2(lo >> 4);
-            pl[2] = nib_pair_to_bf16x2(lo >> 8);
-            pl[3] = nib_pair_to_bf16x2(lo >> 12);
-            ph[0] = nib_pair_to_bf16x2(hi);
-            ph[1] = nib_pair_to_bf16x2(hi >> 4);
-            ph[2] = nib_pair_to_bf16x2(hi >> 8);
-            ph[3] = nib_pair_to_bf16x2(hi >> 12);
+            const uint32_t plo = pick4(spk[2 * t], gl >> 1), phi = pick4(spk[2 * t + 1], gl >> 1);
+            const float slo = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? plo >> 16 : plo)));
+            const float shi = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? phi >> 16 : phi)));
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int s = 0; s < TS; ++s)
-                mma_bf16_16816(part[t][s], pl[2 * h], ph[2 * h], pl[2 * h + 1], ph[2 * h + 1],
-                               h ? bf[s].z : bf[s].x, h ? bf[s].w : bf[s].y);
-          }
-        }
-        issue(gi + kRing);  // refill the slot just read (the registers hold its data)
-        // per-group promotion: remove the offset, then one FP32 multiply by the
-        // FP16 scale of each row
-        float c0v[TS], c1v[TS];
-#pragma unroll
-        for (int s = 0; s < TS; ++s) {
-          const float2 cc = *reinterpret_cast<const float2*>(&csum[gl * kTok + s * 8 + 2 * quad]);
-          c0v[s] = cc.x;
-          c1v[s] = cc.y;
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t plo = pick4(spk[2 * t], gl >> 1), phi = pick4(spk[2 * t + 1], gl >> 1);
-          const float slo = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? plo >> 16 : plo)));
-          const float shi = __half2float(__ushort_as_half((uint16_t)((gl & 1) ? phi >> 16 : phi)));
-#pragma unroll
-          for (int s = 0; s < TS; ++s) {  // pairs of tokens per instruction, same rounding
-            float d0, d1, d2, d3;
-            sub2(d0, d1, part[t][s][0], part[t][s][1], c0v[s], c1v[s]);
-            sub2(d2, d3, part[t][s][2], part[t][s][3], c0v[s], c1v[s]);
-            fma2(acc[t][s][0], acc[t][s][1], d0, d1, slo, slo);
-            fma2(acc[t][s][2], acc[t][s][3], d2, d3, shi, shi);
+            for (int s = 0; s < TS; ++s) {  // pairs of tokens per instruction, same rounding
+              float d0, d1, d2, d3;
+              sub2(d0, d1, part[t][s][0], part[t][s][1], c0v[s], c1v[s]);
+              sub2(d2, d3, part[t][s][2], part[t][s][3], c0v[s], c1v[s]);
+              fma2(acc[t][s][0], acc[t][s][1], d0, d1, slo, slo);
+              fma2(acc[t][s][2], acc[t][s][3], d2, d3, shi, shi);
+            }
           }
         }
       }
