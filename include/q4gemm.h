@@ -263,9 +263,9 @@ q4_status gemm_w4a16_int4(const void* A_bf16, const uint8_t* Wq, const uint16_t*
  * product with an activation is exact; the sums are FP32, g is applied once
  * in FP32, and the only rounding to bf16 is the final store.  NVFP4 weights
  * meet the activations in f16 (weights x 2^-10, exact) for every group of
- * 128 columns whose activations are all f16 values (bf16 values from 2^-17
- * to 65504 in magnitude, zero, infinities, NaN), in bf16 otherwise: the
- * same exact products either way.
+ * 128 columns whose activations are all f16 values (every bf16 value from
+ * 2^-17 to 65504 in magnitude is one, as are zero and the infinities; NaN
+ * stays NaN), in bf16 otherwise: the same exact products either way.
  * K % 128 == 0; any M >= 0 (tuned for M <= 16).  Alignment: A, Wq 16 bytes;
  * NVFP4 Ws 2 bytes, w_tensor_scale 4 bytes.  ws/ws_bytes as for
  * gemm_w4a16_int4 (q4_workspace_size(Q4_OP_GEMM_W4A16_NVFP4 or _MXFP4, ...)
